@@ -1,0 +1,431 @@
+"""Benchmark of the FP4 MoE decode layer on GB300.
+
+Metric: microseconds per MoE layer (and the weight-stream GB/s it implies, as a
+fraction of the measured HBM bandwidth) on the NVFP4 MTP decode workload:
+T=4 token rows, E=256 experts, top-8, hidden 2048, intermediate 512, SwiGLU.
+
+A step is one decode step of a 40-layer model: 40 calls of
+qmoe_fp4_moe_forward (routing -> permute -> FC1 GEMV + SwiGLU -> FC2 GEMV ->
+weighted un-permute), each on its own layer's weights (17 GB in total, far
+larger than the 129 MB L2), replayed as one CUDA graph.  Inputs are seeded
+synthetic data with the workload's shapes and distributions.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the plain CPU oracle (the reference arm of this
+project) on a bounded sample of the same workload, on the host's cores.
+Multi-GPU runs are independent replicas (the layer has no cross-GPU step
+here): one process per GPU under torchrun, max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "nvfp4_mtp_decode"
+LAYERS = 40
+METRIC = "us per MoE layer (NVFP4 MTP decode, T=4 E=256 top-8 H=2048 I=512)"
+UNIT = "us/layer"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(per_rank_seconds: float, layers_per_rank: int, world: int) -> dict:
+    """Replica aggregation: the job's time is the slowest rank's; the job
+    processed layers_per_rank * world layers in it."""
+    t = reduce_max(per_rank_seconds, world)
+    total_layers = layers_per_rank * world
+    return dict(seconds=t, total_layers=total_layers, us_per_layer=t * 1e6 / total_layers)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) with host
+    timestamps, so the ones inside the timed region can be picked."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 6:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "inside timed region"
+        if not inside and self.samples:
+            nearest = min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
+            inside, note = [nearest[1]], "nearest sample (timed region shorter than the 50 ms period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[2 + i].lower() == "active"})
+        sm = [float(p[0]) for p in inside if p[0].replace(".", "").isdigit()]
+        mx = [float(p[1]) for p in inside if p[1].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------- workload
+
+def make_layers(n_layers: int, seed: int, device):
+    """Seeded synthetic layers of the decode workload, generated on the GPU
+    (weights) and with the shared host generator (activations, logits)."""
+    import numpy as np
+    import torch
+    import synthetic as syn
+    wl = syn.WORKLOADS[WORKLOAD]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    layers = []
+    E, H, I = wl.E, wl.H, wl.I
+
+    def e4m3_codes(shape):
+        idx = torch.randint(0, 32, shape, generator=gen, device=device, dtype=torch.int32)
+        return (((idx // 8) + 5) << 3 | (idx % 8)).to(torch.uint8)
+
+    def gscale():
+        u = torch.randint(0, 5, (E,), generator=gen, device=device, dtype=torch.int32)
+        return torch.ldexp(torch.ones(E, device=device), -u.float()).float()
+
+    for li in range(n_layers):
+        rng = syn.rng_for(seed, 100 + li)
+        x = torch.from_numpy(syn.activations(rng, wl.T, H).view(np.int16)).to(device).view(torch.bfloat16)
+        lg = torch.from_numpy(syn.logits(rng, wl.T, E, wl.logit_std)).to(device)
+        w1 = torch.randint(0, 256, (E, H, I), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+        w2 = torch.randint(0, 256, (E, I, H // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+        layers.append(dict(x=x, logits=lg, w1=w1, s1=e4m3_codes((E, 2 * I, H // 16)), g1=gscale(),
+                           w2=w2, s2=e4m3_codes((E, H, I // 16)), g2=gscale()))
+    return wl, layers
+
+
+def per_expert_bytes(wl):
+    bs = 16 if wl.fmt == 0 else 32
+    fc1 = wl.H * wl.I + 2 * wl.I * (wl.H // bs)
+    fc2 = wl.I * (wl.H // 2) + wl.H * (wl.I // bs)
+    return fc1, fc2
+
+
+def run_gpu(args):
+    import torch
+    import block_scaled_fp4_gb300 as q
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    q.build()
+    q.load()
+    wl, layers = make_layers(LAYERS, seed=1234 + rank, device=device)
+    ws_bytes = q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, wl.fmt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
+    ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=device) for _ in layers]
+    stream = torch.cuda.Stream(device=device)
+
+    def step(lst=layers):
+        for i, L in enumerate(lst):
+            q.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
+                          wl.fmt, wl.k, wl.normalize, out=outs[i], topk_ids=ids[i], workspace=ws)
+
+    # --- graph capture of one step (40 layers)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+
+    fc1_b, fc2_b = per_expert_bytes(wl)
+    act = [len(set(i.cpu().numpy().reshape(-1).tolist())) for i in ids]
+    alg_bytes_layer = [a * (fc1_b + fc2_b) + wl.T * wl.H * 2 * 2 + wl.T * wl.E * 4 for a in act]
+    mean_alg = sum(alg_bytes_layer) / len(alg_bytes_layer)
+
+    clocks = ClockSampler(device.index or 0)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(world)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    clocks.stop()
+    agg = aggregate(sec, args.steps * LAYERS, world)
+    us_layer = agg["us_per_layer"]
+
+    # --- eager (no graph) timing of the same steps, for reference
+    with torch.cuda.stream(stream):
+        step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n_eager = max(1, min(args.steps, 50))
+        for _ in range(n_eager):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    eager_us = e0.elapsed_time(e1) * 1e3 / (n_eager * LAYERS)
+
+    # --- per-kernel durations (stage events around each kernel, eager)
+    n_inst = max(1, min(args.steps, 20))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_inst * LAYERS)]
+    with torch.cuda.stream(stream):
+        for j, L in enumerate(layers * n_inst):
+            for e in evs[j]:
+                e.record(stream)  # create the event objects
+            q.set_stage_events(evs[j])
+            q.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
+                          wl.fmt, wl.k, wl.normalize, out=outs[j % LAYERS], workspace=ws)
+        q.set_stage_events(None)
+    torch.cuda.synchronize()
+    dur = {"route": [], "fc1": [], "fc2": []}
+    for j in range(len(evs)):
+        e = evs[j]
+        dur["route"].append(e[0].elapsed_time(e[1]) * 1e3)
+        dur["fc1"].append(e[1].elapsed_time(e[2]) * 1e3)
+        dur["fc2"].append(e[2].elapsed_time(e[3]) * 1e3)
+    kern_us = {k: statistics.mean(v) for k, v in dur.items()}
+    fc1_bytes = [a * fc1_b + wl.T * wl.H * 2 + wl.T * wl.k * wl.I * 2 for a in act]
+    fc1_alg = sum(fc1_bytes) / len(fc1_bytes)
+    peak, peak_src = _peaks()
+    fc1_gbs = fc1_alg / (kern_us["fc1"] * 1e-6) / 1e9
+
+    # --- end to end: host buffers, H2D of each layer's inputs, D2H of each output
+    hx = [L["x"].cpu().pin_memory() for L in layers]
+    hl = [L["logits"].cpu().pin_memory() for L in layers]
+    ho = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in layers]
+    dx = [torch.empty_like(L["x"]) for L in layers]
+    dl = [torch.empty_like(L["logits"]) for L in layers]
+    n_e2e = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        for i, L in enumerate(layers):
+            dx[i].copy_(hx[i], non_blocking=True)
+            dl[i].copy_(hl[i], non_blocking=True)
+            q.moe_forward(dx[i], dl[i], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], wl.fmt,
+                          wl.k, wl.normalize, out=outs[i], workspace=ws)
+            ho[i].copy_(outs[i], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_agg = aggregate(x0.elapsed_time(x1) / 1e3, n_e2e * LAYERS, world)
+    h2d = LAYERS * (wl.T * wl.H * 2 + wl.T * wl.E * 4)
+    d2h = LAYERS * wl.T * wl.H * 2
+
+    res = None
+    if rank == 0:
+        cpu = cpu_baseline(args) if (world == 1 and not args.no_cpu_baseline) else None
+        stream_gbs = mean_alg / (us_layer * 1e-6) / 1e9 * world
+        res = {
+            "metric": METRIC, "value": round(us_layer, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(agg["seconds"] * 1e3 / args.steps, 4),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e2m1 x bf16 -> fp32 accumulate (bf16 out)", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: T=4 E=256 k=8 H=2048 I=512 NVFP4 SwiGLU",
+                       "layers_per_step": LAYERS, "global_batch_tokens": wl.T * world,
+                       "l2": "inputs larger than L2: 40 distinct layers, 17.3 GB of weights per step",
+                       "graph": True, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "weight_stream": {"alg_bytes_per_layer": int(mean_alg),
+                              "mean_active_experts": statistics.mean(act),
+                              "gbs": round(stream_gbs, 1), "frac_of_hbm": round(stream_gbs / (peak * world), 4),
+                              "peak_gbs": peak, "peak_source": peak_src},
+            "eager_us_per_layer": round(eager_us, 3),
+            "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},
+            "roofline": {"kernel": "moe_gemv_kernel<FC1> (FC1 GEMV + E2M1 decode + SwiGLU)",
+                         "bound": "hbm", "achieved": round(fc1_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(fc1_gbs / peak, 4), "traffic": None,
+                         "alg_bytes_per_launch": int(fc1_alg), "peak_source": peak_src},
+            "gpu_launches": args.steps * LAYERS * 3,
+            "e2e": {"value": round(e2e_agg["us_per_layer"], 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clocks.summary(t_host0, t_host1),
+            "cpu_baseline": cpu,
+        }
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return res
+
+
+# ---------------------------------------------------------------- CPU (oracle)
+
+def cpu_baseline(args, budget_s: float | None = None) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the workload: whole
+    layers (all 4 tokens), repeated until ~budget seconds of CPU work."""
+    import oracle
+    import synthetic as syn
+    wl = syn.WORKLOADS[WORKLOAD]
+    oracle.build()
+    budget = budget_s if budget_s is not None else args.cpu_seconds
+    cores = os.cpu_count() or 1
+    L = syn.layer(wl, seed=0)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
+                           wl.fmt, wl.k, wl.normalize, nthreads=cores)
+        n += 1
+        if time.perf_counter() - t0 >= budget:
+            break
+    sec = time.perf_counter() - t0
+    return {"value": round(sec * 1e6 / n, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} full layer(s) of {WORKLOAD} (4 tokens, 32 expert rows), fp64 oracle, "
+                      f"OpenMP over (token, expert) pairs"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    import synthetic as syn
+    wl = syn.WORKLOADS[WORKLOAD]
+    oracle.build()
+    cores = os.cpu_count() or 1
+    L = syn.layer(wl, seed=0)
+
+    def one():
+        oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
+                           wl.fmt, wl.k, wl.normalize, nthreads=cores)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    sec = time.perf_counter() - t0
+    us = sec * 1e6 / args.steps
+    sample = f"each step = 1 layer of {WORKLOAD} (a bounded sample of the 40-layer step)"
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp64 (oracle)", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: T=4 E=256 k=8 H=2048 I=512 NVFP4 SwiGLU",
+                       "layers_per_step": 1},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,236 @@
+// The C ABI declared in include/qmoe.h: host-side validation, workspace
+// layout and kernel launches.  Every check runs before the first launch; an
+// invalid call launches nothing.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "qmoe_common.cuh"
+
+namespace qmoe {
+
+static thread_local char g_err[256] = "";
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 132;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static cudaEvent_t *g_stage_events = nullptr;
+static int g_stage_nevents = 0;
+
+static inline void stage_event(int i, cudaStream_t s) {
+  if (g_stage_events && i < g_stage_nevents) cudaEventRecord(g_stage_events[i], s);
+}
+
+static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define QMOE_REQUIRE(cond, status, ...) \
+  do {                                  \
+    if (!(cond)) {                      \
+      set_error(__VA_ARGS__);           \
+      return status;                    \
+    }                                   \
+  } while (0)
+
+static qmoe_status cuda_status(cudaError_t err, const char *what) {
+  if (err == cudaSuccess) return QMOE_OK;
+  set_error("%s: %s", what, cudaGetErrorString(err));
+  return QMOE_ERR_CUDA;
+}
+
+// Bump allocator over the caller's workspace (256-byte aligned regions).
+struct Carve {
+  char *base;
+  size_t off = 0;
+  explicit Carve(void *b) : base(static_cast<char *>(b)) {}
+  template <typename T>
+  T *take(size_t count) {
+    off = (off + 255) & ~(size_t)255;
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+static qmoe_status check_route_args(const float *logits, int T, int E, int k) {
+  QMOE_REQUIRE(logits, QMOE_ERR_INVALID_ARG, "logits is NULL");
+  QMOE_REQUIRE(T >= 1, QMOE_ERR_INVALID_ARG, "T must be >= 1 (got %d)", T);
+  QMOE_REQUIRE(E >= 1, QMOE_ERR_INVALID_ARG, "E must be >= 1 (got %d)", E);
+  QMOE_REQUIRE(k >= 1 && k <= E, QMOE_ERR_INVALID_ARG, "k must be in [1, E] (got k=%d, E=%d)", k, E);
+  QMOE_REQUIRE(k <= kMaxTopK, QMOE_ERR_INVALID_ARG, "k must be <= %d (got %d)", kMaxTopK, k);
+  QMOE_REQUIRE(E <= kMaxExperts, QMOE_ERR_UNSUPPORTED, "E must be <= %d (got %d)", kMaxExperts, E);
+  QMOE_REQUIRE(((uintptr_t)logits & 3u) == 0, QMOE_ERR_MISALIGNED, "logits must be 4-byte aligned");
+  QMOE_REQUIRE((long long)T * k <= (1ll << 30), QMOE_ERR_UNSUPPORTED, "T*k too large");
+  return QMOE_OK;
+}
+
+}  // namespace qmoe
+
+using namespace qmoe;
+
+extern "C" const char *qmoe_last_error(void) { return g_err; }
+
+extern "C" int qmoe_set_stage_events(cudaEvent_t *events, int n_events) {
+  g_stage_events = events;
+  g_stage_nevents = events ? n_events : 0;
+  return 3;
+}
+
+extern "C" qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normalize, int32_t *topk_ids,
+                                       float *topk_weights, int32_t *expert_offsets, int32_t *perm_to_expanded,
+                                       int32_t *expanded_to_perm, void *workspace, size_t *workspace_bytes,
+                                       cudaStream_t stream) {
+  g_err[0] = 0;
+  qmoe_status st = check_route_args(logits, T, E, k);
+  if (st != QMOE_OK) return st;
+  QMOE_REQUIRE(workspace_bytes, QMOE_ERR_INVALID_ARG, "workspace_bytes is NULL");
+  // Routing needs no scratch memory: a call with every output NULL is a size query.
+  if (!workspace) *workspace_bytes = 0;
+  if (!topk_ids && !topk_weights && !expert_offsets && !perm_to_expanded && !expanded_to_perm) return QMOE_OK;
+  QMOE_REQUIRE(topk_ids && topk_weights && expert_offsets && perm_to_expanded && expanded_to_perm,
+               QMOE_ERR_INVALID_ARG, "an output pointer is NULL");
+  RouteOut o{};
+  o.ids = topk_ids;
+  o.weights = topk_weights;
+  o.offsets = expert_offsets;
+  o.p2e = perm_to_expanded;
+  o.e2p = expanded_to_perm;
+  return cuda_status(launch_route(logits, T, E, k, normalize, o, stream), "route launch");
+}
+
+extern "C" qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *block_scales,
+                                        const float *global_scale, int E, int N, int K, qmoe_fp4_format fmt,
+                                        uint16_t *out, cudaStream_t stream) {
+  g_err[0] = 0;
+  QMOE_REQUIRE(packed && block_scales && out, QMOE_ERR_INVALID_ARG, "packed, block_scales and out must be non-NULL");
+  QMOE_REQUIRE(fmt == QMOE_NVFP4 || fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
+  QMOE_REQUIRE(E >= 1 && N >= 1 && K >= 1, QMOE_ERR_INVALID_ARG, "E, N, K must be >= 1 (got %d, %d, %d)", E, N, K);
+  QMOE_REQUIRE(N % 64 == 0 && K % 64 == 0, QMOE_ERR_UNSUPPORTED, "N and K must be multiples of 64 (got %d, %d)", N,
+               K);
+  QMOE_REQUIRE(aligned16(packed) && aligned16(block_scales) && aligned16(out) &&
+                   (global_scale == nullptr || ((uintptr_t)global_scale & 3u) == 0),
+               QMOE_ERR_MISALIGNED, "packed, block_scales and out must be 16-byte aligned");
+  return cuda_status(launch_dequant(packed, block_scales, global_scale, E, N, K, (int)fmt, out, stream),
+                     "dequant launch");
+}
+
+namespace qmoe {
+
+struct DecodeLayout {
+  int32_t *ids, *offsets, *p2e, *e2p, *active, *meta, *counters;
+  float *weights, *y;
+  uint16_t *a;
+  size_t bytes;
+};
+
+static DecodeLayout decode_layout(void *ws, int T, int H, int I, int E, int k) {
+  const size_t R = (size_t)T * k;
+  Carve c(ws);
+  DecodeLayout L{};
+  L.ids = c.take<int32_t>(R);
+  L.weights = c.take<float>(R);
+  L.offsets = c.take<int32_t>((size_t)E + 1);
+  L.p2e = c.take<int32_t>(R);
+  L.e2p = c.take<int32_t>(R);
+  L.active = c.take<int32_t>((size_t)(E < (int)R ? E : (int)R));
+  L.meta = c.take<int32_t>(4);
+  L.counters = c.take<int32_t>((size_t)gemv_fc2_counter_words(H));
+  L.a = c.take<uint16_t>(R * I);
+  L.y = c.take<float>(R * H);
+  L.bytes = (c.off + 255) & ~(size_t)255;
+  return L;
+}
+
+}  // namespace qmoe
+
+extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w,
+                                            const uint8_t *fc1_s, const float *fc1_g, const uint8_t *fc2_w,
+                                            const uint8_t *fc2_s, const float *fc2_g, const uint16_t *fc1_wd,
+                                            const uint16_t *fc2_wd, qmoe_fp4_format fmt, int T, int H, int I, int E,
+                                            int k, int normalize, int swiglu_fusion, float alpha, float beta,
+                                            float limit, uint16_t *out, int32_t *topk_ids_out, void *workspace,
+                                            size_t *workspace_bytes, cudaStream_t stream) {
+  g_err[0] = 0;
+  qmoe_status st = check_route_args(logits, T, E, k);
+  if (st != QMOE_OK) return st;
+  QMOE_REQUIRE(workspace_bytes, QMOE_ERR_INVALID_ARG, "workspace_bytes is NULL");
+  QMOE_REQUIRE(fmt == QMOE_NVFP4 || fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
+  QMOE_REQUIRE(H >= 64 && I >= 64, QMOE_ERR_INVALID_ARG, "H and I must be >= 64 (got %d, %d)", H, I);
+  QMOE_REQUIRE(H % 64 == 0 && I % 64 == 0, QMOE_ERR_UNSUPPORTED, "H and I must be multiples of 64 (got %d, %d)", H,
+               I);
+  QMOE_REQUIRE(swiglu_fusion == 1, QMOE_ERR_UNSUPPORTED, "only swiglu_fusion=1 (interleaved) is supported (got %d)",
+               swiglu_fusion);
+  QMOE_REQUIRE(!std::isnan(alpha) && !std::isnan(beta) && !std::isnan(limit), QMOE_ERR_INVALID_ARG,
+               "alpha, beta and limit must not be NaN");
+  const long long R = (long long)T * k;
+  const bool gemv = R <= QMOE_GEMV_MAX_ROWS;
+  QMOE_REQUIRE(gemv, QMOE_ERR_UNSUPPORTED, "T*k = %lld > %d needs the prefill path", R, QMOE_GEMV_MAX_ROWS);
+  QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
+  (void)fc1_wd;
+  (void)fc2_wd;
+  const DecodeLayout need = decode_layout(nullptr, T, H, I, E, k);
+  if (!workspace) {
+    *workspace_bytes = need.bytes;
+    return QMOE_OK;
+  }
+  QMOE_REQUIRE(*workspace_bytes >= need.bytes, QMOE_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes",
+               *workspace_bytes, need.bytes);
+  QMOE_REQUIRE(x && fc1_w && fc1_s && fc2_w && fc2_s && out, QMOE_ERR_INVALID_ARG,
+               "x, weights, scales and out must be non-NULL");
+  QMOE_REQUIRE(aligned16(x) && aligned16(fc1_w) && aligned16(fc1_s) && aligned16(fc2_w) && aligned16(fc2_s) &&
+                   aligned16(out) && aligned16(workspace),
+               QMOE_ERR_MISALIGNED, "x, weights, scales, out and workspace must be 16-byte aligned");
+  QMOE_REQUIRE((fc1_g == nullptr || ((uintptr_t)fc1_g & 3u) == 0) && (fc2_g == nullptr || ((uintptr_t)fc2_g & 3u) == 0),
+               QMOE_ERR_MISALIGNED, "global scales must be 4-byte aligned");
+
+  const DecodeLayout L = decode_layout(workspace, T, H, I, E, k);
+  RouteOut ro{};
+  ro.ids = topk_ids_out ? topk_ids_out : L.ids;
+  ro.weights = L.weights;
+  ro.offsets = L.offsets;
+  ro.p2e = L.p2e;
+  ro.e2p = L.e2p;
+  ro.active = L.active;
+  ro.meta = L.meta;
+  ro.zero_words = L.counters;
+  ro.n_zero_words = gemv_fc2_counter_words(H);
+
+  GemvArgs g{};
+  g.fmt = (int)fmt;
+  g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
+  g.alpha = alpha; g.beta = beta; g.limit = limit;
+  g.x = x;
+  g.w1 = fc1_w; g.s1 = fc1_s; g.g1 = fc1_g;
+  g.w2 = fc2_w; g.s2 = fc2_s; g.g2 = fc2_g;
+  g.offsets = L.offsets; g.p2e = L.p2e; g.e2p = L.e2p; g.active = L.active; g.meta = L.meta;
+  g.weights = L.weights;
+  g.a = L.a; g.y = L.y; g.counters = L.counters; g.out = out;
+
+  stage_event(0, stream);
+  cudaError_t err = launch_route(logits, T, E, k, normalize, ro, stream);
+  if (err != cudaSuccess) return cuda_status(err, "route launch");
+  stage_event(1, stream);
+  err = launch_fc1_gemv(g, stream);
+  if (err != cudaSuccess) return cuda_status(err, "fc1 launch");
+  stage_event(2, stream);
+  err = launch_fc2_gemv(g, stream);
+  if (err != cudaSuccess) return cuda_status(err, "fc2 launch");
+  stage_event(3, stream);
+  return QMOE_OK;
+}

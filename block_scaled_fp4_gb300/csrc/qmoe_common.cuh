@@ -1,0 +1,116 @@
+// Shared device helpers and host-side declarations of the QMoE CUDA library.
+// Format decoding follows "MoE and QMoE - CUDA Operator Documentation" §6.5 /
+// §9b (E2M1 codes, E4M3FN and E8M0 block scales, fp32 global scale).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qmoe.h"
+
+namespace qmoe {
+
+constexpr int kNvfp4Block = 16;
+constexpr int kMxfp4Block = 32;
+constexpr int kMaxExperts = 256;   // warp top-k holds at most 8 keys per lane
+constexpr int kMaxTopK = 8;
+
+__host__ __device__ inline int block_size(int fmt) { return fmt == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block; }
+
+// ---- element codecs (device) -------------------------------------------------
+
+// Two E2M1 codes (low nibble = element 2j, high nibble = element 2j+1) -> f16x2,
+// exact, with the sm_100+ hardware converter (no lookup table).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte_in_low_bits));
+  return r;
+}
+
+// d = a * b + c with a, b fp16 and c, d fp32; the product is formed exactly.
+__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+
+// E4M3FN byte -> fp32, exact for every code (subnormals included); S.1111.111 -> NaN.
+// The 7 exponent/mantissa bits are placed at the fp32 exponent/mantissa
+// position (which gives value * 2^-120, exactly, as an fp32 number, subnormal
+// for exponent field 0) and rescaled by 2^120.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t em = b & 0x7Fu;
+  float f = __uint_as_float(em << 20) * 0x1p120f;
+  if (em == 0x7Fu) f = __uint_as_float(0x7FC00000u);
+  return (b & 0x80u) ? -f : f;
+}
+
+// E8M0 byte -> fp32: 2^(b-127); 0xFF -> NaN; 0 -> 2^-127 (an fp32 subnormal).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  b &= 0xFFu;
+  if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
+  if (b == 0u) return __uint_as_float(0x00400000u);
+  return __uint_as_float(b << 23);
+}
+
+__device__ __forceinline__ float scale_to_f32(int fmt, uint32_t b) {
+  return fmt == QMOE_NVFP4 ? e4m3_to_f32(b) : e8m0_to_f32(b);
+}
+
+// fp32 -> bf16 bits, round to nearest even; NaN -> 0x7FC0.
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// ---- host side -------------------------------------------------------------------
+
+void set_error(const char *fmt, ...);
+int num_sms();
+
+// Decode routing: one CTA does top-k, softmax and the stable expert ranking for
+// T <= kFusedRouteMaxTokens tokens.
+constexpr int kFusedRouteMaxTokens = 64;
+
+struct RouteOut {
+  int32_t *ids;        // [T*k]
+  float *weights;      // [T*k]
+  int32_t *offsets;    // [E+1]
+  int32_t *p2e;        // [T*k]
+  int32_t *e2p;        // [T*k]
+  int32_t *active;     // [min(E, T*k)] experts that got rows, ascending; may be null
+  int32_t *meta;       // [4] meta[0] = number of active experts; may be null
+  int32_t *zero_words; // words cleared by the route kernel for later kernels; may be null
+  int n_zero_words;
+};
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize, const RouteOut &o,
+                         cudaStream_t stream);
+
+struct GemvArgs {
+  int fmt, T, H, I, E, k;
+  float alpha, beta, limit;
+  const uint16_t *x;
+  const uint8_t *w1, *s1, *w2, *s2;
+  const float *g1, *g2;
+  const int32_t *offsets, *p2e, *e2p, *active, *meta;
+  const float *weights;
+  uint16_t *a;       // [R, I] bf16
+  float *y;          // [R, H] fp32
+  int32_t *counters; // [H / 64] arrival counters (zeroed by the route kernel)
+  uint16_t *out;     // [T, H] bf16
+};
+int gemv_fc2_counter_words(int H);
+cudaError_t launch_fc1_gemv(const GemvArgs &a, cudaStream_t stream);
+cudaError_t launch_fc2_gemv(const GemvArgs &a, cudaStream_t stream);
+
+cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const float *g, int E, int N, int K,
+                           int fmt, uint16_t *out, cudaStream_t stream);
+
+}  // namespace qmoe

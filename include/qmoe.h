@@ -1,0 +1,188 @@
+/*
+ * qmoe.h -- C ABI of the GB300 (sm_103a) weight-only FP4 mixture-of-experts
+ * layer (QMoE, W4A16): top-k softmax routing, permute-by-expert, FC1 with
+ * SwiGLU, FC2, weighted un-permute, and the FP4 -> bf16 weight dequantisation
+ * used at prefill.
+ *
+ * The operation follows the pages' operator statement:
+ *   "MoE and QMoE - CUDA Operator Documentation" §1 (pipeline: router top-k
+ *   softmax -> permute by expert -> GEMM1 -> activation -> GEMM2 -> un-permute
+ *   -> weighted sum), §2 (inputs: router probabilities, fc1/fc2 weights, block
+ *   scales, global scales; attributes k, swiglu_fusion, activation_alpha/beta,
+ *   swiglu_limit, normalize_routing_weights), §6.5 (packed [E, K, N/2] e2m1
+ *   storage and W = fp4(W) * block_scale * global_scale), §8 (SwiGLU), §9b
+ *   (NVFP4: E4M3 scale per 16 k and a per-expert fp32 global scale);
+ *   "[CUDA] Coalesce QMoE MXFP4/NVFP4 weight dequantization" (the [E, K, N/2]
+ *   -> [E, N, K] dequantisation);
+ *   "[CUDA] Cut the MoE routing prologue/epilogue cost for small-batch decode"
+ *   (stable top-k, renormalised weights, stable expert ranking).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or keeps them.  bf16 tensors are passed as their
+ *    16-bit patterns (uint16_t).
+ *  - Packed FP4 weights: uint8 [E, K, N/2]; byte (e, k, j) holds logical
+ *    element (n = 2j) in its low nibble and (n = 2j + 1) in its high nibble.
+ *    E2M1 code: bit 3 sign, bits 2:0 select 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ *  - Block scales: uint8 [E, N, K/bs]: E4M3FN with bs = 16 (QMOE_NVFP4) or
+ *    E8M0 (bias 127, 0xFF = NaN) with bs = 32 (QMOE_MXFP4).
+ *  - Global scales: fp32 [E]; NULL means 1.0 for every expert.
+ *  - Weights, scales and activations must be 16-byte aligned
+ *    (QMOE_ERR_MISALIGNED otherwise).
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *    never synchronise.  Every argument is validated on the host before any
+ *    launch; an invalid call launches nothing and returns a status != 0.
+ *    A launch failure is reported as QMOE_ERR_CUDA (cudaGetLastError).
+ *    qmoe_last_error() gives a one-line reason for the last failure on the
+ *    calling host thread.
+ *  - Scratch memory is a caller-provided device workspace.  Calling with
+ *    workspace == NULL stores the required size in *workspace_bytes and
+ *    returns QMOE_OK without launching.  The workspace needs no
+ *    initialisation; its contents on return are unspecified.  Two calls that
+ *    share one workspace must not run concurrently on the GPU.
+ */
+#ifndef QMOE_H_
+#define QMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMOE_OK = 0,
+    QMOE_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, k > E, k > 8, ... */
+    QMOE_ERR_MISALIGNED = 2,   /* a tensor pointer is not 16-byte aligned */
+    QMOE_ERR_UNSUPPORTED = 3,  /* shape outside what the kernels cover */
+    QMOE_ERR_WORKSPACE = 4,    /* *workspace_bytes smaller than required */
+    QMOE_ERR_CUDA = 5          /* a CUDA call or kernel launch failed */
+} qmoe_status;
+
+typedef enum {
+    QMOE_NVFP4 = 0, /* E2M1 + E4M3FN scale per 16 k + fp32 global scale per expert */
+    QMOE_MXFP4 = 1  /* E2M1 + E8M0 scale per 32 k (+ optional fp32 global scale) */
+} qmoe_fp4_format;
+
+/* Largest number of expanded rows (T * k) the decode GEMV path takes; more rows
+ * take the prefill path (dequantise + tensor-core grouped GEMM).  The window
+ * is the one PR #31159 sets for MTP verification ("kMaxProfiledExpandedRows
+ * 8 -> 64"). */
+#define QMOE_GEMV_MAX_ROWS 64
+
+/*
+ * qmoe_route_topk -- top-k softmax routing and permute-by-expert maps.
+ * Operator doc §1 ("router (top-k softmax) -> permute by expert"); PR #31156
+ * (warp top-k with a stable tie-break, renormalised weights, stable ranking of
+ * the T*k assignments by expert).
+ *
+ *   logits           fp32 [T, E] router logits.
+ *   T, E, k          tokens (>= 1), experts (1..256), experts per token (1..min(8, E)).
+ *   normalize        0: weight = softmax over all E at the selected expert;
+ *                    != 0: those k weights divided by their sum.
+ *   topk_ids         int32 [T, k] out: selected experts per token, ordered by
+ *                    (logit descending, expert index ascending).
+ *   topk_weights     fp32 [T, k] out: routing weights in the same order.
+ *   expert_offsets   int32 [E + 1] out: first permuted row of each expert;
+ *                    expert_offsets[E] = T * k.
+ *   perm_to_expanded int32 [T * k] out: expanded index (t * k + j) of each
+ *                    permuted row; rows of one expert keep ascending expanded
+ *                    index (stable).
+ *   expanded_to_perm int32 [T * k] out: the inverse permutation.
+ *   workspace, workspace_bytes: see the conventions above.
+ * Selection is exact (made on the fp32 logits; -0.0 and +0.0 compare equal).
+ * NaN logits are outside the contract.
+ */
+qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normalize,
+                            int32_t *topk_ids, float *topk_weights,
+                            int32_t *expert_offsets, int32_t *perm_to_expanded,
+                            int32_t *expanded_to_perm,
+                            void *workspace, size_t *workspace_bytes,
+                            cudaStream_t stream);
+
+/*
+ * qmoe_fp4_moe_forward -- the whole MoE layer:
+ *   out[t] = bf16( sum_j w[t][j] * FFN_{id[t][j]}(x[t]) ),
+ *   FFN_e(x) = Wd2_e * bf16( SwiGLU( Wd1_e * x ) ),
+ * with Wd the dequantised weights, fp32 accumulation, the SwiGLU of operator
+ * doc §8 on interleaved FC1 columns (2m = gate, 2m + 1 = linear;
+ * swiglu_fusion = 1):
+ *   G = min(gate, limit); L = clamp(linear, -limit, limit);
+ *   SwiGLU = G * sigmoid(alpha * G) * (L + beta)
+ * (alpha = 1, beta = 0, limit = +inf is SiLU(gate) * linear).
+ *
+ *   x            bf16 [T, H] activations.
+ *   logits       fp32 [T, E] router logits (routed as in qmoe_route_topk).
+ *   fc1_w        uint8 [E, H, I]  packed e2m1, K = H, N = 2I.
+ *   fc1_s        uint8 [E, 2I, H/bs] block scales.
+ *   fc1_g        fp32 [E] global scales, or NULL.
+ *   fc2_w        uint8 [E, I, H/2] packed e2m1, K = I, N = H.
+ *   fc2_s        uint8 [E, H, I/bs] block scales.
+ *   fc2_g        fp32 [E] global scales, or NULL.
+ *   fc1_wd       bf16 [E, 2I, H] already-dequantised FC1 weights, or NULL;
+ *   fc2_wd       bf16 [E, H, I] already-dequantised FC2 weights, or NULL.
+ *                (Used only when T * k > QMOE_GEMV_MAX_ROWS; when NULL that
+ *                path dequantises into the workspace.)
+ *   fmt          QMOE_NVFP4 or QMOE_MXFP4.
+ *   T, H, I, E, k  sizes: T >= 1; H, I multiples of 64; 1 <= E <= 256;
+ *                1 <= k <= min(8, E).
+ *   normalize    as in qmoe_route_topk.
+ *   swiglu_fusion must be 1 (interleaved gate/linear columns).
+ *   alpha, beta, limit  SwiGLU parameters (limit may be +inf).
+ *   out          bf16 [T, H] result.
+ *   topk_ids_out int32 [T, k] selected experts, or NULL.
+ *   workspace, workspace_bytes: see the conventions above.
+ * T * k <= QMOE_GEMV_MAX_ROWS runs the decode GEMVs (dequantisation in
+ * registers); larger T * k runs the prefill path.
+ */
+qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits,
+                                 const uint8_t *fc1_w, const uint8_t *fc1_s, const float *fc1_g,
+                                 const uint8_t *fc2_w, const uint8_t *fc2_s, const float *fc2_g,
+                                 const uint16_t *fc1_wd, const uint16_t *fc2_wd,
+                                 qmoe_fp4_format fmt, int T, int H, int I, int E, int k,
+                                 int normalize, int swiglu_fusion,
+                                 float alpha, float beta, float limit,
+                                 uint16_t *out, int32_t *topk_ids_out,
+                                 void *workspace, size_t *workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
+ * qmoe_fp4_dequant -- FP4 -> bf16 weight dequantisation (PR #31349; operator
+ * doc §4.3, §6.5, §9b):
+ *   out[e][n][k] = bf16_rne( e2m1(nibble(packed[e][k][n/2], n % 2))
+ *                            * scale(block_scales[e][n][k/bs]) * global_scale[e] )
+ * with the product taken exactly and rounded once (round to nearest even);
+ * a NaN scale gives the bf16 NaN 0x7FC0.
+ *
+ *   packed        uint8 [E, K, N/2].
+ *   block_scales  uint8 [E, N, K/bs].
+ *   global_scale  fp32 [E], or NULL (1.0).
+ *   E, N, K       E >= 1; N a multiple of 64; K a multiple of 64.
+ *   fmt           QMOE_NVFP4 or QMOE_MXFP4.
+ *   out           bf16 [E, N, K].
+ * Needs no workspace.
+ */
+qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *block_scales,
+                             const float *global_scale, int E, int N, int K,
+                             qmoe_fp4_format fmt, uint16_t *out, cudaStream_t stream);
+
+/* One-line description of the last failed call on this host thread ("" if none). */
+const char *qmoe_last_error(void);
+
+/*
+ * Instrumentation (benchmarks): when `events` is non-NULL, every later
+ * qmoe_fp4_moe_forward call records events[0] on its stream before its first
+ * kernel and events[i] after its i-th kernel, for i < n_events.  The events
+ * are created by the caller (cudaEventCreate) and must outlive the calls.
+ * Pass NULL to switch it off.  Process-wide setting; not thread-safe.
+ * Returns the number of kernels one forward call launches for (T, k) decode
+ * shapes (route, FC1, FC2), i.e. how many events after the first are used.
+ */
+int qmoe_set_stage_events(cudaEvent_t *events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMOE_H_ */

