@@ -25,7 +25,7 @@ STATUS = {0: "QMOE_OK", 1: "QMOE_ERR_INVALID_ARG", 2: "QMOE_ERR_MISALIGNED",
 
 # Every symbol include/qmoe.h declares.
 EXPORTS = ("qmoe_route_topk", "qmoe_fp4_moe_forward", "qmoe_fp4_dequant", "qmoe_last_error",
-           "qmoe_set_stage_events")
+           "qmoe_set_stage_events", "qmoe_fp4_moe_forward_no_alloc")
 
 
 class QMoEError(RuntimeError):
@@ -64,6 +64,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
             L.qmoe_last_error.argtypes = []
             L.qmoe_set_stage_events.restype = i
             L.qmoe_set_stage_events.argtypes = [P, i]
+            L.qmoe_fp4_moe_forward_no_alloc.restype = i
+            L.qmoe_fp4_moe_forward_no_alloc.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
+                                                        f, f, f, P, P, P]
             _lib = L
     return _lib
 
@@ -151,6 +154,29 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: 
     return out
 
 
+def moe_forward_no_alloc(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: int = 1,
+                         alpha: float = 1.0, beta: float = 0.0, limit: float = math.inf, out=None,
+                         topk_ids=None, stream=None):
+    """The MoE layer through the entry point that allocates no device memory
+    (its scratch is a fixed array inside the library; see include/qmoe.h).
+    ``out`` must be given by callers that cannot allocate; when it is None a
+    bf16 [T,H] tensor is created here for convenience."""
+    import torch
+    for t, n in ((x, "x"), (logits, "logits"), (w1, "w1"), (s1, "s1"), (g1, "g1"), (w2, "w2"),
+                 (s2, "s2"), (g2, "g2"), (out, "out")):
+        _cuda(t, n)
+    T, H = x.shape
+    E, _, I = w1.shape
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(load().qmoe_fp4_moe_forward_no_alloc(_ptr(x), _ptr(logits), _ptr(w1), _ptr(s1), _ptr(g1),
+                                                _ptr(w2), _ptr(s2), _ptr(g2), fmt, T, H, I, E, k,
+                                                int(normalize), 1, float(alpha), float(beta),
+                                                float(limit), _ptr(out), _ptr(topk_ids),
+                                                _stream(stream)))
+    return out
+
+
 def dequant(packed, scales, gscale, fmt: int, out=None, stream=None):
     """packed uint8 [E,K,N/2], scales uint8 [E,N,K/bs], gscale f32 [E] or
     None -> bf16 [E,N,K]."""
@@ -182,5 +208,5 @@ def set_stage_events(events) -> int:
 _stage_keepalive = None
 
 __all__ = ["NVFP4", "MXFP4", "BLOCK", "GEMV_MAX_ROWS", "QMoEError", "build", "load", "library_path",
-           "route_topk", "moe_forward", "forward_workspace_bytes", "dequant", "set_stage_events",
-           "EXPORTS"]
+           "route_topk", "moe_forward", "moe_forward_no_alloc", "forward_workspace_bytes", "dequant",
+           "set_stage_events", "EXPORTS"]

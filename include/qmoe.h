@@ -168,6 +168,42 @@ qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *block_scales,
                              const float *global_scale, int E, int N, int K,
                              qmoe_fp4_format fmt, uint16_t *out, cudaStream_t stream);
 
+/*
+ * qmoe_fp4_moe_forward_no_alloc -- the same layer as qmoe_fp4_moe_forward for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * to this entry point; it exists for callers such as a plug-in that runs inside
+ * another engine's memory pool and only receives its input and output buffers,
+ * or a latency-critical loop in which a cudaMalloc (it can stall the whole
+ * device) is not allowed.
+ *
+ * Scratch comes from a device array inside the library of
+ * QMOE_NO_ALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library
+ * holds until the process exits.  The caller still passes all inputs and
+ * outputs; arguments, results and errors are those of qmoe_fp4_moe_forward
+ * (without fc*_wd, workspace and workspace_bytes).  Sizes whose scratch need
+ * exceeds QMOE_NO_ALLOC_SCRATCH_BYTES are rejected with QMOE_ERR_WORKSPACE
+ * before anything is launched.  No cudaMalloc, cudaFree or other allocating
+ * routine is called.
+ *  - The first call on a device looks up the array's device address there
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call, on any stream or host thread, uses the same array, which keeps
+ *    the last call's contents: calls that overlap on the GPU race and corrupt
+ *    each other's results.  Order them (one stream, or events).
+ *  - Nothing in the array needs to start at zero: the routing kernel clears the
+ *    per-call counters the later kernels rely on at the start of every call.
+ */
+#define QMOE_NO_ALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const float *logits,
+                                          const uint8_t *fc1_w, const uint8_t *fc1_s,
+                                          const float *fc1_g, const uint8_t *fc2_w,
+                                          const uint8_t *fc2_s, const float *fc2_g,
+                                          qmoe_fp4_format fmt, int T, int H, int I, int E, int k,
+                                          int normalize, int swiglu_fusion,
+                                          float alpha, float beta, float limit,
+                                          uint16_t *out, int32_t *topk_ids_out,
+                                          cudaStream_t stream);
+
 /* One-line description of the last failed call on this host thread ("" if none). */
 const char *qmoe_last_error(void);
 
