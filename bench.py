@@ -196,6 +196,8 @@ def run_gpu(args):
     torch.cuda.set_device(device)
     q.build()
     q.load()
+    global LAYERS
+    LAYERS = args.layers
     wl, layers = make_layers(LAYERS, seed=1234 + rank, device=device)
     ws_bytes = q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, wl.fmt)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
@@ -415,6 +417,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="distinct layers per step (default 40; fewer only for small profiler runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

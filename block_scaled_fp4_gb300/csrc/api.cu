@@ -133,14 +133,18 @@ extern "C" qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *bl
 namespace qmoe {
 
 struct DecodeLayout {
-  int32_t *ids, *offsets, *p2e, *e2p, *active, *meta, *counters;
+  int32_t *ids, *offsets, *p2e, *e2p, *active, *meta, *counters, *xshift;
+  uint32_t *rowmax;
+  SlotDesc *slots;
   float *weights, *y;
-  uint16_t *a;
+  uint16_t *a, *x16;
   size_t bytes;
+  int n_zero;  // words from `counters` on that the routing kernel clears
 };
 
 static DecodeLayout decode_layout(void *ws, int T, int H, int I, int E, int k) {
   const size_t R = (size_t)T * k;
+  const size_t S = (size_t)(E < (int)R ? E : (int)R);
   Carve c(ws);
   DecodeLayout L{};
   L.ids = c.take<int32_t>(R);
@@ -148,9 +152,16 @@ static DecodeLayout decode_layout(void *ws, int T, int H, int I, int E, int k) {
   L.offsets = c.take<int32_t>((size_t)E + 1);
   L.p2e = c.take<int32_t>(R);
   L.e2p = c.take<int32_t>(R);
-  L.active = c.take<int32_t>((size_t)(E < (int)R ? E : (int)R));
+  L.active = c.take<int32_t>(S);
+  L.slots = c.take<SlotDesc>(S);
   L.meta = c.take<int32_t>(4);
-  L.counters = c.take<int32_t>((size_t)gemv_fc2_counter_words(H));
+  L.xshift = c.take<int32_t>((size_t)T);
+  // counters and row maxima are contiguous: the routing kernel zeroes both
+  const int nc = gemv_fc2_counter_words(H);
+  L.counters = c.take<int32_t>((size_t)nc + R);
+  L.rowmax = reinterpret_cast<uint32_t *>(L.counters ? L.counters + nc : nullptr);
+  L.n_zero = nc + (int)R;
+  L.x16 = c.take<uint16_t>((size_t)T * H);
   L.a = c.take<uint16_t>(R * I);
   L.y = c.take<float>(R * H);
   L.bytes = (c.off + 255) & ~(size_t)255;
@@ -208,19 +219,24 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   ro.e2p = L.e2p;
   ro.active = L.active;
   ro.meta = L.meta;
+  ro.slots = L.slots;
   ro.zero_words = L.counters;
-  ro.n_zero_words = gemv_fc2_counter_words(H);
+  ro.n_zero_words = L.n_zero;
+  ro.x = x;
+  ro.x16 = L.x16;
+  ro.xshift = L.xshift;
+  ro.H = H;
 
   GemvArgs g{};
   g.fmt = (int)fmt;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
   g.alpha = alpha; g.beta = beta; g.limit = limit;
-  g.x = x;
   g.w1 = fc1_w; g.s1 = fc1_s; g.g1 = fc1_g;
   g.w2 = fc2_w; g.s2 = fc2_s; g.g2 = fc2_g;
-  g.offsets = L.offsets; g.p2e = L.p2e; g.e2p = L.e2p; g.active = L.active; g.meta = L.meta;
+  g.e2p = L.e2p; g.meta = L.meta; g.slots = L.slots; g.p2e = L.p2e;
   g.weights = L.weights;
-  g.a = L.a; g.y = L.y; g.counters = L.counters; g.out = out;
+  g.x16 = L.x16; g.xshift = L.xshift;
+  g.a = L.a; g.rowmax = L.rowmax; g.y = L.y; g.counters = L.counters; g.out = out;
 
   stage_event(0, stream);
   cudaError_t err = launch_route(logits, T, E, k, normalize, ro, stream);

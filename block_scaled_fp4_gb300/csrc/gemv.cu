@@ -7,37 +7,43 @@
 // table-free E2M1 decode, the block scale applied to a per-block partial sum
 // instead of to every weight, fp32 accumulation for bf16 activations, and a
 // 64-expanded-row window.  Design here (sm_103a):
-//  * one CTA = one active expert x 64 output columns x all of K; 256 threads =
-//    8 column words (8 columns each, one 32-bit load per k row) x 32 k-groups;
-//    a k-group owns whole scale blocks (16 rows NVFP4, 32 rows MXFP4);
+//  * one CTA = one active expert ("slot") x NT output columns x all of K.
+//    256 threads = (NT/8) column words (8 columns = one 32-bit load per k row)
+//    x (2048/NT) k-groups; NT in {64, 128, 256} is picked per launch so that
+//    the grid holds about two CTAs per SM; a k-group owns whole scale blocks;
+//  * two load groups of 16 k rows ping-pong in registers: while one is
+//    decoded the next is in flight; the first is issued before the
+//    activations are staged;
 //  * E2M1 pairs decode with the hardware cvt.rn.f16x2.e2m1x2 (one instruction
 //    per two weights) and multiply-accumulate with fma.rn.f32.f16 (fp16
 //    operands, exact product, fp32 accumulator);
-//  * activations are staged in shared memory as fp16 after an exact
-//    power-of-two rescale per row (largest |x| in [2^14, 2^15)), so every
-//    finite bf16 activation stays in fp16 range; the factor is undone on the
-//    fp32 result;
+//  * activations arrive as fp16 rescaled per row by a power of two (largest
+//    |x| in [2^14, 2^15)), so every finite bf16 activation is exact in fp16;
+//    FC1 takes them from the routing kernel, FC2 rescales its bf16 rows with
+//    the row maxima FC1 publishes (atomicMax on fp32 bits: order-free);
 //  * the per-block partial sum is multiplied once by the block scale; NVFP4
 //    scales are used as E4M3 * 2^-120 (bits moved into fp32 position, exact)
-//    and the 2^120 is folded into the per-expert global scale at the end;
-//  * k-group partials are reduced in shared memory in a fixed order
-//    (deterministic), then FC1 applies SwiGLU and writes bf16 activations;
-//    FC2 writes fp32 rows and the last CTA to finish a column tile (arrival
-//    counter, no waiting) forms out[t] = bf16(sum_j w[t][j] * y[t*k+j]) in
-//    fixed j order.
+//    and the 2^120 is applied once at the end;
+//  * k-group partials are reduced with warp shuffles, then across warps in
+//    shared memory, in a fixed order (deterministic).  FC1 applies SwiGLU and
+//    writes bf16 activations; FC2 writes fp32 rows and the last CTA to finish
+//    a 64-column tile (arrival counter, no waiting) forms
+//    out[t] = bf16(sum_j w[t][j] * y[t*k+j]) in fixed j order;
+//  * the kernels are chained with programmatic dependent launch: a kernel
+//    starts while its predecessor runs and waits (griddepcontrol.wait) before
+//    it reads the predecessor's results.
 #include <cuda_fp16.h>
 
 #include "qmoe_common.cuh"
 
 namespace qmoe {
 
-constexpr int kTileN = 64;          // output columns per CTA
 constexpr int kGemvThreads = 256;
-constexpr int kWords = kTileN / 8;  // 32-bit words (8 codes) per k row in a tile
-constexpr int kKGroups = kGemvThreads / kWords;  // 32
-constexpr int kRowChunk = 4;        // rows decoded together
+constexpr int kCounterTile = 64;  // un-permute column tile (counters are per 64 columns)
+constexpr int kRowChunk = 2;      // rows decoded together
+constexpr int kGroupRows = 16;    // k rows per load group
 
-int gemv_fc2_counter_words(int H) { return H / kTileN; }
+int gemv_fc2_counter_words(int H) { return H / kCounterTile; }
 
 // Raw block scale as fp32.  NVFP4: E4M3 value * 2^-120 (exact); MXFP4: 2^(b-127).
 // `special` is set for codes that need the exact slow path (NaN; E8M0 0 / 255).
@@ -58,129 +64,81 @@ __device__ __forceinline__ float exact_raw_scale(uint32_t b) {
   return e8m0_to_f32(b);
 }
 
-// Largest |x| of `n` bf16 values (bit pattern compare of the magnitudes).
-__device__ __forceinline__ uint32_t row_absmax_bits(const uint16_t *src, int n) {
-  uint32_t m = 0;
-  for (int i = threadIdx.x * 8; i < n; i += kGemvThreads * 8) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(src + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      m = max(m, w[q] & 0x7FFFu);
-      m = max(m, (w[q] >> 16) & 0x7FFFu);
-    }
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, s));
-  return m;
-}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// Power-of-two exponent s with max|x| * 2^-s in [2^14, 2^15) (clamped).
-__device__ __forceinline__ int prescale_exponent(uint32_t absmax_bf16_bits) {
-  if (absmax_bf16_bits == 0u) return 0;
-  const int e = (int)((absmax_bf16_bits >> 7) & 0xFFu) - 127;  // floor(log2) for normal values
-  int s = e - 14;
-  return max(-100, min(100, s));
-}
-
-struct StageShared {
-  uint32_t warp_max[kGemvThreads / 32][kRowChunk];
-  int shift[kRowChunk];
+template <int NT>
+struct Tile {
+  static constexpr int kWords = NT / 8;                   // column words per k row
+  static constexpr int kKGroups = kGemvThreads / kWords;  // k-groups in the CTA
+  static constexpr int kWarps = kGemvThreads / 32;
 };
 
-// Stage up to kRowChunk activation rows (bf16, length K) into shared memory as
-// fp16 after the per-row power-of-two rescale.  Rows >= nrows are zero.
-__device__ void stage_rows(const uint16_t *const *src, int nrows, int K, __half *xs, StageShared &ss) {
-  const int w = threadIdx.x >> 5;
-  for (int r = 0; r < kRowChunk; ++r) {
-    uint32_t m = 0;
-    if (r < nrows) m = row_absmax_bits(src[r], K);
-    if (lane_id() == 0) ss.warp_max[w][r] = m;
-  }
-  __syncthreads();
-  if (threadIdx.x < kRowChunk) {
-    uint32_t m = 0;
-    for (int i = 0; i < kGemvThreads / 32; ++i) m = max(m, ss.warp_max[i][threadIdx.x]);
-    ss.shift[threadIdx.x] = prescale_exponent(m);
-  }
-  __syncthreads();
-  for (int r = 0; r < kRowChunk; ++r) {
-    __half2 *dst = reinterpret_cast<__half2 *>(xs + (size_t)r * K);
-    if (r >= nrows) {
-      for (int i = threadIdx.x; i < K / 2; i += kGemvThreads) dst[i] = __half2(__float2half(0.f), __float2half(0.f));
-      continue;
-    }
-    const float f = __uint_as_float((uint32_t)(127 - ss.shift[r]) << 23);  // 2^-shift
-    for (int i = threadIdx.x * 8; i < K; i += kGemvThreads * 8) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(src[r] + i);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+// Weight rows [k0, k0+16) of this thread's column word, plus (at a block start)
+// the block's 8 scale bytes.
+struct LoadGroup {
+  uint32_t w[kGroupRows];
+  uint32_t s[8];
+};
+
+template <int BS>
+__device__ __forceinline__ void issue_group(LoadGroup &g, const uint8_t *wcol, const uint8_t *scol,
+                                            size_t row_bytes, int nblocks, int blk, int sub) {
+  const int k0 = blk * BS + sub * kGroupRows;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = bf16_to_f32(wv[q] & 0xFFFFu) * f, hi = bf16_to_f32(wv[q] >> 16) * f;
-        dst[(i >> 1) + q] = __floats2half2_rn(lo, hi);
-      }
-    }
+  for (int kk = 0; kk < kGroupRows; ++kk)
+    g.w[kk] = __ldg(reinterpret_cast<const uint32_t *>(wcol + (size_t)(k0 + kk) * row_bytes));
+  if (sub == 0) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) g.s[c] = __ldg(scol + (size_t)c * nblocks + blk);
   }
-  __syncthreads();
 }
 
-// acc[r][c] (+)= sum over this thread's scale blocks of raw_scale * sum_k x[r][k] * e2m1
-template <int FMT, int BS, int RC>
-__device__ __forceinline__ void gemv_mainloop(const uint8_t *__restrict__ wexp, const uint8_t *__restrict__ sexp,
-                                              int K, int N, int n0, const __half *xs, float (&acc)[RC][8]) {
-  const int lane = (int)lane_id();
-  const int wi = lane & 7;
-  const int kg = ((threadIdx.x >> 5) << 2) | (lane >> 3);
-  const int nblocks = K / BS;
-  const size_t row_bytes = (size_t)N / 2;
-  const uint8_t *wcol = wexp + n0 / 2 + wi * 4;
-  const uint8_t *scol = sexp + (size_t)(n0 + wi * 8) * nblocks;
+// One load group (16 k rows x 8 columns) decoded and multiplied into the
+// block partials bp; at the end of a scale block bp is scaled into acc.
+template <int FMT, int RC>
+__device__ __forceinline__ void consume_group(const LoadGroup &cur, int sub, const __half *xb, int K,
+                                              uint32_t (&sb)[8], float (&bp)[RC][8], float (&acc)[RC][8]) {
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  constexpr int G = BS / kGroupRows;
+  if (sub == 0) {
+    if (G > 1) {  // the scale bytes must outlive this buffer's reuse
 #pragma unroll
-  for (int r = 0; r < RC; ++r)
-#pragma unroll
-    for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
-  for (int b = kg; b < nblocks; b += kKGroups) {
-    uint32_t wv[BS];
-#pragma unroll
-    for (int kk = 0; kk < BS; ++kk)
-      wv[kk] = __ldg(reinterpret_cast<const uint32_t *>(wcol + ((size_t)b * BS + kk) * row_bytes));
-    uint32_t sb[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) sb[c] = __ldg(scol + (size_t)c * nblocks + b);
-    float bp[RC][8];
+      for (int c = 0; c < 8; ++c) sb[c] = cur.s[c];
+    }
 #pragma unroll
     for (int r = 0; r < RC; ++r)
 #pragma unroll
       for (int c = 0; c < 8; ++c) bp[r][c] = 0.f;
-    const __half *xb = xs + (size_t)b * BS;
+  }
 #pragma unroll
-    for (int kk = 0; kk < BS; kk += 2) {
-      uint32_t x2[RC];
+  for (int kk = 0; kk < kGroupRows; kk += 2) {
+    uint32_t x2[RC];
 #pragma unroll
-      for (int r = 0; r < RC; ++r) x2[r] = *reinterpret_cast<const uint32_t *>(xb + (size_t)r * K + kk);
+    for (int r = 0; r < RC; ++r) x2[r] = *reinterpret_cast<const uint32_t *>(xb + (size_t)r * K + kk);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t wd = wv[kk + h];
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t wd = cur.w[kk + h];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t p = e2m1x2_to_f16x2(wd >> (8 * q));
-          const uint16_t lo = (uint16_t)(p & 0xFFFFu), hi = (uint16_t)(p >> 16);
+      for (int qq = 0; qq < 4; ++qq) {
+        const uint32_t p = e2m1x2_to_f16x2(wd >> (8 * qq));
+        const uint16_t lo = (uint16_t)(p & 0xFFFFu), hi = (uint16_t)(p >> 16);
 #pragma unroll
-          for (int r = 0; r < RC; ++r) {
-            const uint16_t xv = (uint16_t)(h ? (x2[r] >> 16) : (x2[r] & 0xFFFFu));
-            bp[r][2 * q] = fma_f16_f32(lo, xv, bp[r][2 * q]);
-            bp[r][2 * q + 1] = fma_f16_f32(hi, xv, bp[r][2 * q + 1]);
-          }
+        for (int r = 0; r < RC; ++r) {
+          const uint16_t xv = (uint16_t)(h ? (x2[r] >> 16) : (x2[r] & 0xFFFFu));
+          bp[r][2 * qq] = fma_f16_f32(lo, xv, bp[r][2 * qq]);
+          bp[r][2 * qq + 1] = fma_f16_f32(hi, xv, bp[r][2 * qq + 1]);
         }
       }
     }
+  }
+  if (sub == G - 1) {
     bool special = false;
     float sc[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) sc[c] = raw_scale<FMT>(sb[c], special);
+    for (int c = 0; c < 8; ++c) sc[c] = raw_scale<FMT>(G > 1 ? sb[c] : cur.s[c], special);
     if (special) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) sc[c] = exact_raw_scale<FMT>(sb[c]);
+      for (int c = 0; c < 8; ++c) sc[c] = exact_raw_scale<FMT>(G > 1 ? sb[c] : cur.s[c]);
     }
 #pragma unroll
     for (int r = 0; r < RC; ++r)
@@ -189,26 +147,84 @@ __device__ __forceinline__ void gemv_mainloop(const uint8_t *__restrict__ wexp, 
   }
 }
 
-// Sum the 32 k-group partials of each (row, column) in a fixed order.
-// red: [kKGroups][kRowChunk][kTileN] floats.  Returns via red[0][r][col].
-template <int RC>
-__device__ __forceinline__ void reduce_kgroups(float (&acc)[RC][8], float *red) {
-  const int lane = (int)lane_id();
-  const int wi = lane & 7;
-  const int kg = ((threadIdx.x >> 5) << 2) | (lane >> 3);
-  __syncthreads();  // xs may alias red
+// acc[r][c] = sum over this thread's scale blocks of raw_scale * sum_k x[r][k] * e2m1.
+// Two load groups ping-pong: while one is decoded the other is in flight.
+// `ga` already holds the first group.
+template <int FMT, int NT, int RC>
+__device__ __forceinline__ void gemv_mainloop(const uint8_t *__restrict__ wexp, const uint8_t *__restrict__ sexp,
+                                              int K, int N, int n0, const __half *xs, LoadGroup &ga,
+                                              float (&acc)[RC][8]) {
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  constexpr int G = BS / kGroupRows;  // load groups per scale block
+  using T = Tile<NT>;
+  const int wi = threadIdx.x % T::kWords;
+  const int kg = threadIdx.x / T::kWords;
+  const int nblocks = K / BS;
+  const size_t row_bytes = (size_t)N / 2;
+  const uint8_t *wcol = wexp + n0 / 2 + wi * 4;
+  const uint8_t *scol = sexp + (size_t)(n0 + wi * 8) * nblocks;
+  const int my_blocks = kg < nblocks ? (nblocks - 1 - kg) / T::kKGroups + 1 : 0;
+  const int nq = my_blocks * G;
 #pragma unroll
-  for (int r = 0; r < RC; ++r) {
-    float4 *d = reinterpret_cast<float4 *>(red + ((size_t)kg * kRowChunk + r) * kTileN + wi * 8);
-    d[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-    d[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+  LoadGroup gb;
+  uint32_t sb[8];
+  float bp[RC][8];
+  for (int q = 0; q < nq; q += 2) {
+    if (q + 1 < nq)
+      issue_group<BS>(gb, wcol, scol, row_bytes, nblocks, kg + ((q + 1) / G) * T::kKGroups, (q + 1) % G);
+    consume_group<FMT, RC>(ga, q % G, xs + (size_t)(kg + (q / G) * T::kKGroups) * BS + (q % G) * kGroupRows, K,
+                           sb, bp, acc);
+    if (q + 1 >= nq) break;
+    if (q + 2 < nq)
+      issue_group<BS>(ga, wcol, scol, row_bytes, nblocks, kg + ((q + 2) / G) * T::kKGroups, (q + 2) % G);
+    consume_group<FMT, RC>(gb, (q + 1) % G,
+                           xs + (size_t)(kg + ((q + 1) / G) * T::kKGroups) * BS + ((q + 1) % G) * kGroupRows, K,
+                           sb, bp, acc);
+  }
+}
+
+// Sum the k-group partials of each (row, column) in a fixed order: shuffles
+// inside a warp, then the warps' partials in shared memory (red: [warps][rows][NT]).
+// The result is left in red[r * NT + col].
+template <int NT, int RC>
+__device__ __forceinline__ void reduce_kgroups(float (&acc)[RC][8], float *red) {
+  using T = Tile<NT>;
+  constexpr int kPer = (RC * NT + kGemvThreads - 1) / kGemvThreads;
+  const int lane = (int)lane_id(), warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = T::kWords; m < 32; m <<= 1)
+#pragma unroll
+    for (int r = 0; r < RC; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], m);
+  __syncthreads();  // the staged activations (aliasing red) are no longer read
+  if (lane < T::kWords) {
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+      float4 *d = reinterpret_cast<float4 *>(red + ((size_t)warp * kRowChunk + r) * NT + lane * 8);
+      d[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      d[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+    }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < RC * kTileN; i += kGemvThreads) {
-    const int r = i / kTileN, col = i % kTileN;
-    float s = 0.f;
-    for (int g = 0; g < kKGroups; ++g) s += red[((size_t)g * kRowChunk + r) * kTileN + col];
-    red[(size_t)r * kTileN + col] = s;
+  float s[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = threadIdx.x + j * kGemvThreads;
+    s[j] = 0.f;
+    if (i < RC * NT) {
+      const int r = i / NT, col = i % NT;
+      for (int w = 0; w < T::kWarps; ++w) s[j] += red[((size_t)w * kRowChunk + r) * NT + col];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = threadIdx.x + j * kGemvThreads;
+    if (i < RC * NT) red[i] = s[j];
   }
   __syncthreads();
 }
@@ -219,118 +235,206 @@ __device__ __forceinline__ float swiglu(float gate, float lin, float alpha, floa
   return G * (1.0f / (1.0f + expf(-alpha * G))) * (L + beta);
 }
 
+template <int NT>
 static size_t gemv_smem_bytes(int K) {
   const size_t xs = (size_t)kRowChunk * K * sizeof(__half);
-  const size_t red = (size_t)kKGroups * kRowChunk * kTileN * sizeof(float);
+  const size_t red = (size_t)Tile<NT>::kWarps * kRowChunk * NT * sizeof(float);
   return xs > red ? xs : red;
 }
 
-// FC = 1: K = H, N = 2I, rows read x[token]; output a (bf16, SwiGLU'd).
+// Stage activation rows [c0, c0 + nrows) of the slot into shared memory (fp16,
+// rescaled).  FC1: copies of the token rows the routing kernel converted.
+// FC2: the bf16 rows of a, rescaled with the row maxima FC1 published.
+// shifts[r] receive the exponents to undo.
+template <int FC>
+__device__ __forceinline__ void stage_rows(const GemvArgs &g, const SlotDesc &sd, int c0, int nrows, int K,
+                                           __half *xs, int *shifts) {
+  if (threadIdx.x < kRowChunk) {
+    int sh = 0;
+    if ((int)threadIdx.x < nrows) {
+      const int p = sd.row0 + c0 + threadIdx.x;
+      if (FC == 1) {
+        sh = g.xshift[g.p2e[p] / g.k];
+      } else {
+        const uint32_t m = __ldcg(g.rowmax + p);
+        if (m != 0u) sh = max(-100, min(100, (int)((m >> 23) & 0xFFu) - 127 - 14));
+      }
+    }
+    shifts[threadIdx.x] = sh;
+  }
+  __syncthreads();
+  for (int r = 0; r < kRowChunk; ++r) {
+    uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)r * K);
+    if (r >= nrows) {
+      for (int i = threadIdx.x; i < K / 8; i += kGemvThreads) dst[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const int p = sd.row0 + c0 + r;
+    if (FC == 1) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(g.x16 + (size_t)(g.p2e[p] / g.k) * g.H);
+      for (int i = threadIdx.x; i < K / 8; i += kGemvThreads) dst[i] = __ldcg(src + i);
+    } else {
+      const uint4 *src = reinterpret_cast<const uint4 *>(g.a + (size_t)p * g.I);
+      const float f = pow2f(-shifts[r]);
+      for (int i = threadIdx.x; i < K / 8; i += kGemvThreads) {
+        const uint4 v = __ldcg(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __half2 h = __floats2half2_rn(bf16_to_f32(w[q] & 0xFFFFu) * f, bf16_to_f32(w[q] >> 16) * f);
+          o[q] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// FC = 1: K = H, N = 2I, rows read x16[token]; output a (bf16, SwiGLU'd).
 // FC = 2: K = I, N = H, rows read a[row]; output y (fp32) + un-permute.
-template <int FC, int FMT>
+template <int FC, int FMT, int NT>
 __global__ void __launch_bounds__(kGemvThreads, 2) moe_gemv_kernel(GemvArgs g) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ StageShared ss;
+  __shared__ int shifts[kRowChunk];
   __shared__ int is_last;
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  using T = Tile<NT>;
+  pdl_wait();  // routing (and for FC2 also FC1) results are visible from here on
+  if (FC == 1) pdl_launch_dependents();
   const int slot = blockIdx.y;
-  const int num_active = g.meta[0];
-  if (slot >= num_active) return;
-  const int e = g.active[slot];
-  const int n0 = blockIdx.x * kTileN;
+  if (slot >= g.meta[0]) return;
+  const SlotDesc sd = g.slots[slot];
+  const int e = sd.e;
+  const int n0 = blockIdx.x * NT;
   const int K = FC == 1 ? g.H : g.I;
   const int N = FC == 1 ? 2 * g.I : g.H;
-  const int row0 = g.offsets[e], nrows_all = g.offsets[e + 1] - row0;
   const uint8_t *wexp = (FC == 1 ? g.w1 : g.w2) + (size_t)e * K * (N / 2);
   const uint8_t *sexp = (FC == 1 ? g.s1 : g.s2) + (size_t)e * N * (K / BS);
   const float *gs = FC == 1 ? g.g1 : g.g2;
   const float gscale = gs ? gs[e] : 1.0f;
   __half *xs = reinterpret_cast<__half *>(smem_raw);
   float *red = reinterpret_cast<float *>(smem_raw);
+  const int wi = threadIdx.x % T::kWords, kg = threadIdx.x / T::kWords;
+  const int nblocks = K / BS;
 
-  for (int c0 = 0; c0 < nrows_all; c0 += kRowChunk) {
-    const int nrows = min(kRowChunk, nrows_all - c0);
-    const uint16_t *src[kRowChunk];
-#pragma unroll
-    for (int r = 0; r < kRowChunk; ++r) {
-      const int p = row0 + c0 + min(r, nrows - 1);
-      src[r] = FC == 1 ? g.x + (size_t)(g.p2e[p] / g.k) * g.H : g.a + (size_t)p * g.I;
-    }
-    stage_rows(src, nrows, K, xs, ss);
-    float acc4[4][8];
+  for (int c0 = 0; c0 < sd.nrows; c0 += kRowChunk) {
+    const int nrows = min(kRowChunk, sd.nrows - c0);
+    // first weight group in flight before the activations are staged
+    LoadGroup first;
+    if (kg < nblocks)
+      issue_group<BS>(first, wexp + n0 / 2 + wi * 4, sexp + (size_t)(n0 + wi * 8) * nblocks, (size_t)N / 2,
+                      nblocks, kg, 0);
+    stage_rows<FC>(g, sd, c0, nrows, K, xs, shifts);
     if (nrows == 1) {
       float acc[1][8];
-      gemv_mainloop<FMT, BS, 1>(wexp, sexp, K, N, n0, xs, acc);
-      reduce_kgroups<1>(acc, red);
-    } else if (nrows == 2) {
-      float acc[2][8];
-      gemv_mainloop<FMT, BS, 2>(wexp, sexp, K, N, n0, xs, acc);
-      reduce_kgroups<2>(acc, red);
+      gemv_mainloop<FMT, NT, 1>(wexp, sexp, K, N, n0, xs, first, acc);
+      reduce_kgroups<NT, 1>(acc, red);
     } else {
-      gemv_mainloop<FMT, BS, 4>(wexp, sexp, K, N, n0, xs, acc4);
-      reduce_kgroups<4>(acc4, red);
+      float acc[2][8];
+      gemv_mainloop<FMT, NT, 2>(wexp, sexp, K, N, n0, xs, first, acc);
+      reduce_kgroups<NT, 2>(acc, red);
     }
-    // epilogue: red[r][col] holds the raw sums of this chunk
+    // epilogue: red[r * NT + col] holds the raw sums of this chunk.  The 2^120
+    // fold comes first so that undoing the row's 2^-shift cannot underflow.
     const float fold = FMT == QMOE_NVFP4 ? 0x1p120f : 1.0f;
     if (FC == 1) {
-      for (int i = threadIdx.x; i < nrows * (kTileN / 2); i += kGemvThreads) {
-        const int r = i / (kTileN / 2), m = i % (kTileN / 2);
-        const float un = __uint_as_float((uint32_t)(127 + ss.shift[r]) << 23);
-        // fold first: red * 2^120 is the sum in units of the rescaled row, near
-        // 2^20 for any row, so undoing the row's 2^-shift afterwards cannot underflow
-        const float hg = red[r * kTileN + 2 * m] * fold * un * gscale;
-        const float hl = red[r * kTileN + 2 * m + 1] * fold * un * gscale;
-        const float act = swiglu(hg, hl, g.alpha, g.beta, g.limit);
-        g.a[(size_t)(row0 + c0 + r) * g.I + n0 / 2 + m] = (uint16_t)f32_to_bf16_rne(act);
+      for (int i = threadIdx.x; i < nrows * (NT / 2); i += kGemvThreads) {
+        const int r = i / (NT / 2), m = i % (NT / 2);
+        const float un = pow2f(shifts[r]);
+        const float hg = red[r * NT + 2 * m] * fold * un * gscale;
+        const float hl = red[r * NT + 2 * m + 1] * fold * un * gscale;
+        const uint32_t ab = f32_to_bf16_rne(swiglu(hg, hl, g.alpha, g.beta, g.limit));
+        const int p = sd.row0 + c0 + r;
+        g.a[(size_t)p * g.I + n0 / 2 + m] = (uint16_t)ab;
+        // NT / 2 >= 32 and nrows * NT / 2 is a multiple of 32: a warp is either
+        // wholly inside this loop iteration and shares one row r, or outside it
+        const uint32_t mag = __reduce_max_sync(0xFFFFFFFFu, (ab & 0x7FFFu) << 16);
+        if (lane_id() == 0) atomicMax(g.rowmax + p, mag);
       }
     } else {
-      for (int i = threadIdx.x; i < nrows * kTileN; i += kGemvThreads) {
-        const int r = i / kTileN, col = i % kTileN;
-        const float un = __uint_as_float((uint32_t)(127 + ss.shift[r]) << 23);
-        g.y[(size_t)(row0 + c0 + r) * g.H + n0 + col] = red[r * kTileN + col] * fold * un * gscale;
+      for (int i = threadIdx.x; i < nrows * NT; i += kGemvThreads) {
+        const int r = i / NT, col = i % NT;
+        const float un = pow2f(shifts[r]);
+        g.y[(size_t)(sd.row0 + c0 + r) * g.H + n0 + col] = red[r * NT + col] * fold * un * gscale;
       }
     }
     __syncthreads();
   }
   if (FC == 2) {
-    // last CTA of this column tile forms the weighted un-permute
+    // the last CTA of each 64-column un-permute tile forms the weighted sum
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) is_last = atomicAdd(&g.counters[blockIdx.x], 1) == num_active - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    for (int i = threadIdx.x; i < g.T * kTileN; i += kGemvThreads) {
-      const int t = i / kTileN, col = i % kTileN;
-      float s = 0.f;
-      for (int j = 0; j < g.k; ++j) {
-        const int ex = t * g.k + j;
-        s = fmaf(__ldcg(g.weights + ex), __ldcg(g.y + (size_t)__ldcg(g.e2p + ex) * g.H + n0 + col), s);
+    for (int t0 = 0; t0 < NT; t0 += kCounterTile) {
+      const int tile = (n0 + t0) / kCounterTile;
+      if (threadIdx.x == 0) is_last = atomicAdd(&g.counters[tile], 1) == g.meta[0] - 1;
+      __syncthreads();
+      if (is_last) {
+        __threadfence();
+        for (int i = threadIdx.x; i < g.T * kCounterTile; i += kGemvThreads) {
+          const int t = i / kCounterTile, col = n0 + t0 + i % kCounterTile;
+          float s = 0.f;
+          for (int j = 0; j < g.k; ++j) {
+            const int ex = t * g.k + j;
+            s = fmaf(__ldcg(g.weights + ex), __ldcg(g.y + (size_t)__ldcg(g.e2p + ex) * g.H + col), s);
+          }
+          g.out[(size_t)t * g.H + col] = (uint16_t)f32_to_bf16_rne(s);
+        }
       }
-      g.out[(size_t)t * g.H + n0 + col] = (uint16_t)f32_to_bf16_rne(s);
+      __syncthreads();
     }
   }
+}
+
+template <int FC, int FMT, int NT>
+static cudaError_t launch_one(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t stream) {
+  // The opt-in shared-memory size is raised only when a larger one is needed,
+  // so steady-state calls (and graph capture) make no attribute calls.
+  static size_t smem_set = 0;
+  auto kfn = moe_gemv_kernel<FC, FMT, NT>;
+  if (smem > 48 * 1024 && smem > smem_set) {
+    cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    smem_set = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, a);
+}
+
+// Widest column tile that still gives about two CTAs per SM.
+static int pick_tile(int N, int slots) {
+  const int target = 2 * num_sms();
+  for (int nt : {256, 128}) {
+    if (N % nt == 0 && (long long)slots * (N / nt) >= target) return nt;
+  }
+  return 64;
 }
 
 template <int FC>
 static cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t stream) {
   const int K = FC == 1 ? a.H : a.I;
   const int N = FC == 1 ? 2 * a.I : a.H;
-  const size_t smem = gemv_smem_bytes(K);
-  const int max_slots = a.E < a.T * a.k ? a.E : a.T * a.k;
-  dim3 grid(N / kTileN, max_slots);
-  // The opt-in shared-memory size is raised only when a larger one is needed,
-  // so steady-state calls (and graph capture) make no attribute calls.
-  static size_t smem_set[2] = {0, 0};
-  const int fi = a.fmt == QMOE_NVFP4 ? 0 : 1;
-  auto kfn = a.fmt == QMOE_NVFP4 ? moe_gemv_kernel<FC, QMOE_NVFP4> : moe_gemv_kernel<FC, QMOE_MXFP4>;
-  if (smem > 48 * 1024 && smem > smem_set[fi]) {
-    cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    smem_set[fi] = smem;
+  const int slots = a.E < a.T * a.k ? a.E : a.T * a.k;
+  const int nt = pick_tile(N, slots);
+  const dim3 grid(N / nt, slots);
+  if (a.fmt == QMOE_NVFP4) {
+    if (nt == 256) return launch_one<FC, QMOE_NVFP4, 256>(a, grid, gemv_smem_bytes<256>(K), stream);
+    if (nt == 128) return launch_one<FC, QMOE_NVFP4, 128>(a, grid, gemv_smem_bytes<128>(K), stream);
+    return launch_one<FC, QMOE_NVFP4, 64>(a, grid, gemv_smem_bytes<64>(K), stream);
   }
-  kfn<<<grid, kGemvThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  if (nt == 256) return launch_one<FC, QMOE_MXFP4, 256>(a, grid, gemv_smem_bytes<256>(K), stream);
+  if (nt == 128) return launch_one<FC, QMOE_MXFP4, 128>(a, grid, gemv_smem_bytes<128>(K), stream);
+  return launch_one<FC, QMOE_MXFP4, 64>(a, grid, gemv_smem_bytes<64>(K), stream);
 }
 
 cudaError_t launch_fc1_gemv(const GemvArgs &a, cudaStream_t stream) { return launch_gemv<1>(a, stream); }

@@ -78,6 +78,11 @@ int num_sms();
 // T <= kFusedRouteMaxTokens tokens.
 constexpr int kFusedRouteMaxTokens = 64;
 
+// Decode-path slot descriptor: the s-th expert (ascending id) that received rows.
+struct SlotDesc {
+  int e, row0, nrows, pad;
+};
+
 struct RouteOut {
   int32_t *ids;        // [T*k]
   float *weights;      // [T*k]
@@ -86,8 +91,14 @@ struct RouteOut {
   int32_t *e2p;        // [T*k]
   int32_t *active;     // [min(E, T*k)] experts that got rows, ascending; may be null
   int32_t *meta;       // [4] meta[0] = number of active experts; may be null
+  SlotDesc *slots;     // [min(E, T*k)] slot descriptors; may be null
   int32_t *zero_words; // words cleared by the route kernel for later kernels; may be null
   int n_zero_words;
+  // decode only: activations rescaled per token by a power of two into fp16
+  const uint16_t *x;   // bf16 [T, H] or null
+  uint16_t *x16;       // fp16 [T, H]
+  int32_t *xshift;     // [T]: x16 = x * 2^-xshift
+  int H;
 };
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize, const RouteOut &o,
@@ -96,19 +107,28 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize
 struct GemvArgs {
   int fmt, T, H, I, E, k;
   float alpha, beta, limit;
-  const uint16_t *x;
   const uint8_t *w1, *s1, *w2, *s2;
   const float *g1, *g2;
-  const int32_t *offsets, *p2e, *e2p, *active, *meta;
+  const int32_t *e2p, *meta;
+  const SlotDesc *slots;
+  const int32_t *p2e;
   const float *weights;
-  uint16_t *a;       // [R, I] bf16
-  float *y;          // [R, H] fp32
-  int32_t *counters; // [H / 64] arrival counters (zeroed by the route kernel)
-  uint16_t *out;     // [T, H] bf16
+  const uint16_t *x16;     // fp16 [T, H] (from the route kernel)
+  const int32_t *xshift;   // [T]
+  uint16_t *a;             // [R, I] bf16
+  uint32_t *rowmax;        // [R] largest |a| of each row (fp32 bits), zeroed by the route kernel
+  float *y;                // [R, H] fp32
+  int32_t *counters;       // [H / 64] arrival counters (zeroed by the route kernel)
+  uint16_t *out;           // [T, H] bf16
 };
 int gemv_fc2_counter_words(int H);
 cudaError_t launch_fc1_gemv(const GemvArgs &a, cudaStream_t stream);
 cudaError_t launch_fc2_gemv(const GemvArgs &a, cudaStream_t stream);
+
+// Programmatic dependent launch: let the next kernel in the stream start while
+// this one runs / wait here until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const float *g, int E, int N, int K,
                            int fmt, uint16_t *out, cudaStream_t stream);

@@ -10,7 +10,7 @@
 // Ties are broken by a packed stable key: fp32 logit (order-preserving bits,
 // -0.0 folded onto +0.0) in the high word, (0xFFFF - expert) in the low word,
 // so a larger key means a larger logit, then a lower expert index.
-#include <cstdio>
+#include <cuda_fp16.h>
 
 #include "qmoe_common.cuh"
 
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
 // expert's count is prefixed over warps (segment order = expanded order, so
 // the rank is stable), then over experts.
 __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, int32_t *p2e, int32_t *e2p,
-                           int32_t *active, int32_t *meta, int32_t *cnt /* smem [W][E] */,
+                           int32_t *active, int32_t *meta, SlotDesc *slots, int32_t *cnt /* smem [W][E] */,
                            int32_t *tot /* smem [E+1] */) {
   const int W = blockDim.x >> 5, w = (int)(threadIdx.x >> 5), lane = (int)lane_id();
   for (int i = threadIdx.x; i < W * E; i += blockDim.x) cnt[i] = 0;
@@ -191,6 +191,7 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
         offsets[e] = run;
         tot[e] = run;
         if (c > 0 && active) active[arun] = e;
+        if (c > 0 && slots) slots[arun] = SlotDesc{e, run, c, 0};
         arun += c > 0;
         run += c;
       }
@@ -210,16 +211,53 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
   }
 }
 
-// Decode routing: one CTA routes T <= 64 tokens (warp per token) and builds the maps.
+// Per-token power-of-two rescale of the activations into fp16 for the decode
+// GEMVs: x16 = x * 2^-s with the row's largest |x| * 2^-s in [2^14, 2^15), so
+// every finite bf16 value keeps its 8 significant bits in fp16.  One warp per token.
+__device__ void convert_token_fp16(const uint16_t *x, int H, int t, uint16_t *x16, int32_t *xshift) {
+  const int lane = (int)lane_id();
+  const uint16_t *row = x + (size_t)t * H;
+  uint32_t m = 0;
+  for (int i = lane * 8; i < H; i += 256) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, s));
+  int sh = 0;
+  if (m != 0u) sh = max(-100, min(100, (int)((m >> 7) & 0xFFu) - 127 - 14));
+  const float f = __uint_as_float((uint32_t)(127 - sh) << 23);
+  for (int i = lane * 8; i < H; i += 256) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(bf16_to_f32(w[q] & 0xFFFFu) * f, bf16_to_f32(w[q] >> 16) * f);
+      o[q] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(x16 + (size_t)t * H + i) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) xshift[t] = sh;
+}
+
+// Decode routing: one CTA routes T <= 64 tokens (warp per token), builds the
+// maps and the slot descriptors, and converts the activations for the GEMVs.
 template <int N>
 __global__ void __launch_bounds__(256) route_maps_fused_kernel(const float *__restrict__ logits, int T, int E,
                                                               int k, int normalize, RouteOut o) {
   extern __shared__ int32_t smem_i32[];
+  pdl_launch_dependents();
   const int W = blockDim.x >> 5, w = (int)(threadIdx.x >> 5);
   for (int i = threadIdx.x; i < o.n_zero_words; i += blockDim.x) o.zero_words[i] = 0;
   for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights);
+  if (o.x) {
+    for (int t = W - 1 - w; t < T; t += W) convert_token_fp16(o.x, o.H, t, o.x16, o.xshift);
+  }
   __syncthreads();
-  build_maps(o.ids, T * k, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, smem_i32, smem_i32 + W * E);
+  build_maps(o.ids, T * k, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
 }
 
 // Prefill routing, second step: one CTA of 1024 threads builds the maps.
@@ -227,7 +265,7 @@ __global__ void __launch_bounds__(1024) maps_kernel(int R, int E, RouteOut o) {
   extern __shared__ int32_t smem_i32[];
   const int W = blockDim.x >> 5;
   for (int i = threadIdx.x; i < o.n_zero_words; i += blockDim.x) o.zero_words[i] = 0;
-  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, smem_i32, smem_i32 + W * E);
+  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
 }
 
 static int keys_per_lane(int E, int k) {
