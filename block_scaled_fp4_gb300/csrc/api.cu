@@ -89,7 +89,7 @@ extern "C" const char *qmoe_last_error(void) { return g_err; }
 extern "C" int qmoe_set_stage_events(cudaEvent_t *events, int n_events) {
   g_stage_events = events;
   g_stage_nevents = events ? n_events : 0;
-  return 3;
+  return 2;
 }
 
 extern "C" qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normalize, int32_t *topk_ids,
@@ -133,16 +133,13 @@ extern "C" qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *bl
 namespace qmoe {
 
 struct DecodeLayout {
-  int32_t *ids, *offsets, *p2e, *e2p, *active, *meta, *counters, *xshift;
-  uint32_t *rowmax;
+  int32_t *ids, *offsets, *p2e, *e2p, *active, *meta;
   SlotDesc *slots;
-  float *weights, *y;
-  uint16_t *a, *x16;
+  float *weights, *p1, *p2;
   size_t bytes;
-  int n_zero;  // words from `counters` on that the routing kernel clears
 };
 
-static DecodeLayout decode_layout(void *ws, int T, int H, int I, int E, int k) {
+static DecodeLayout decode_layout(void *ws, int T, int E, int k, size_t p1_floats, size_t p2_floats) {
   const size_t R = (size_t)T * k;
   const size_t S = (size_t)(E < (int)R ? E : (int)R);
   Carve c(ws);
@@ -154,16 +151,9 @@ static DecodeLayout decode_layout(void *ws, int T, int H, int I, int E, int k) {
   L.e2p = c.take<int32_t>(R);
   L.active = c.take<int32_t>(S);
   L.slots = c.take<SlotDesc>(S);
-  L.meta = c.take<int32_t>(4);
-  L.xshift = c.take<int32_t>((size_t)T);
-  // counters and row maxima are contiguous: the routing kernel zeroes both
-  const int nc = gemv_fc2_counter_words(H);
-  L.counters = c.take<int32_t>((size_t)nc + R);
-  L.rowmax = reinterpret_cast<uint32_t *>(L.counters ? L.counters + nc : nullptr);
-  L.n_zero = nc + (int)R;
-  L.x16 = c.take<uint16_t>((size_t)T * H);
-  L.a = c.take<uint16_t>(R * I);
-  L.y = c.take<float>(R * H);
+  L.meta = c.take<int32_t>(4);  // [0] active experts, [1] device error flag, [2], [3] grid barriers
+  L.p1 = c.take<float>(p1_floats);
+  L.p2 = c.take<float>(p2_floats);
   L.bytes = (c.off + 255) & ~(size_t)255;
   return L;
 }
@@ -195,7 +185,11 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
   (void)fc1_wd;
   (void)fc2_wd;
-  const DecodeLayout need = decode_layout(nullptr, T, H, I, E, k);
+  LayerPlan plan;
+  size_t p1_floats = 0, p2_floats = 0;
+  st = make_layer_plan((int)fmt, T, H, I, E, k, plan, p1_floats, p2_floats);
+  if (st != QMOE_OK) return st;
+  const DecodeLayout need = decode_layout(nullptr, T, E, k, p1_floats, p2_floats);
   if (!workspace) {
     *workspace_bytes = need.bytes;
     return QMOE_OK;
@@ -210,7 +204,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   QMOE_REQUIRE((fc1_g == nullptr || ((uintptr_t)fc1_g & 3u) == 0) && (fc2_g == nullptr || ((uintptr_t)fc2_g & 3u) == 0),
                QMOE_ERR_MISALIGNED, "global scales must be 4-byte aligned");
 
-  const DecodeLayout L = decode_layout(workspace, T, H, I, E, k);
+  const DecodeLayout L = decode_layout(workspace, T, E, k, p1_floats, p2_floats);
   RouteOut ro{};
   ro.ids = topk_ids_out ? topk_ids_out : L.ids;
   ro.weights = L.weights;
@@ -220,33 +214,27 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   ro.active = L.active;
   ro.meta = L.meta;
   ro.slots = L.slots;
-  ro.zero_words = L.counters;
-  ro.n_zero_words = L.n_zero;
-  ro.x = x;
-  ro.x16 = L.x16;
-  ro.xshift = L.xshift;
-  ro.H = H;
+  ro.zero_words = L.meta + 1;  // error flag and grid-barrier counters start every call at 0
+  ro.n_zero_words = 3;
 
-  GemvArgs g{};
+  LayerArgs g{};
   g.fmt = (int)fmt;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
   g.alpha = alpha; g.beta = beta; g.limit = limit;
+  g.x = x;
   g.w1 = fc1_w; g.s1 = fc1_s; g.g1 = fc1_g;
   g.w2 = fc2_w; g.s2 = fc2_s; g.g2 = fc2_g;
-  g.e2p = L.e2p; g.meta = L.meta; g.slots = L.slots; g.p2e = L.p2e;
+  g.e2p = L.e2p; g.p2e = L.p2e; g.meta = L.meta; g.slots = L.slots;
   g.weights = L.weights;
-  g.x16 = L.x16; g.xshift = L.xshift;
-  g.a = L.a; g.rowmax = L.rowmax; g.y = L.y; g.counters = L.counters; g.out = out;
+  g.p1 = L.p1; g.p2 = L.p2; g.out = out;
 
   stage_event(0, stream);
   cudaError_t err = launch_route(logits, T, E, k, normalize, ro, stream);
   if (err != cudaSuccess) return cuda_status(err, "route launch");
   stage_event(1, stream);
-  err = launch_fc1_gemv(g, stream);
-  if (err != cudaSuccess) return cuda_status(err, "fc1 launch");
+  err = launch_layer(g, plan, E, stream);
+  if (err == cudaErrorCooperativeLaunchTooLarge && g_err[0]) return QMOE_ERR_CUDA;  // message already set
+  if (err != cudaSuccess) return cuda_status(err, "layer launch");
   stage_event(2, stream);
-  err = launch_fc2_gemv(g, stream);
-  if (err != cudaSuccess) return cuda_status(err, "fc2 launch");
-  stage_event(3, stream);
   return QMOE_OK;
 }

@@ -1,0 +1,1250 @@
+// Decode path of the FP4 MoE layer in one persistent kernel: FC1 GEMV with
+// SwiGLU, FC2 GEMV and the weighted un-permute, with the E2M1 weights
+// dequantised in registers.
+//
+// Prior art on the pages ("[CUDA] Speed up the NVFP4 QMoE decode GEMV and
+// enable it for MTP verify", PR #31159; operator doc §9b.2/§9b.3): coalesced
+// weight and scale streams, weight loads batched ahead of their decode, a
+// table-free E2M1 decode, the block scale applied to a per-block partial sum
+// instead of to every weight, fp32 accumulation for bf16 activations, and a
+// 64-expanded-row window.  Design here (sm_103a, one CTA per SM):
+//  * work unit = 16*RGS k rows x NT columns of one active expert's weights
+//    (about 32 KB).  The units of all active experts are laid end to end
+//    (expert slot, column tile, k) and split evenly over the CTAs
+//    ("stream-K"): every CTA streams the same number of bytes whatever the
+//    number of rows each expert received.  A CTA's consecutive units of one
+//    (expert, tile) form a segment, which it reduces to a partial sum;
+//  * one warp issues the bulk async copies (cp.async.bulk, completion counted
+//    on an mbarrier) of the CTA's FC1 units and then, without waiting for FC1
+//    to finish anywhere, of its FC2 units into a 4-slot ring.  Just before
+//    the first unit of each window of 16 scale blocks it issues a 2-D tensor
+//    copy (cp.async.bulk.tensor) of that window's block scales, [NT][16]
+//    bytes, so scales and weights arrive in one ordered stream; the
+//    consumers transpose the window in shared memory at the window boundary
+//    so that a thread reads the 8 scale bytes of its 8 columns with one load.
+//    Scales whose rows are not 16-byte multiples are read with byte loads;
+//  * the copy warp starts once the first activations are staged: small loads
+//    issued behind a GPU-wide burst of bulk copies wait for all of it;
+//  * 16 consumer warps: thread (w, rg) owns column word w (8 columns) of
+//    k-group rg (16 rows) of a unit, decodes with the hardware
+//    cvt.rn.f16x2.e2m1x2 and multiplies with fma.rn.f32.f16 (fp16 operands,
+//    exact product, fp32 accumulator); the 16-row partial is multiplied once
+//    by its block scale (NVFP4 scales used as E4M3 * 2^-120, bits moved into
+//    fp32 position, exact; the 2^120 applied at the end);
+//  * activations are staged in fp16 after an exact power-of-two rescale per
+//    row (largest |x| in [2^14, 2^15)), so every finite bf16 activation is
+//    exact in fp16; the rescale is undone on the fp32 partial;
+//  * partial sums are reduced over row groups in shared memory and written to
+//    global memory (fp32).  After a grid barrier, FC2 forms its bf16
+//    activations a = SwiGLU(g1 * sum of FC1 partials) for the k range it
+//    needs; after a second grid barrier, out[t] = bf16(sum_j w[t][j] * g2 *
+//    sum of FC2 partials of (t, j)).  All sums run in a fixed order, so the
+//    result is deterministic;
+//  * the kernel is launched cooperatively (all CTAs resident, so the grid
+//    barriers cannot deadlock) and with programmatic dependent launch after
+//    the routing kernel, which also clears the barrier counters;
+//  * every wait is bounded: a wait that gives up sets the device error flag
+//    meta[1] and the CTA carries on without waiting again, so no CTA hangs.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "route_common.cuh"
+
+namespace qmoe {
+
+constexpr int kCons = 512;                 // consumer threads
+constexpr int kConsWarps = kCons / 32;
+constexpr int kLayerThreads = kCons + 32;  // + the weight-copy warp
+constexpr int kWarpW = kConsWarps;
+constexpr int kRing = 3;                   // weight ring slots (96 KB in flight per SM)
+constexpr int kTmaWB = 16;                 // blocks per scale window copied by the tensor unit
+constexpr int kTmaMaxNT = 1024;            // so that a window is at most 16 KB
+constexpr int kMaxWinBytes = 16 * 1024;
+constexpr int kMaxSegs = 16;               // segments of one FC in one CTA
+constexpr int kMaxCtas = 256;              // grid size (one CTA per SM)
+constexpr int kXsK = 2048;                 // activations staged per row at a time
+constexpr int kRowsMax = 2;                // rows decoded together (more rows: more passes)
+constexpr int kXrawSlot = kRowsMax * kXsK * 2;  // bytes of one raw (bf16) activation slot
+constexpr int kXrawBytes = 2 * kXrawSlot;        // two slots; FC2 reuses them as one buffer
+constexpr int kMaxSlots = 64;
+constexpr int kMaxTiles = 16;
+constexpr int kMaxPairs = kMaxSlots * kMaxTiles;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kSpinLimit = 1u << 24;
+static_assert(kCons == kRowsMax * (kXsK / 8), "one staged 8-value vector per consumer thread");
+
+// ---- PTX helpers --------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0u;
+}
+// 2-D tensor copy global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void tensor_g2s_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+// Consumer threads only (the copy and scale warps never take part).
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
+
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ---- scales and activation helpers -----------------------------------------------
+
+// Raw block scale as fp32.  NVFP4: E4M3 value * 2^-120 (exact); MXFP4: 2^(b-127).
+// `special` is set for codes that need the exact slow path (NaN; E8M0 0 / 255).
+template <int FMT>
+__device__ __forceinline__ float raw_scale(uint32_t b, bool &special) {
+  if (FMT == QMOE_NVFP4) {
+    special |= (b & 0x7Fu) == 0x7Fu;
+    const float f = __uint_as_float((b & 0x7Fu) << 20);
+    return (b & 0x80u) ? -f : f;
+  } else {
+    special |= (b == 0u) || (b == 0xFFu);
+    return __uint_as_float(b << 23);
+  }
+}
+template <int FMT>
+__device__ __forceinline__ float exact_raw_scale(uint32_t b) {
+  if (FMT == QMOE_NVFP4) return e4m3_to_f32(b) * 0x1p-120f;  // NaN stays NaN
+  return e8m0_to_f32(b);
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// x * 2^d for |d| <= 254 (two exact power-of-two steps).
+__device__ __forceinline__ float ldexp2(float x, int d) {
+  const int h = d / 2;
+  return x * pow2f(h) * pow2f(d - h);
+}
+
+__device__ __forceinline__ float swiglu(float gate, float lin, float alpha, float beta, float limit) {
+  const float G = fminf(gate, limit);
+  const float L = fmaxf(fminf(lin, limit), -limit);
+  return G * (1.0f / (1.0f + expf(-alpha * G))) * (L + beta);
+}
+
+// Shift that puts the largest |x| (bf16 bits, sign cleared) in [2^14, 2^15).
+__device__ __forceinline__ int row_shift(uint32_t m) {
+  return m == 0u ? 0 : max(-100, min(100, (int)((m >> 7) & 0xFFu) - 127 - 14));
+}
+
+__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4 &v) {
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) m = max(m, max(w4[q] & 0x7FFFu, (w4[q] >> 16) & 0x7FFFu));
+  return m;
+}
+
+// 8 bf16 -> 8 fp16 scaled by f (a power of two)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 &x4, float f) {
+  const uint32_t w4[4] = {x4.x, x4.y, x4.z, x4.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2 h = __floats2half2_rn(bf16_to_f32(w4[q] & 0xFFFFu) * f, bf16_to_f32(w4[q] >> 16) * f);
+    o[q] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// v_i byte q = scale of column i at block q  ->  row q of dst = the 4 columns' bytes
+__device__ __forceinline__ void store_tile4x4(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3, uint8_t *dst,
+                                              int stride, int rows) {
+  const uint32_t t01lo = __byte_perm(v0, v1, 0x5140), t01hi = __byte_perm(v0, v1, 0x7362);
+  const uint32_t t23lo = __byte_perm(v2, v3, 0x5140), t23hi = __byte_perm(v2, v3, 0x7362);
+  const uint32_t rr[4] = {__byte_perm(t01lo, t23lo, 0x5410), __byte_perm(t01lo, t23lo, 0x7632),
+                          __byte_perm(t01hi, t23hi, 0x5410), __byte_perm(t01hi, t23hi, 0x7632)};
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (q < rows) *reinterpret_cast<uint32_t *>(dst + (size_t)q * stride) = rr[q];
+}
+
+// ---- work geometry ------------------------------------------------------------------
+
+// Work split: the units of FC f, in (expert slot, column tile, k) order, are
+// cut into gridDim.x ranges of about equal cost, cost(unit) = 3 + 2 * rows for
+// an expert with `rows` rows (decoding a unit for two rows takes about 1.4x
+// one row; more rows are decoded two at a time); CTA c gets units
+// [bnd[f][c], bnd[f][c + 1]).
+__host__ __device__ __forceinline__ int unit_cost(int rows) { return 3 + 2 * rows; }
+
+struct FcWork {
+  int lo, hi;
+};
+// CTA holding unit u: the largest c with bnd[c] <= u (empty ranges skipped).
+__device__ __forceinline__ int cta_of(const int *bnd, int u) {
+  int lo = 0, hi = (int)gridDim.x - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (bnd[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+// Scale window holding the blocks of unit j (a unit never straddles two).
+template <int FMT>
+__device__ __forceinline__ int unit_window(const FcPlan &P, int j) {
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  return ((j * P.RGS * 16) / BS) / P.WB;
+}
+__device__ __forceinline__ int unit_rows(const FcPlan &P, int j) { return min(16 * P.RGS, P.K - j * 16 * P.RGS); }
+
+// A CTA's consecutive units of one (expert slot, column tile) pair.
+struct Seg {
+  int pair, a, t, j0, j1, wid0, wid1, pad;
+};
+
+struct Shared {
+  uint64_t full[kRing], empty[kRing];  // weight ring
+  uint64_t wfull[2], wempty[2];        // scale-window staging
+  uint64_t xfull[2], xempty[2];        // raw FC1 activation slots
+  uint64_t gsready;
+  int4 slot[kMaxSlots];                // {e, row0, nrows, -}
+  float gs[2][kMaxSlots];              // global scales per slot (1 for MXFP4)
+  int base[2][kMaxPairs + 1];          // partial-sum offsets (floats) per (slot, tile) pair
+  Seg seg[2][kMaxSegs];
+  int nseg[2];
+  int bnd[2][kMaxCtas + 1];            // work split (units)
+  short pcnt[2][kMaxPairs];            // partial-sum slots (CTAs holding units) of each pair
+  short busy[2][kMaxCtas + 1];         // CTAs holding units among [0, c)
+  int scum[2][kMaxSlots + 1];          // cost prefix over expert slots
+  int row2slot[kMaxSlots];
+  int row_tok[kMaxSlots];              // token of each permuted row
+  int r_e2p[kMaxSlots];                 // routing results of the routing kernel
+  float r_w[kMaxSlots];
+  uint32_t wmax[kConsWarps];
+  int na;
+  int abort;
+  int fc2_pre;                         // FC2 activations pre-staged in the raw buffer
+};
+
+__device__ __forceinline__ FcWork fc_work(const Shared &S, int f) {
+  return FcWork{S.bnd[f][blockIdx.x], S.bnd[f][blockIdx.x + 1]};
+}
+// The CTAs holding the first and the last unit of (expert slot, tile) pair p.
+__device__ __forceinline__ int first_cta(const Shared &S, const FcPlan &P, int f, int p) {
+  return cta_of(S.bnd[f], p * P.ku);
+}
+__device__ __forceinline__ int last_cta(const Shared &S, const FcPlan &P, int f, int p) {
+  return cta_of(S.bnd[f], p * P.ku + P.ku - 1);
+}
+// CTAs in [c0, c1) that hold at least one unit.  The partial-sum slots of a
+// pair are numbered by these only: a CTA with an empty range writes nothing.
+__device__ __forceinline__ int busy_ctas(const Shared &S, int f, int c0, int c1) {
+  return S.busy[f][c1] - S.busy[f][c0];
+}
+
+__device__ __forceinline__ bool wait_bar(Shared &S, const LayerArgs &g, uint64_t *bar, uint32_t parity) {
+  const uint32_t limit = *(volatile int *)&S.abort ? 64u : kWaitLimit;
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  *(volatile int *)&S.abort = 1;
+  pdl_wait();  // the routing kernel clears the flag: set it only after that
+  atomicExch(g.meta + 1, 1);
+  return false;
+}
+
+__device__ void grid_barrier(Shared &S, const LayerArgs &g, int32_t *ctr) {
+  cons_sync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1);
+    const uint32_t limit = *(volatile int *)&S.abort ? 1024u : kSpinLimit;
+    for (uint32_t i = 0; ld_acquire(ctr) < (int)gridDim.x; ++i) {
+      if (i >= limit) {
+        *(volatile int *)&S.abort = 1;
+        atomicExch(g.meta + 1, 1);  // after pdl_wait (grid_barrier's caller)
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  cons_sync();
+}
+
+// ---- set-up ----------------------------------------------------------------------------
+
+// This CTA's segments of FC f (one thread).
+template <int FMT>
+__device__ void build_segments(Shared &S, const LayerArgs &g, const FcPlan &P, int f) {
+  const FcWork W = fc_work(S, f);
+  int n = 0;
+  for (int u = W.lo; u < W.hi;) {
+    if (n == kMaxSegs) {  // the host bounds this; report rather than drop work
+      *(volatile int *)&S.abort = 1;
+      pdl_wait();
+      atomicExch(g.meta + 1, 1);
+      break;
+    }
+    const int pair = u / P.ku;
+    const int end = min(W.hi, (pair + 1) * P.ku);
+    Seg sg;
+    sg.pair = pair;
+    sg.a = pair / P.ct;
+    sg.t = pair - sg.a * P.ct;
+    sg.j0 = u - pair * P.ku;
+    sg.j1 = end - pair * P.ku;
+    sg.wid0 = unit_window<FMT>(P, sg.j0);
+    sg.wid1 = unit_window<FMT>(P, sg.j1 - 1);
+    sg.pad = 0;
+    S.seg[f][n++] = sg;
+    u = end;
+  }
+  S.nseg[f] = n;
+}
+
+// Cost prefix over the expert slots and the split boundaries of FC f.
+// Prefix: one warp; boundaries: threads [t0, t0 + G].
+__device__ void cost_prefix(Shared &S, const FcPlan &P, int f) {
+  const int lane = (int)lane_id();
+  const int per = (S.na + 31) / 32;
+  int sum = 0;
+  for (int q = 0; q < per; ++q) {
+    const int a = lane * per + q;
+    if (a < S.na) sum += P.ct * P.ku * unit_cost(S.slot[a].z);
+  }
+  int incl = sum;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+    if (lane >= m) incl += v;
+  }
+  int run = incl - sum;
+  for (int q = 0; q < per; ++q) {
+    const int a = lane * per + q;
+    if (a < S.na) {
+      S.scum[f][a] = run;
+      run += P.ct * P.ku * unit_cost(S.slot[a].z);
+    }
+  }
+  if (lane == 31) S.scum[f][S.na] = run;
+}
+// busy[f][c] = CTAs among [0, c) whose range is not empty (one warp).
+__device__ void busy_prefix(Shared &S, int f) {
+  const int lane = (int)lane_id(), G = (int)gridDim.x;
+  const int per = (G + 31) / 32;
+  int sum = 0;
+  for (int q = 0; q < per; ++q) {
+    const int c = lane * per + q;
+    if (c < G) sum += S.bnd[f][c] < S.bnd[f][c + 1];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+    if (lane >= m) incl += v;
+  }
+  int run = incl - sum;
+  for (int q = 0; q < per; ++q) {
+    const int c = lane * per + q;
+    if (c < G) {
+      S.busy[f][c] = (short)run;
+      run += S.bnd[f][c] < S.bnd[f][c + 1];
+    }
+  }
+  if (lane == 31) S.busy[f][G] = (short)run;
+}
+
+__device__ void split_bound(Shared &S, const FcPlan &P, int f, int c) {
+  const int G = (int)gridDim.x, na = S.na;
+  const int U = na * P.ct * P.ku;
+  if (c >= G) {
+    S.bnd[f][G] = U;
+    return;
+  }
+  const int total = S.scum[f][na];
+  const long long x = total < 0x7FFFFFFF / G ? (long long)((c * total) / G) : (long long)c * total / G;
+  int lo = 0, hi = na - 1;  // the last slot whose prefix is <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (S.scum[f][mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  const int cu = unit_cost(S.slot[lo].z);
+  const long long du = (x - S.scum[f][lo] + cu - 1) / cu;
+  S.bnd[f][c] = lo * P.ct * P.ku + (int)min(du, (long long)P.ct * P.ku);
+}
+
+// Exclusive prefix of the partial-sum sizes of all (slot, tile) pairs of FC f (one warp).
+__device__ void partial_bases(Shared &S, const FcPlan &P, int f) {
+  const int lane = (int)lane_id();
+  const int np = S.na * P.ct;
+  const int per = (np + 31) / 32;
+  int sum = 0;
+  for (int q = 0; q < per; ++q) {
+    const int p = lane * per + q;
+    if (p < np) {
+      const int cnt = busy_ctas(S, f, first_cta(S, P, f, p), last_cta(S, P, f, p) + 1);
+      S.pcnt[f][p] = (short)cnt;
+      sum += cnt * S.slot[p / P.ct].z * P.NT;
+    }
+  }
+  int incl = sum;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+    if (lane >= m) incl += v;
+  }
+  int run = incl - sum;
+  for (int q = 0; q < per; ++q) {
+    const int p = lane * per + q;
+    if (p < np) {
+      S.base[f][p] = run;
+      run += S.pcnt[f][p] * S.slot[p / P.ct].z * P.NT;
+    }
+  }
+  if (lane == 31) S.base[f][np] = run;
+}
+
+// ---- the copy warp --------------------------------------------------------------------
+
+// Every unit of the CTA, FC1 then FC2, in consumption order; before the first
+// unit of each scale window, that window's block scales (tensor copy).
+template <int FMT>
+__device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
+                                      uint8_t *stage, unsigned char *xraw) {
+  const int lane = (int)lane_id();
+  // global scales (needed after the first grid barrier): a few small loads,
+  // issued before the bulk copies so that they do not queue behind them
+  for (int i = lane; i < S.na; i += 32) {
+    S.gs[0][i] = g.g1 ? __ldg(g.g1 + S.slot[i].x) : 1.0f;
+    S.gs[1][i] = g.g2 ? __ldg(g.g2 + S.slot[i].x) : 1.0f;
+  }
+  mbar_arrive(&S.gsready);
+  uint32_t it = 0, wn = 0, xn = 0;
+  for (int f = 0; f < 2; ++f) {
+    const FcPlan &P = L.f[f];
+    const uint8_t *wbase = f == 0 ? g.w1 : g.w2;
+    const CUtensorMap *map = f == 0 ? &g.tm_s1 : &g.tm_s2;
+    const uint32_t row_bytes = (uint32_t)(P.NT / 2);
+    for (int si = 0; si < S.nseg[f]; ++si) {
+      const Seg sg = S.seg[f][si];
+      const int4 sd = S.slot[sg.a];
+      const uint8_t *wexp = wbase + (size_t)sd.x * P.K * (P.N / 2) + (size_t)sg.t * row_bytes;
+      const int col0 = sd.x * P.N + sg.t * P.NT;  // first scale row of the tile
+      const int unit_k = 16 * P.RGS, xw_units = kXsK / unit_k;
+      for (int c0 = 0; c0 < sd.z; c0 += kRowsMax) {
+        const int rows_p = min(kRowsMax, sd.z - c0);
+        int cur = -1;
+        for (int j = sg.j0; j < sg.j1; ++j, ++it) {
+          if (f == 0 && (j - sg.j0) % xw_units == 0) {
+            // FC1: the activation rows of this k window, ahead of its weights
+            const int k0 = j * unit_k, len = min(P.K, min(sg.j1, j + xw_units) * unit_k) - k0;
+            const int s = (int)(xn & 1u);
+            if (xn >= 2u) {
+              if (lane == 0) wait_bar(S, g, &S.xempty[s], ((xn >> 1) + 1u) & 1u);
+              __syncwarp();
+            }
+            if (lane == 0) mbar_expect_tx(&S.xfull[s], (uint32_t)(rows_p * len * 2));
+            __syncwarp();
+            if (lane < rows_p) {
+              const int tok = S.row_tok[sd.y + c0 + lane];
+              bulk_g2s(xraw + (size_t)s * kXrawSlot + (size_t)lane * kXsK * 2, g.x + (size_t)tok * g.H + k0,
+                       (uint32_t)(len * 2), &S.xfull[s]);
+            }
+            ++xn;
+          }
+          const int wid = unit_window<FMT>(P, j);
+          if (P.tma && wid != cur) {
+            const int s = (int)(wn & 1u);
+            if (wn >= 2u) {
+              if (lane == 0) wait_bar(S, g, &S.wempty[s], ((wn >> 1) + 1u) & 1u);
+              __syncwarp();
+            }
+            uint8_t *dst = stage + (size_t)s * L.win_bytes;
+            if (lane == 0) mbar_expect_tx(&S.wfull[s], (uint32_t)(P.NT * kTmaWB));
+            __syncwarp();
+            for (int r = lane * P.box_rows; r < P.NT; r += 32 * P.box_rows)
+              tensor_g2s_2d(dst + (size_t)r * kTmaWB, map, wid * kTmaWB, col0 + r, &S.wfull[s]);
+            ++wn;
+            cur = wid;
+          }
+          const int s = (int)(it % kRing);
+          if (it >= (uint32_t)kRing) {
+            if (lane == 0) wait_bar(S, g, &S.empty[s], ((it / kRing) + 1u) & 1u);
+            __syncwarp();
+          }
+          unsigned char *dst = ring + (size_t)s * L.slot_bytes;
+          const int r0 = j * 16 * P.RGS, rows = unit_rows(P, j);
+          // the slot was only read by the consumers (generic loads) before they
+          // released it: no proxy fence is needed before the async copy writes it
+          if (lane == 0) mbar_expect_tx(&S.full[s], (uint32_t)rows * row_bytes);
+          __syncwarp();
+          if (P.ct == 1) {
+            if (lane == 0) bulk_g2s(dst, wexp + (size_t)r0 * row_bytes, (uint32_t)rows * row_bytes, &S.full[s]);
+          } else {
+            for (int r = lane; r < rows; r += 32)
+              bulk_g2s(dst + (size_t)r * row_bytes, wexp + (size_t)(r0 + r) * (P.N / 2), row_bytes, &S.full[s]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---- consumers -------------------------------------------------------------------------
+
+// The 8 E2M1 codes of a word -> 4 f16x2 (byte q -> p[q]; low nibble in the low half).
+__device__ __forceinline__ void dec8(uint32_t w, uint32_t (&p)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3])
+      : "r"(w));
+}
+// a[c] += p[c] * x.lo + q[c] * x.hi for the 8 columns c, fp16 operands with
+// exact products (fma.rn.f32.f16), fp32 accumulation; x = the fp16 pair of
+// two consecutive k rows (p: the word of the first row, q: of the second).
+__device__ __forceinline__ void fma16(const uint32_t (&p)[4], const uint32_t (&q)[4], uint32_t x2, float (&a)[8]) {
+  asm("{ .reg .f16 x0, x1, l0, h0, l1, h1, l2, h2, l3, h3;\n mov.b32 {x0, x1}, %16;\n"
+      " mov.b32 {l0, h0}, %8;\n mov.b32 {l1, h1}, %9;\n mov.b32 {l2, h2}, %10;\n mov.b32 {l3, h3}, %11;\n"
+      " fma.rn.f32.f16 %0, l0, x0, %0;\n fma.rn.f32.f16 %1, h0, x0, %1;\n"
+      " fma.rn.f32.f16 %2, l1, x0, %2;\n fma.rn.f32.f16 %3, h1, x0, %3;\n"
+      " fma.rn.f32.f16 %4, l2, x0, %4;\n fma.rn.f32.f16 %5, h2, x0, %5;\n"
+      " fma.rn.f32.f16 %6, l3, x0, %6;\n fma.rn.f32.f16 %7, h3, x0, %7;\n"
+      " mov.b32 {l0, h0}, %12;\n mov.b32 {l1, h1}, %13;\n mov.b32 {l2, h2}, %14;\n mov.b32 {l3, h3}, %15;\n"
+      " fma.rn.f32.f16 %0, l0, x1, %0;\n fma.rn.f32.f16 %1, h0, x1, %1;\n"
+      " fma.rn.f32.f16 %2, l1, x1, %2;\n fma.rn.f32.f16 %3, h1, x1, %3;\n"
+      " fma.rn.f32.f16 %4, l2, x1, %4;\n fma.rn.f32.f16 %5, h2, x1, %5;\n"
+      " fma.rn.f32.f16 %6, l3, x1, %6;\n fma.rn.f32.f16 %7, h3, x1, %7; }"
+      : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3]), "+f"(a[4]), "+f"(a[5]), "+f"(a[6]), "+f"(a[7])
+      : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3]), "r"(x2));
+}
+
+// Two activation rows: the words of k rows k and k+1 are decoded once and
+// accumulated into both rows' 8 column sums inside one asm block (no decoded
+// value outlives it, which keeps the two-row loop within its registers).
+__device__ __forceinline__ void dfma_r2(uint32_t w0, uint32_t w1, uint32_t xa, uint32_t xb, float (&a)[8],
+                                        float (&b)[8]) {
+  asm("{ .reg .b8 b0, b1, b2, b3, c0, c1, c2, c3; .reg .b32 p0, p1, p2, p3, q0, q1, q2, q3;\n"
+      " .reg .f16 xa0, xa1, xb0, xb1, l0, h0, l1, h1, l2, h2, l3, h3;\n"
+      " mov.b32 {b0, b1, b2, b3}, %16;\n mov.b32 {c0, c1, c2, c3}, %17;\n"
+      " mov.b32 {xa0, xa1}, %18;\n mov.b32 {xb0, xb1}, %19;\n"
+      " cvt.rn.f16x2.e2m1x2 p0, b0;\n cvt.rn.f16x2.e2m1x2 p1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 p2, b2;\n cvt.rn.f16x2.e2m1x2 p3, b3;\n"
+      " mov.b32 {l0, h0}, p0;\n mov.b32 {l1, h1}, p1;\n mov.b32 {l2, h2}, p2;\n mov.b32 {l3, h3}, p3;\n"
+      " fma.rn.f32.f16 %0, l0, xa0, %0;\n fma.rn.f32.f16 %1, h0, xa0, %1;\n"
+      " fma.rn.f32.f16 %2, l1, xa0, %2;\n fma.rn.f32.f16 %3, h1, xa0, %3;\n"
+      " fma.rn.f32.f16 %4, l2, xa0, %4;\n fma.rn.f32.f16 %5, h2, xa0, %5;\n"
+      " fma.rn.f32.f16 %6, l3, xa0, %6;\n fma.rn.f32.f16 %7, h3, xa0, %7;\n"
+      " fma.rn.f32.f16 %8, l0, xb0, %8;\n fma.rn.f32.f16 %9, h0, xb0, %9;\n"
+      " fma.rn.f32.f16 %10, l1, xb0, %10;\n fma.rn.f32.f16 %11, h1, xb0, %11;\n"
+      " fma.rn.f32.f16 %12, l2, xb0, %12;\n fma.rn.f32.f16 %13, h2, xb0, %13;\n"
+      " fma.rn.f32.f16 %14, l3, xb0, %14;\n fma.rn.f32.f16 %15, h3, xb0, %15;\n"
+      " cvt.rn.f16x2.e2m1x2 q0, c0;\n cvt.rn.f16x2.e2m1x2 q1, c1;\n"
+      " cvt.rn.f16x2.e2m1x2 q2, c2;\n cvt.rn.f16x2.e2m1x2 q3, c3;\n"
+      " mov.b32 {l0, h0}, q0;\n mov.b32 {l1, h1}, q1;\n mov.b32 {l2, h2}, q2;\n mov.b32 {l3, h3}, q3;\n"
+      " fma.rn.f32.f16 %0, l0, xa1, %0;\n fma.rn.f32.f16 %1, h0, xa1, %1;\n"
+      " fma.rn.f32.f16 %2, l1, xa1, %2;\n fma.rn.f32.f16 %3, h1, xa1, %3;\n"
+      " fma.rn.f32.f16 %4, l2, xa1, %4;\n fma.rn.f32.f16 %5, h2, xa1, %5;\n"
+      " fma.rn.f32.f16 %6, l3, xa1, %6;\n fma.rn.f32.f16 %7, h3, xa1, %7;\n"
+      " fma.rn.f32.f16 %8, l0, xb1, %8;\n fma.rn.f32.f16 %9, h0, xb1, %9;\n"
+      " fma.rn.f32.f16 %10, l1, xb1, %10;\n fma.rn.f32.f16 %11, h1, xb1, %11;\n"
+      " fma.rn.f32.f16 %12, l2, xb1, %12;\n fma.rn.f32.f16 %13, h2, xb1, %13;\n"
+      " fma.rn.f32.f16 %14, l3, xb1, %14;\n fma.rn.f32.f16 %15, h3, xb1, %15; }"
+      : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3]), "+f"(a[4]), "+f"(a[5]), "+f"(a[6]), "+f"(a[7]),
+        "+f"(b[0]), "+f"(b[1]), "+f"(b[2]), "+f"(b[3]), "+f"(b[4]), "+f"(b[5]), "+f"(b[6]), "+f"(b[7])
+      : "r"(w0), "r"(w1), "r"(xa), "r"(xb));
+}
+
+// One k-group (16 rows x 8 columns) of a unit for RC activation rows: each
+// word is decoded once and used for every row.
+template <int FMT>
+__device__ __forceinline__ void block_scales8(uint2 sv, float (&sc)[8]) {
+  bool special = false;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) sc[c] = raw_scale<FMT>(((c < 4 ? sv.x : sv.y) >> (8 * (c & 3))) & 0xFFu, special);
+  if (special) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) sc[c] = exact_raw_scale<FMT>(((c < 4 ? sv.x : sv.y) >> (8 * (c & 3))) & 0xFFu);
+  }
+}
+
+template <int FMT, int RC>
+__device__ __forceinline__ void consume_kg(const unsigned char *rows, int row_bytes, const __half *xb, uint2 sv,
+                                           float (&acc)[RC][8]) {
+  static_assert(RC == 1 || RC == 2, "one or two rows per pass");
+  float bp[RC][8];
+#pragma unroll
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) bp[r][c] = 0.f;
+  // 8 k rows at a time; the loop is not unrolled so that the words of one
+  // half are not kept alive alongside the other's (spills would go to L2:
+  // almost all of the SM's memory is shared memory here)
+#pragma unroll 1
+  for (int g8 = 0; g8 < 16; g8 += 8) {
+    uint32_t wv[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) wv[kk] = *reinterpret_cast<const uint32_t *>(rows + (size_t)(g8 + kk) * row_bytes);
+    uint4 x8[RC];
+#pragma unroll
+    for (int r = 0; r < RC; ++r) x8[r] = *reinterpret_cast<const uint4 *>(xb + (size_t)r * kXsK + g8);
+#pragma unroll
+    for (int kk = 0; kk < 8; kk += 2) {
+      const uint32_t xa = kk == 0 ? x8[0].x : kk == 2 ? x8[0].y : kk == 4 ? x8[0].z : x8[0].w;
+      if (RC == 1) {
+        uint32_t p[4], q[4];
+        dec8(wv[kk], p);
+        dec8(wv[kk + 1], q);
+        fma16(p, q, xa, bp[0]);
+      } else {
+        const uint32_t xb2 = kk == 0 ? x8[RC - 1].x : kk == 2 ? x8[RC - 1].y : kk == 4 ? x8[RC - 1].z : x8[RC - 1].w;
+        dfma_r2(wv[kk], wv[kk + 1], xa, xb2, bp[0], bp[RC - 1]);
+      }
+    }
+  }
+  float sc[8];
+  block_scales8<FMT>(sv, sc);
+#pragma unroll
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(bp[r][c], sc[c], acc[r][c]);
+}
+
+struct PassCtx {
+  int f, a, t, pair, c0, rows, j0, j1;
+  int4 sd;
+  float *dst;  // partial rows of this segment: dst[row * NT + col], row = c0 + r
+};
+
+// Window boundary (all consumer threads): the block scales of window `wid` of
+// the pass's tile -> win[b][col].  Tensor-copied windows are read from staging
+// slot wn & 1 ([col][16] bytes) and the slot is handed back to the copy warp.
+// Out of line, arguments by value: the hot loop's state stays in registers.
+// Returns the next window count.
+template <int FMT>
+__device__ __noinline__ uint32_t enter_window(Shared &S, const LayerArgs &g, const LayerPlan &L, int f, int e, int t,
+                                              int wid, uint8_t *win, const uint8_t *stage, uint32_t wn) {
+  const FcPlan &P = L.f[f];
+  const int b0 = wid * P.WB, nb = min(P.WB, P.nblocks - b0);
+  if (P.tma) {
+    // Per thread, no CTA barrier: the thread's 8 columns' 16-byte runs (8
+    // loads), of which it keeps the bytes of its own blocks (u * RGS + rg for
+    // the window's 16 / RGS units), one 8-byte word (8 columns) per unit in
+    // its private slots win[u][tid].
+    const int s = (int)(wn & 1u);
+    wait_bar(S, g, &S.wfull[s], (wn >> 1) & 1u);
+    const int tid = threadIdx.x, w = tid % P.NW, rg = tid / P.NW;
+    if (rg < P.RGS) {
+      // step i: column 8w + ((i + w) % 8), so that 8 neighbouring lanes read 8
+      // different 16-byte bank groups; its bytes go to byte (column % 8) of the
+      // unit's word
+      const uint8_t *src = stage + (size_t)s * L.win_bytes + (size_t)w * 128;
+      const int upw = kTmaWB / P.RGS;  // 1, 2 or 4
+      uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = (i + w) & 7;
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + (c << 4));
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (u < upw) {
+            const int b = u * P.RGS + rg;  // block of unit u of the window
+            const uint32_t byte = (vw[b >> 2] >> (8 * (b & 3))) & 0xFFu;
+            if (c < 4) lo[u] |= byte << (8 * c); else hi[u] |= byte << (8 * (c - 4));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (u < upw) reinterpret_cast<uint2 *>(win)[(size_t)u * kCons + threadIdx.x] = make_uint2(lo[u], hi[u]);
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&S.wempty[s]);
+    ++wn;
+  } else {
+    cons_sync();
+    const uint8_t *scol = (f == 0 ? g.s1 : g.s2) + ((size_t)e * P.N + (size_t)t * P.NT) * P.nblocks + b0;
+    const int groups = P.NT / 4, bgroups = (nb + 3) / 4;
+    for (int job = threadIdx.x; job < groups * bgroups; job += kCons) {
+      const int c4 = job / bgroups, bq = (job - c4 * bgroups) * 4;
+      uint32_t v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t *src = scol + (size_t)(4 * c4 + i) * P.nblocks + bq;
+        uint32_t x = 0;
+        for (int q = 0; q < 4 && bq + q < nb; ++q) x |= (uint32_t)__ldg(src + q) << (8 * q);
+        v[i] = x;
+      }
+      store_tile4x4(v[0], v[1], v[2], v[3], win + (size_t)bq * P.NT + 4 * c4, P.NT, min(4, nb - bq));
+    }
+    cons_sync();
+  }
+  return wn;
+}
+
+// a[row][k] = bf16(SwiGLU(g1 * h)) for FC2's activations, h = the FC1 partial
+// sums of this row (row c0 + rr of slot a) summed in segment order.
+__device__ __forceinline__ uint16_t fc2_activation(const Shared &S, const LayerArgs &g, const LayerPlan &L, int a,
+                                                   int nrows, int row, int k) {
+  const FcPlan &P1 = L.f[0];
+  const int col = 2 * k;
+  const int t1 = col / P1.NT, c1 = col - t1 * P1.NT;
+  const int pair = a * P1.ct + t1;
+  const int nc = S.pcnt[0][pair];
+  const size_t stride = (size_t)nrows * P1.NT;
+  const float *src = g.p1 + S.base[0][pair] + (size_t)row * P1.NT + c1;
+  float hg = 0.f, hl = 0.f;
+  for (int c = 0; c < nc; c += 8) {  // up to 8 loads in flight, summed in segment order
+    float2 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = c + u < nc ? __ldcg(reinterpret_cast<const float2 *>(src + (c + u) * stride)) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (c + u < nc) { hg += v[u].x; hl += v[u].y; }
+  }
+  const float g1 = S.gs[0][a];
+  return (uint16_t)f32_to_bf16_rne(swiglu(hg * g1, hl * g1, g.alpha, g.beta, g.limit));
+}
+
+// Stages activation rows [c0, c0 + rows) of the pass, k in [k0, k0 + len), as
+// fp16 in xs with a per-row power-of-two rescale; returns the shifts in sh[].
+// Raw bf16 rows come from: FC1, raw slot xn & 1 (bulk-copied by the copy
+// warp); FC2, the pre-staged buffer (row stride len) at *pre_off, or, when
+// pre-staging did not fit, they are computed here from the FC1 partials.
+template <int RC>
+__device__ __forceinline__ void stage_activations(Shared &S, const LayerArgs &g, const LayerPlan &L,
+                                                  const PassCtx &C, int k0, int len, __half *xs,
+                                                  const unsigned char *xraw, uint32_t &xn, int &pre_off,
+                                                  int (&sh)[RC]) {
+  const int tid = threadIdx.x, r = tid >> 8, q = tid & 255;
+  const bool valid = r < C.rows && 8 * q < len;
+  uint4 *vec = reinterpret_cast<uint4 *>(xs + (size_t)r * kXsK) + q;
+  const uint16_t *src = nullptr;
+  int stride = kXsK;
+  cons_sync();  // the previous window's activations are no longer read
+  if (C.f == 0) {
+    const int s = (int)(xn & 1u);
+    wait_bar(S, g, &S.xfull[s], (xn >> 1) & 1u);
+    src = reinterpret_cast<const uint16_t *>(xraw + (size_t)s * kXrawSlot);
+  } else if (S.fc2_pre) {
+    src = reinterpret_cast<const uint16_t *>(xraw) + pre_off;
+    stride = len;
+    pre_off += C.rows * len;
+  } else {
+    uint16_t *xb = reinterpret_cast<uint16_t *>(xs);
+    for (int i = tid; i < C.rows * len; i += kCons) {
+      const int rr = i / len, kk = i - rr * len;
+      xb[(size_t)rr * kXsK + kk] = fc2_activation(S, g, L, C.a, C.sd.z, C.c0 + rr, k0 + kk);
+    }
+    cons_sync();
+    src = xb;
+  }
+  const uint4 v = valid ? *reinterpret_cast<const uint4 *>(src + (size_t)r * stride + 8 * q) : make_uint4(0, 0, 0, 0);
+  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, absmax_bf16x8(v));
+  if ((tid & 31) == 0) S.wmax[tid >> 5] = m;
+  cons_sync();  // every raw value has been read
+  if (C.f == 0) {
+    if ((tid & 31) == 0) mbar_arrive(&S.xempty[xn & 1u]);
+    ++xn;
+  }
+  uint32_t mrow[kRowsMax];
+#pragma unroll
+  for (int rr = 0; rr < kRowsMax; ++rr) {
+    uint32_t mm = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mm = max(mm, S.wmax[8 * rr + i]);
+    mrow[rr] = mm;
+  }
+#pragma unroll
+  for (int rr = 0; rr < RC; ++rr) sh[rr] = row_shift(mrow[rr]);
+  const int shr = row_shift(r == 0 ? mrow[0] : mrow[1]);
+  *vec = bf16x8_to_f16x8(v, pow2f(-shr));
+  cons_sync();
+}
+
+// FC2's activations of every pass of this CTA, computed once right after the
+// first grid barrier (while the memory system is quiet) into the raw buffer,
+// pass after pass, row stride = the pass's k length.  Returns false (nothing
+// staged) when a pass needs more than one staging window or the buffer is
+// too small.
+__device__ bool prestage_fc2(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *xraw) {
+  const FcPlan &P = L.f[1];
+  const int unit_k = 16 * P.RGS;
+  int total = 0;
+  for (int si = 0; si < S.nseg[1]; ++si) {
+    const Seg sg = S.seg[1][si];
+    const int len = min(P.K, sg.j1 * unit_k) - sg.j0 * unit_k;
+    if (len > kXsK) return false;
+    total += S.slot[sg.a].z * len;
+  }
+  if (total * 2 > kXrawBytes) return false;
+  uint16_t *dst = reinterpret_cast<uint16_t *>(xraw);
+  for (int si = 0; si < S.nseg[1]; ++si) {
+    const Seg sg = S.seg[1][si];
+    const int4 sd = S.slot[sg.a];
+    const int k0 = sg.j0 * unit_k, len = min(P.K, sg.j1 * unit_k) - k0;
+    for (int c0 = 0; c0 < sd.z; c0 += kRowsMax) {
+      const int rows = min(kRowsMax, sd.z - c0);
+      for (int i = threadIdx.x; i < rows * len; i += kCons) {
+        const int rr = i / len, kk = i - rr * len;
+        dst[i] = fc2_activation(S, g, L, sg.a, sd.z, c0 + rr, k0 + kk);
+      }
+      dst += rows * len;
+    }
+  }
+  return true;
+}
+
+template <int FMT, int RC>
+__device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const LayerPlan &L, const PassCtx &C,
+                                         unsigned char *ring, uint8_t *win, const uint8_t *stage, __half *xs,
+                                         const unsigned char *xraw, float *red, uint32_t &it, uint32_t &wn,
+                                         uint32_t &xn, int &pre_off) {
+  const FcPlan &P = L.f[C.f];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int w = tid % P.NW, rg = tid / P.NW;
+  const int row_bytes = P.NT / 2;
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  float acc[RC][8];
+#pragma unroll
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+  int sh[RC];
+#pragma unroll
+  for (int r = 0; r < RC; ++r) sh[r] = 0;
+  const int unit_k = 16 * P.RGS;
+  const int xw_units = kXsK / unit_k;
+  int cur_wid = -1;
+  for (int xj = C.j0; xj < C.j1; xj += xw_units) {
+    const int xj1 = min(C.j1, xj + xw_units);
+    const int k0 = xj * unit_k, len = min(P.K, xj1 * unit_k) - k0;
+    int nsh[RC];
+    stage_activations<RC>(S, g, L, C, k0, len, xs, xraw, xn, pre_off, nsh);
+    if (xj != C.j0) {
+#pragma unroll
+      for (int r = 0; r < RC; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = ldexp2(acc[r][c], sh[r] - nsh[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < RC; ++r) sh[r] = nsh[r];
+    for (int j = xj; j < xj1; ++j, ++it) {
+      const int wid = unit_window<FMT>(P, j);
+      if (wid != cur_wid) {
+        wn = enter_window<FMT>(S, g, L, C.f, C.sd.x, C.t, wid, win, stage, wn);
+        cur_wid = wid;
+      }
+      const int s = (int)(it % kRing);
+      wait_bar(S, g, &S.full[s], (it / kRing) & 1u);
+      const int kg = j * P.RGS + rg;
+      if (rg < P.RGS && kg < P.nkg) {
+        const unsigned char *rows = ring + (size_t)s * L.slot_bytes + (size_t)(rg * 16) * row_bytes + 4 * w;
+        uint2 sv;
+        if (P.tma) {
+          sv = reinterpret_cast<const uint2 *>(win)[(size_t)(j % (kTmaWB / P.RGS)) * kCons + tid];
+        } else {
+          const int blk = (kg * 16) / BS - cur_wid * P.WB;
+          sv = *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
+        }
+        const __half *xb = xs + (kg * 16 - k0);
+        consume_kg<FMT, RC>(rows, row_bytes, xb, sv, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
+    }
+  }
+  // reduce the row groups in a fixed order and write the partial rows:
+  // red[rg][r][col], one barrier for all rows
+  const float fold = FMT == QMOE_NVFP4 ? 0x1p120f : 1.0f;
+  cons_sync();  // red is free
+  if (rg < P.RGS) {
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+      float4 *d = reinterpret_cast<float4 *>(red + ((size_t)rg * kRowsMax + r) * P.NT + 8 * w);
+      d[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      d[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+    }
+  }
+  cons_sync();
+  for (int i = tid; i < C.rows * P.NT; i += kCons) {
+    const int r = i / P.NT, col = i - r * P.NT;
+    float sum = 0.f;
+    for (int q = 0; q < P.RGS; ++q) sum += red[((size_t)q * kRowsMax + r) * P.NT + col];
+    // fold first: sum * 2^120 is near the rescaled row's magnitude, so
+    // undoing the 2^-shift afterwards cannot underflow
+    C.dst[(size_t)(C.c0 + r) * P.NT + col] = sum * fold * pow2f(r == 0 ? sh[0] : sh[RC - 1]);
+  }
+}
+
+// out[t][n] = bf16(sum_j w[t][j] * g2 * y_j[n]), once every FC2 partial is
+// written: 8 lanes per column pair, lane j gathers expert j's FC2 partials; the
+// lanes are summed by a fixed butterfly.
+__device__ __noinline__ void finalize(Shared &S, const LayerArgs &g, const LayerPlan &L) {
+  const FcPlan &P2 = L.f[1];
+  const int half = g.H / 2;
+  const int items = g.T * half * 8;
+  const int items_pad = (items + 31) & ~31;
+  for (int idx = (int)blockIdx.x * kCons + (int)threadIdx.x; idx < items_pad; idx += (int)gridDim.x * kCons) {
+    const int grp = idx >> 3, j = idx & 7;
+    const bool ok = grp < g.T * half && j < g.k;
+    float y0 = 0.f, y1 = 0.f;
+    int t = 0, n = 0;
+    if (ok) {
+      t = grp / half;
+      n = 2 * (grp - t * half);
+      const int ex = t * g.k + j;
+      const int p = S.r_e2p[ex];
+      const int a = S.row2slot[p];
+      const int4 sd = S.slot[a];
+      const int t2 = n / P2.NT, col = n - t2 * P2.NT;
+      const int pair = a * P2.ct + t2;
+      const int nc = S.pcnt[1][pair];
+      const size_t stride = (size_t)sd.z * P2.NT;
+      const float *src = g.p2 + S.base[1][pair] + (size_t)(p - sd.y) * P2.NT + col;
+      float s0 = 0.f, s1 = 0.f;
+      for (int c = 0; c < nc; c += 8) {  // up to 8 loads in flight, summed in segment order
+        float2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = c + u < nc ? __ldcg(reinterpret_cast<const float2 *>(src + (c + u) * stride)) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c + u < nc) { s0 += v[u].x; s1 += v[u].y; }
+      }
+      const float wgt = S.r_w[ex], g2 = S.gs[1][a];
+      y0 = wgt * (s0 * g2);
+      y1 = wgt * (s1 * g2);
+    }
+#pragma unroll
+    for (int m = 4; m > 0; m >>= 1) {
+      y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, m);
+      y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, m);
+    }
+    if (ok && j == 0)
+      reinterpret_cast<uint32_t *>(g.out + (size_t)t * g.H)[n / 2] = f32_to_bf16_rne(y0) | (f32_to_bf16_rne(y1) << 16);
+  }
+}
+
+template <int FMT>
+__device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
+                                      uint8_t *win, const uint8_t *stage, __half *xs, unsigned char *xraw,
+                                      float *red) {
+  uint32_t it = 0, wn = 0, xn = 0;
+  int pre_off = 0;
+  for (int f = 0; f < 2; ++f) {
+    const FcPlan &P = L.f[f];
+    if (f == 1) {
+      grid_barrier(S, g, g.meta + 2);  // every FC1 partial is written
+      wait_bar(S, g, &S.gsready, 0u);
+      const bool pre = prestage_fc2(S, g, L, xraw);
+      if (threadIdx.x == 0) S.fc2_pre = pre ? 1 : 0;
+      cons_sync();
+    }
+    for (int si = 0; si < S.nseg[f]; ++si) {
+      const Seg sg = S.seg[f][si];
+      PassCtx C;
+      C.f = f;
+      C.pair = sg.pair;
+      C.a = sg.a;
+      C.t = sg.t;
+      C.sd = S.slot[sg.a];
+      C.j0 = sg.j0;
+      C.j1 = sg.j1;
+      C.dst = (f == 0 ? g.p1 : g.p2) + S.base[f][sg.pair] +
+              (size_t)busy_ctas(S, f, first_cta(S, P, f, sg.pair), (int)blockIdx.x) * C.sd.z * P.NT;
+      for (int c0 = 0; c0 < C.sd.z; c0 += kRowsMax) {
+        C.c0 = c0;
+        C.rows = min(kRowsMax, C.sd.z - c0);
+        if (C.rows == 1)
+          run_pass<FMT, 1>(S, g, L, C, ring, win, stage, xs, xraw, red, it, wn, xn, pre_off);
+        else
+          run_pass<FMT, 2>(S, g, L, C, ring, win, stage, xs, xraw, red, it, wn, xn, pre_off);
+      }
+    }
+  }
+  grid_barrier(S, g, g.meta + 3);  // every FC2 partial is written
+  finalize(S, g, L);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __grid_constant__ LayerArgs g,
+                                                                   const __grid_constant__ LayerPlan L) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Shared S;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kConsWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.wfull[i], 1);
+      mbar_init(&S.wempty[i], kConsWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.xfull[i], 1);
+      mbar_init(&S.xempty[i], kConsWarps);
+    }
+    mbar_init(&S.gsready, 32);
+    mbar_fence_init();
+    S.abort = 0;
+    S.fc2_pre = 0;
+  }
+  pdl_wait();  // the routing results (and the cleared counters) are complete
+  // one round of loads: the active-expert count, every slot (read before the
+  // count is known), and per row its token, permuted position and weight
+  const int R = g.T * g.k;
+  const int nslots = min(min(g.E, R), kMaxSlots);
+  int4 sd = make_int4(0, 0, 0, 0);
+  if (tid < nslots) sd = __ldcg(reinterpret_cast<const int4 *>(g.slots) + tid);
+  if (tid >= 64 && tid - 64 < R) S.row_tok[tid - 64] = __ldcg(g.p2e + (tid - 64)) / g.k;
+  if (tid >= 128 && tid - 128 < R) S.r_e2p[tid - 128] = __ldcg(g.e2p + (tid - 128));
+  if (tid >= 192 && tid - 192 < R) S.r_w[tid - 192] = __ldcg(g.weights + (tid - 192));
+  if (tid == 256) S.na = min(__ldcg(g.meta), kMaxSlots);
+  __syncthreads();
+  const int na = S.na;
+  if (na <= 0) return;  // every CTA sees the same count
+  if (tid < na) {
+    S.slot[tid] = sd;
+    for (int q = 0; q < sd.z; ++q) S.row2slot[sd.y + q] = tid;
+  }
+  __syncthreads();
+  if (warp < 2) cost_prefix(S, L.f[warp], warp);
+  __syncthreads();
+  {
+    const int G = (int)gridDim.x;
+    if (tid <= G) split_bound(S, L.f[0], 0, tid);
+    else if (tid <= 2 * G + 1) split_bound(S, L.f[1], 1, tid - G - 1);
+  }
+  __syncthreads();
+  if (warp < 2) busy_prefix(S, warp);
+  __syncthreads();
+  if (warp < 2) partial_bases(S, L.f[warp], warp);
+  if (warp == 2 && (tid & 31) == 0) build_segments<FMT>(S, g, L.f[0], 0);
+  if (warp == 3 && (tid & 31) == 0) build_segments<FMT>(S, g, L.f[1], 1);
+  __syncthreads();
+  // 1 KB-aligned regions (the tensor and bulk copies need 16-byte alignment)
+  unsigned char *base = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
+  unsigned char *ring = base;
+  uint8_t *win = base + L.sw_off;
+  uint8_t *stage = base + L.st_off;
+  __half *xs = reinterpret_cast<__half *>(base + L.xs_off);
+  unsigned char *xraw = base + L.xr_off;
+  float *red = reinterpret_cast<float *>(base + L.red_off);
+  if (warp == kWarpW)
+    producer<FMT>(S, g, L, ring, stage, xraw);
+  else
+    consumer<FMT>(S, g, L, ring, win, stage, xs, xraw, red);
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+static bool make_fc_plan(int fmt, int K, int N, int BS, FcPlan &P) {
+  const int nblocks = K / BS;
+  // tensor-copied scale windows: NVFP4 (one block per k-group, so a thread
+  // needs 16 / RGS <= 4 blocks of a window) with whole 16-block windows
+  bool tma = fmt == QMOE_NVFP4 && nblocks % kTmaWB == 0;
+  int best_busy = 0;
+  P = FcPlan{};
+  for (int ct = 1; ct <= kMaxTiles; ++ct) {
+    if (N % ct) continue;
+    const int NT = N / ct;
+    if (NT % 32) continue;
+    if (tma && (NT > kTmaMaxNT || NT % 64)) continue;
+    const int NW = NT / 8;
+    if (NW > kCons) continue;
+    int RGS = 1;
+    while (NW * RGS * 2 <= kCons && RGS < 16) RGS *= 2;
+    if (NW * RGS > best_busy) {
+      best_busy = NW * RGS;
+      P.ct = ct;
+      P.NT = NT;
+      P.NW = NW;
+      P.RGS = RGS;
+    }
+  }
+  if (best_busy == 0) {
+    if (!tma) return false;
+    return make_fc_plan(QMOE_MXFP4 + 1, K, N, BS, P);  // no tensor-copy tiling: plain windows
+  }
+  P.K = K;
+  P.N = N;
+  P.nkg = K / 16;
+  P.ku = (P.nkg + P.RGS - 1) / P.RGS;
+  P.nblocks = nblocks;
+  P.tma = tma ? 1 : 0;
+  int WB = kTmaWB;
+  if (!tma)
+    while (WB * P.NT > kMaxWinBytes) WB /= 2;
+  const int bpu = (P.RGS * 16) / BS > 0 ? (P.RGS * 16) / BS : 1;
+  if (WB < bpu) return false;
+  P.WB = WB;
+  P.box_rows = 256;
+  while (P.NT % P.box_rows) P.box_rows /= 2;
+  if (tma && (P.box_rows < 64 || P.RGS < 4)) {  // <= 4 blocks of a window per thread
+    return make_fc_plan(QMOE_MXFP4 + 1, K, N, BS, P);
+  }
+  return true;
+}
+
+qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPlan &L, size_t &p1_floats,
+                            size_t &p2_floats) {
+  const int BS = block_size(fmt);
+  L = LayerPlan{};
+  if (!make_fc_plan(fmt, H, 2 * I, BS, L.f[0]) || !make_fc_plan(fmt, I, H, BS, L.f[1])) {
+    set_error("no column tiling of N = %d / %d fits the decode kernel", 2 * I, H);
+    return QMOE_ERR_UNSUPPORTED;
+  }
+  const size_t G = (size_t)num_sms();
+  if (G > (size_t)kMaxCtas) {
+    set_error("the decode kernel supports at most %d SMs (this GPU has %zu)", kMaxCtas, G);
+    return QMOE_ERR_UNSUPPORTED;
+  }
+  const size_t R = (size_t)T * k;
+  const size_t na_max = std::min<size_t>((size_t)E, R);
+  int slot = 0, win = 0, red = 0;
+  for (int f = 0; f < 2; ++f) {
+    const FcPlan &P = L.f[f];
+    slot = std::max(slot, 16 * P.RGS * (P.NT / 2));
+    win = std::max(win, (P.tma ? kTmaWB : P.WB) * P.NT);
+    red = std::max(red, P.RGS * kRowsMax * P.NT * 4);
+    // segments of one CTA: at most one more than the whole pairs its units
+    // span.  Its units cost at most total / G + one unit, and the total is
+    // ct * ku * sum over slots of (3 + 2 rows) <= ct * ku * 5 R.
+    const size_t total = (size_t)P.ct * P.ku * 5 * R;
+    const size_t upc = total / (G * (size_t)unit_cost(1)) + 2;
+    if ((upc + P.ku - 1) / P.ku + 1 > (size_t)kMaxSegs) {
+      set_error("too many experts per CTA for the decode kernel (N = %d, K = %d)", P.N, P.K);
+      return QMOE_ERR_UNSUPPORTED;
+    }
+  }
+  L.slot_bytes = (slot + 1023) & ~1023;
+  L.win_bytes = (win + 1023) & ~1023;
+  L.sw_off = kRing * L.slot_bytes;
+  L.st_off = L.sw_off + L.win_bytes;
+  L.xs_off = L.st_off + 2 * L.win_bytes;
+  L.xr_off = L.xs_off + kRowsMax * kXsK * 2;
+  L.red_off = L.xr_off + kXrawBytes;
+  L.smem = L.red_off + red + 1024;  // + room to align the base to 1 KB
+  // Partial rows: every (slot, tile) pair once, plus one more segment of at
+  // most T rows at each boundary between two CTAs.
+  const size_t rows_max = std::min<size_t>((size_t)T, R);
+  p1_floats = (R * L.f[0].ct + (G - 1) * rows_max) * L.f[0].NT;
+  p2_floats = (R * L.f[1].ct + (G - 1) * rows_max) * L.f[1].NT;
+  return QMOE_OK;
+}
+
+// Tensor map of one FC's block scales viewed as a 2-D byte array: E*N rows of
+// nblocks bytes; box = 16 blocks x box_rows rows, stored densely (the 16-byte
+// row of column c at byte 16 c of the window).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static cudaError_t encode_scale_map(CUtensorMap *m, const uint8_t *scales, int E, const FcPlan &P) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+      set_error("cuTensorMapEncodeTiled is not available");
+      return err != cudaSuccess ? err : cudaErrorNotSupported;
+    }
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)P.nblocks, (cuuint64_t)E * (cuuint64_t)P.N};
+  const cuuint64_t strides[1] = {(cuuint64_t)P.nblocks};
+  const cuuint32_t box[2] = {(cuuint32_t)kTmaWB, (cuuint32_t)P.box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(scales), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+template <int FMT>
+static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, cudaStream_t stream) {
+  static int smem_set = 0, smem_ok = 0;
+  auto kfn = moe_layer_kernel<FMT>;
+  if (L.smem > smem_set) {
+    cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+    if (err != cudaSuccess) return err;
+    smem_set = L.smem;
+  }
+  if (L.smem != smem_ok) {  // one CTA per SM must fit, or the cooperative launch is refused
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kLayerThreads, L.smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) {
+      cudaFuncAttributes fa{};
+      cudaFuncGetAttributes(&fa, kfn);
+      set_error("decode kernel does not fit on an SM: %d registers x %d threads, %zu + %d bytes shared memory",
+                fa.numRegs, kLayerThreads, (size_t)fa.sharedSizeBytes, L.smem);
+      return cudaErrorCooperativeLaunchTooLarge;
+    }
+    smem_ok = L.smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kLayerThreads);
+  cfg.dynamicSmemBytes = L.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kfn, a, L);
+}
+
+cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, cudaStream_t stream) {
+  if (L.f[0].tma) {
+    cudaError_t err = encode_scale_map(&a.tm_s1, a.s1, E, L.f[0]);
+    if (err != cudaSuccess) return err;
+  }
+  if (L.f[1].tma) {
+    cudaError_t err = encode_scale_map(&a.tm_s2, a.s2, E, L.f[1]);
+    if (err != cudaSuccess) return err;
+  }
+  if (a.fmt == QMOE_NVFP4) return launch_layer_fmt<QMOE_NVFP4>(a, L, stream);
+  return launch_layer_fmt<QMOE_MXFP4>(a, L, stream);
+}
+
+}  // namespace qmoe

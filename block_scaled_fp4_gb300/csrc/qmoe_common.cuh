@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/qmoe.h"
@@ -94,36 +95,46 @@ struct RouteOut {
   SlotDesc *slots;     // [min(E, T*k)] slot descriptors; may be null
   int32_t *zero_words; // words cleared by the route kernel for later kernels; may be null
   int n_zero_words;
-  // decode only: activations rescaled per token by a power of two into fp16
-  const uint16_t *x;   // bf16 [T, H] or null
-  uint16_t *x16;       // fp16 [T, H]
-  int32_t *xshift;     // [T]: x16 = x * 2^-xshift
-  int H;
 };
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize, const RouteOut &o,
                          cudaStream_t stream);
 
-struct GemvArgs {
+// Decode layer (R = T*k <= 64 rows): arguments of the fused kernel.
+struct LayerArgs {
   int fmt, T, H, I, E, k;
   float alpha, beta, limit;
+  const uint16_t *x;       // bf16 [T, H]
   const uint8_t *w1, *s1, *w2, *s2;
   const float *g1, *g2;
-  const int32_t *e2p, *meta;
+  const int32_t *e2p, *p2e;
+  int32_t *meta;           // [0] active experts, [1] device error flag, [2], [3] grid barrier counters
   const SlotDesc *slots;
-  const int32_t *p2e;
   const float *weights;
-  const uint16_t *x16;     // fp16 [T, H] (from the route kernel)
-  const int32_t *xshift;   // [T]
-  uint16_t *a;             // [R, I] bf16
-  uint32_t *rowmax;        // [R] largest |a| of each row (fp32 bits), zeroed by the route kernel
-  float *y;                // [R, H] fp32
-  int32_t *counters;       // [H / 64] arrival counters (zeroed by the route kernel)
+  float *p1, *p2;          // fp32 partial sums of FC1 / FC2 (split-K segments)
   uint16_t *out;           // [T, H] bf16
+  CUtensorMap tm_s1, tm_s2;  // block scales as 2-D byte arrays (when FcPlan::tma)
 };
-int gemv_fc2_counter_words(int H);
-cudaError_t launch_fc1_gemv(const GemvArgs &a, cudaStream_t stream);
-cudaError_t launch_fc2_gemv(const GemvArgs &a, cudaStream_t stream);
+
+// Geometry of one FC for the decode kernel (host-computed).  Unit = 16*RGS k
+// rows x NT columns; thread (w, rg) owns column word w of k-group rg.
+struct FcPlan {
+  int K, N, NT, ct, NW, RGS;
+  int nkg;      // K / 16
+  int ku;       // units per (expert, column tile)
+  int nblocks;  // K / block size
+  int WB;       // scale window, in blocks
+  int tma;      // 1: scale windows are 16-block tensor copies (nblocks % 16 == 0)
+  int box_rows; // rows of one scale tensor copy
+};
+struct LayerPlan {
+  FcPlan f[2];
+  int slot_bytes, win_bytes;
+  int sw_off, st_off, xs_off, xr_off, red_off, smem;
+};
+qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPlan &L, size_t &p1_floats,
+                            size_t &p2_floats);
+cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, cudaStream_t stream);
 
 // Programmatic dependent launch: let the next kernel in the stream start while
 // this one runs / wait here until the previous kernel's results are visible.

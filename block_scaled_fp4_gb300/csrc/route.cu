@@ -10,116 +10,9 @@
 // Ties are broken by a packed stable key: fp32 logit (order-preserving bits,
 // -0.0 folded onto +0.0) in the high word, (0xFFFF - expert) in the low word,
 // so a larger key means a larger logit, then a lower expert index.
-#include <cuda_fp16.h>
-
-#include "qmoe_common.cuh"
+#include "route_common.cuh"
 
 namespace qmoe {
-
-__device__ __forceinline__ uint64_t route_key(float v, int idx) {
-  uint32_t b = __float_as_uint(v);
-  if (b == 0x80000000u) b = 0u;
-  uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return ((uint64_t)ord << 32) | (uint32_t)(0xFFFFu - (uint32_t)idx);
-}
-__device__ __forceinline__ int key_expert(uint64_t key) { return (int)(0xFFFFu - (uint32_t)(key & 0xFFFFu)); }
-__device__ __forceinline__ float key_logit(uint64_t key) {
-  uint32_t ord = (uint32_t)(key >> 32);
-  uint32_t b = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
-  return __uint_as_float(b);
-}
-
-// Descending bitonic sort of N register-resident keys.
-template <int N>
-__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&a)[N]) {
-#pragma unroll
-  for (int size = 2; size <= N; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-      for (int i = 0; i < N; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const uint64_t x = a[i], y = a[j];
-          if (desc ? (x < y) : (x > y)) { a[i] = y; a[j] = x; }
-        }
-      }
-}
-
-// Sorts a bitonic sequence of N keys descending.
-template <int N>
-__device__ __forceinline__ void bitonic_clean_desc(uint64_t (&a)[N]) {
-#pragma unroll
-  for (int stride = N >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const int j = i ^ stride;
-      if (j > i && a[i] < a[j]) { const uint64_t t = a[i]; a[i] = a[j]; a[j] = t; }
-    }
-}
-
-// After the call every lane holds the N largest keys of the warp, descending.
-template <int N>
-__device__ __forceinline__ void warp_bitonic_topn(uint64_t (&a)[N]) {
-  bitonic_sort_desc<N>(a);
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    uint64_t b[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) b[i] = __shfl_xor_sync(0xFFFFFFFFu, a[i], m);
-#pragma unroll
-    for (int i = 0; i < N; ++i) a[i] = a[i] > b[N - 1 - i] ? a[i] : b[N - 1 - i];
-    bitonic_clean_desc<N>(a);
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, m);
-  return v;
-}
-
-// One warp routes token t: ids/weights for its k experts.
-template <int N>
-__device__ __forceinline__ void route_one_token(const float *__restrict__ logits, int t, int E, int k,
-                                                int normalize, int32_t *__restrict__ ids,
-                                                float *__restrict__ weights) {
-  const int lane = (int)lane_id();
-  const float *row = logits + (size_t)t * E;
-  float v[N];
-  uint64_t key[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const int e = lane + 32 * i;
-    const bool ok = e < E;
-    v[i] = ok ? __ldg(row + e) : 0.f;
-    key[i] = ok ? route_key(v[i], e) : 0ull;
-  }
-  warp_bitonic_topn<N>(key);
-  const float mx = key_logit(key[0]);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < N; ++i)
-    if (lane + 32 * i < E) s += expf(v[i] - mx);
-  s = warp_sum(s);
-  // selected experts, in key order
-  float sel_sum = 0.f;
-  float mine_e = 0.f;
-  int mine_id = 0;
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    if (j < k) {
-      const float ej = expf(key_logit(key[j]) - mx);
-      sel_sum += ej;
-      if (j == lane) { mine_e = ej; mine_id = key_expert(key[j]); }
-    }
-  }
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = mine_id;
-    weights[(size_t)t * k + lane] = normalize ? mine_e / sel_sum : mine_e / s;
-  }
-}
 
 template <int N>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T, int E, int k,
@@ -211,53 +104,27 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
   }
 }
 
-// Per-token power-of-two rescale of the activations into fp16 for the decode
-// GEMVs: x16 = x * 2^-s with the row's largest |x| * 2^-s in [2^14, 2^15), so
-// every finite bf16 value keeps its 8 significant bits in fp16.  One warp per token.
-__device__ void convert_token_fp16(const uint16_t *x, int H, int t, uint16_t *x16, int32_t *xshift) {
-  const int lane = (int)lane_id();
-  const uint16_t *row = x + (size_t)t * H;
-  uint32_t m = 0;
-  for (int i = lane * 8; i < H; i += 256) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, s));
-  int sh = 0;
-  if (m != 0u) sh = max(-100, min(100, (int)((m >> 7) & 0xFFu) - 127 - 14));
-  const float f = __uint_as_float((uint32_t)(127 - sh) << 23);
-  for (int i = lane * 8; i < H; i += 256) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __half2 h = __floats2half2_rn(bf16_to_f32(w[q] & 0xFFFFu) * f, bf16_to_f32(w[q] >> 16) * f);
-      o[q] = *reinterpret_cast<const uint32_t *>(&h);
-    }
-    *reinterpret_cast<uint4 *>(x16 + (size_t)t * H + i) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (lane == 0) xshift[t] = sh;
-}
-
-// Decode routing: one CTA routes T <= 64 tokens (warp per token), builds the
-// maps and the slot descriptors, and converts the activations for the GEMVs.
+// Decode routing: one CTA routes T <= 64 tokens (warp per token) and builds the
+// maps and the slot descriptors.  The next kernel may launch as soon as this
+// one starts (it waits for these results before reading them).
 template <int N>
 __global__ void __launch_bounds__(256) route_maps_fused_kernel(const float *__restrict__ logits, int T, int E,
                                                               int k, int normalize, RouteOut o) {
   extern __shared__ int32_t smem_i32[];
   pdl_launch_dependents();
   const int W = blockDim.x >> 5, w = (int)(threadIdx.x >> 5);
+  const int R = T * k;
   for (int i = threadIdx.x; i < o.n_zero_words; i += blockDim.x) o.zero_words[i] = 0;
-  for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights);
-  if (o.x) {
-    for (int t = W - 1 - w; t < T; t += W) convert_token_fp16(o.x, o.H, t, o.x16, o.xshift);
+  if (R <= 64) {
+    int32_t *ids_s = smem_i32, *cnt = smem_i32 + 64, *off = cnt + E;
+    for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights, ids_s);
+    __syncthreads();
+    if (w == 0) build_maps_small(ids_s, R, E, o, cnt, off);
+    return;
   }
+  for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights);
   __syncthreads();
-  build_maps(o.ids, T * k, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
+  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
 }
 
 // Prefill routing, second step: one CTA of 1024 threads builds the maps.
@@ -280,7 +147,9 @@ static cudaError_t launch_route_n(const float *logits, int T, int E, int k, int 
                                   cudaStream_t stream) {
   if (T <= kFusedRouteMaxTokens) {
     const int threads = 256, W = threads / 32;
-    const size_t smem = sizeof(int32_t) * ((size_t)W * E + E + 1);
+    size_t smem = sizeof(int32_t) * ((size_t)W * E + E + 1);
+    const size_t smem_small = sizeof(int32_t) * (64 + 2 * (size_t)E);
+    if (smem_small > smem) smem = smem_small;
     route_maps_fused_kernel<N><<<1, threads, smem, stream>>>(logits, T, E, k, normalize, o);
     return cudaGetLastError();
   }

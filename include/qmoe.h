@@ -134,8 +134,11 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   out          bf16 [T, H] result.
  *   topk_ids_out int32 [T, k] selected experts, or NULL.
  *   workspace, workspace_bytes: see the conventions above.
- * T * k <= QMOE_GEMV_MAX_ROWS runs the decode GEMVs (dequantisation in
- * registers); larger T * k runs the prefill path.
+ * T * k <= QMOE_GEMV_MAX_ROWS runs the decode path (routing kernel, then one
+ * persistent kernel for FC1, SwiGLU, FC2 and the un-permute, dequantising in
+ * registers); larger T * k runs the prefill path.  The decode kernel is a
+ * cooperative launch of one CTA per SM: it needs the whole GPU's residency
+ * and returns QMOE_ERR_CUDA if another context keeps it from launching.
  */
 qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits,
                                  const uint8_t *fc1_w, const uint8_t *fc1_s, const float *fc1_g,
@@ -192,7 +195,7 @@ qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *block_scales,
  *  - Nothing in the array needs to start at zero: the routing kernel clears the
  *    per-call counters the later kernels rely on at the start of every call.
  */
-#define QMOE_NO_ALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+#define QMOE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
 qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const float *logits,
                                           const uint8_t *fc1_w, const uint8_t *fc1_s,
@@ -213,8 +216,9 @@ const char *qmoe_last_error(void);
  * kernel and events[i] after its i-th kernel, for i < n_events.  The events
  * are created by the caller (cudaEventCreate) and must outlive the calls.
  * Pass NULL to switch it off.  Process-wide setting; not thread-safe.
- * Returns the number of kernels one forward call launches for (T, k) decode
- * shapes (route, FC1, FC2), i.e. how many events after the first are used.
+ * Returns the number of kernels one forward call launches for decode shapes
+ * (routing, then the fused FC1 + FC2 + un-permute kernel), i.e. how many
+ * events after the first are used.
  */
 int qmoe_set_stage_events(cudaEvent_t *events, int n_events);
 

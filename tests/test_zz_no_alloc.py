@@ -58,13 +58,27 @@ def test_no_alloc_matches_workspace_entry_point_twice(qgpu, name):
 
 def test_no_alloc_rejects_sizes_beyond_its_scratch(qgpu):
     """A shape whose scratch need exceeds the fixed array is refused with a
-    clear error before anything is launched."""
+    clear error before anything is launched.  Only the router logits are a
+    real buffer; every other pointer is deliberately misaligned, so that a
+    call that got past the size check would stop at argument validation
+    instead of launching anything."""
     lib = qgpu.load()
-    wl = syn.small("big", T=8, E=8, k=8, H=16384, I=1024)
-    P = ctypes.c_void_p(256)
-    rc = lib.qmoe_fp4_moe_forward_no_alloc(P, P, P, P, None, P, P, None, wl.fmt, wl.T, wl.H, wl.I,
-                                           wl.E, wl.k, 1, 1, ctypes.c_float(1.0),
-                                           ctypes.c_float(0.0), ctypes.c_float(math.inf), P, None,
-                                           None)
+    wl = syn.small("big", T=64, E=64, k=1, H=8192, I=4096)
+    need = qgpu.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, wl.fmt)
+    assert need > lib_scratch_bytes()
+    logits = torch.zeros((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    bad = ctypes.c_void_p(0x1001)
+    rc = lib.qmoe_fp4_moe_forward_no_alloc(bad, _ptr(logits), bad, bad, None, bad, bad, None, wl.fmt, wl.T,
+                                           wl.H, wl.I, wl.E, wl.k, 1, 1, ctypes.c_float(1.0),
+                                           ctypes.c_float(0.0), ctypes.c_float(math.inf), bad, None, None)
     assert rc == 4
     assert b"static scratch" in lib.qmoe_last_error()
+
+
+def lib_scratch_bytes():
+    """QMOE_NO_ALLOC_SCRATCH_BYTES as declared in the public header."""
+    import os
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qmoe.h")
+    m = re.search(r"#define QMOE_NO_ALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", open(hdr).read())
+    return int(m.group(1)) << int(m.group(2))
