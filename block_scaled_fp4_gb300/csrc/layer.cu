@@ -56,24 +56,26 @@ namespace qmoe {
 
 constexpr int kCons = 512;                 // consumer threads
 constexpr int kConsWarps = kCons / 32;
-constexpr int kLayerThreads = kCons + 32;  // + the weight-copy warp
+constexpr int kLayerThreads = kCons + 64;  // + the weight-copy warp + the activation/scale-copy warp
 constexpr int kWarpW = kConsWarps;
+constexpr int kWarpS = kConsWarps + 1;
 constexpr int kRing = 3;                   // weight ring slots (96 KB in flight per SM)
 constexpr int kTmaWB = 16;                 // blocks per scale window copied by the tensor unit
 constexpr int kTmaMaxNT = 1024;            // so that a window is at most 16 KB
 constexpr int kMaxWinBytes = 16 * 1024;
 constexpr int kMaxSegs = 16;               // segments of one FC in one CTA
 constexpr int kMaxCtas = 256;              // grid size (one CTA per SM)
-constexpr int kXsK = 2048;                 // activations staged per row at a time
+constexpr int kXsK = 512;                  // activations staged per row at a time (per warp)
 constexpr int kRowsMax = 2;                // rows decoded together (more rows: more passes)
 constexpr int kXrawSlot = kRowsMax * kXsK * 2;  // bytes of one raw (bf16) activation slot
-constexpr int kXrawBytes = 2 * kXrawSlot;        // two slots; FC2 reuses them as one buffer
+constexpr int kXrawBytes = 16 * 1024;            // FC1: two slots at the start; FC2: pre-staged activations
+constexpr int kXwBytes = kRowsMax * kXsK * 2;    // one warp's fp16 activation window
 constexpr int kMaxSlots = 64;
 constexpr int kMaxTiles = 16;
 constexpr int kMaxPairs = kMaxSlots * kMaxTiles;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 24;
-static_assert(kCons == kRowsMax * (kXsK / 8), "one staged 8-value vector per consumer thread");
+static_assert(2 * kXrawSlot <= kXrawBytes, "two raw activation slots");
 
 // ---- PTX helpers --------------------------------------------------------------
 
@@ -231,7 +233,7 @@ struct Shared {
   uint64_t full[kRing], empty[kRing];  // weight ring
   uint64_t wfull[2], wempty[2];        // scale-window staging
   uint64_t xfull[2], xempty[2];        // raw FC1 activation slots
-  uint64_t gsready;
+  uint64_t gsready, smallfirst, basesready;
   int4 slot[kMaxSlots];                // {e, row0, nrows, -}
   float gs[2][kMaxSlots];              // global scales per slot (1 for MXFP4)
   int base[2][kMaxPairs + 1];          // partial-sum offsets (floats) per (slot, tile) pair
@@ -432,17 +434,37 @@ __device__ void partial_bases(Shared &S, const FcPlan &P, int f) {
 
 // Every unit of the CTA, FC1 then FC2, in consumption order; before the first
 // unit of each scale window, that window's block scales (tensor copy).
-template <int FMT>
+// The two copy warps walk the same sequence of passes and units.  ROLE 0
+// copies the weight units into the ring; ROLE 1 copies the FC1 activation
+// rows and the scale windows, each blocking only on its own two slots, so
+// that these small copies are issued a whole window ahead of their use
+// instead of queueing behind the weight stream.
+template <int FMT, int ROLE>
 __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
                                       uint8_t *stage, unsigned char *xraw) {
   const int lane = (int)lane_id();
-  // global scales (needed after the first grid barrier): a few small loads,
-  // issued before the bulk copies so that they do not queue behind them
-  for (int i = lane; i < S.na; i += 32) {
-    S.gs[0][i] = g.g1 ? __ldg(g.g1 + S.slot[i].x) : 1.0f;
-    S.gs[1][i] = g.g2 ? __ldg(g.g2 + S.slot[i].x) : 1.0f;
+  // the weight stream starts once the first small copies are on their way:
+  // small copies issued behind a GPU-wide burst of bulk copies wait for it
+  if (ROLE == 0) {
+    if (lane == 0) wait_bar(S, g, &S.smallfirst, 0u);
+    __syncwarp();
   }
-  mbar_arrive(&S.gsready);
+  bool first_done = ROLE == 0;
+  // ROLE 1, once its first copies are issued: the global scales (needed after
+  // the first grid barrier) and the partial-sum offsets (needed at the end of
+  // the first pass), both off the consumers' path
+  auto after_first = [&]() {
+    if (lane == 0) mbar_arrive(&S.smallfirst);
+    for (int i = lane; i < S.na; i += 32) {
+      S.gs[0][i] = g.g1 ? __ldg(g.g1 + S.slot[i].x) : 1.0f;
+      S.gs[1][i] = g.g2 ? __ldg(g.g2 + S.slot[i].x) : 1.0f;
+    }
+    mbar_arrive(&S.gsready);
+    partial_bases(S, L.f[0], 0);
+    partial_bases(S, L.f[1], 1);
+    mbar_arrive(&S.basesready);
+    first_done = true;
+  };
   uint32_t it = 0, wn = 0, xn = 0;
   for (int f = 0; f < 2; ++f) {
     const FcPlan &P = L.f[f];
@@ -459,7 +481,7 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
         const int rows_p = min(kRowsMax, sd.z - c0);
         int cur = -1;
         for (int j = sg.j0; j < sg.j1; ++j, ++it) {
-          if (f == 0 && (j - sg.j0) % xw_units == 0) {
+          if (ROLE == 1 && f == 0 && (j - sg.j0) % xw_units == 0) {
             // FC1: the activation rows of this k window, ahead of its weights
             const int k0 = j * unit_k, len = min(P.K, min(sg.j1, j + xw_units) * unit_k) - k0;
             const int s = (int)(xn & 1u);
@@ -477,7 +499,7 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
             ++xn;
           }
           const int wid = unit_window<FMT>(P, j);
-          if (P.tma && wid != cur) {
+          if (ROLE == 1 && P.tma && wid != cur) {
             const int s = (int)(wn & 1u);
             if (wn >= 2u) {
               if (lane == 0) wait_bar(S, g, &S.wempty[s], ((wn >> 1) + 1u) & 1u);
@@ -491,6 +513,10 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
             ++wn;
             cur = wid;
           }
+          if (ROLE == 1) {
+            if (!first_done) after_first();
+            continue;
+          }
           const int s = (int)(it % kRing);
           if (it >= (uint32_t)kRing) {
             if (lane == 0) wait_bar(S, g, &S.empty[s], ((it / kRing) + 1u) & 1u);
@@ -502,16 +528,23 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
           // released it: no proxy fence is needed before the async copy writes it
           if (lane == 0) mbar_expect_tx(&S.full[s], (uint32_t)rows * row_bytes);
           __syncwarp();
+          // row group rg (16 k rows) at dst + rg * rg_stride: the padding puts
+          // the row groups read by one warp in different banks
           if (P.ct == 1) {
-            if (lane == 0) bulk_g2s(dst, wexp + (size_t)r0 * row_bytes, (uint32_t)rows * row_bytes, &S.full[s]);
+            const int nr = min(16, rows - 16 * lane);
+            if (lane < P.RGS && nr > 0)
+              bulk_g2s(dst + (size_t)lane * P.rg_stride, wexp + (size_t)(r0 + 16 * lane) * row_bytes,
+                       (uint32_t)nr * row_bytes, &S.full[s]);
           } else {
             for (int r = lane; r < rows; r += 32)
-              bulk_g2s(dst + (size_t)r * row_bytes, wexp + (size_t)(r0 + r) * (P.N / 2), row_bytes, &S.full[s]);
+              bulk_g2s(dst + (size_t)(r >> 4) * P.rg_stride + (size_t)(r & 15) * row_bytes,
+                       wexp + (size_t)(r0 + r) * (P.N / 2), row_bytes, &S.full[s]);
           }
         }
       }
     }
   }
+  if (!first_done) after_first();
 }
 
 // ---- consumers -------------------------------------------------------------------------
@@ -543,44 +576,7 @@ __device__ __forceinline__ void fma16(const uint32_t (&p)[4], const uint32_t (&q
       : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3]), "r"(x2));
 }
 
-// Two activation rows: the words of k rows k and k+1 are decoded once and
-// accumulated into both rows' 8 column sums inside one asm block (no decoded
-// value outlives it, which keeps the two-row loop within its registers).
-__device__ __forceinline__ void dfma_r2(uint32_t w0, uint32_t w1, uint32_t xa, uint32_t xb, float (&a)[8],
-                                        float (&b)[8]) {
-  asm("{ .reg .b8 b0, b1, b2, b3, c0, c1, c2, c3; .reg .b32 p0, p1, p2, p3, q0, q1, q2, q3;\n"
-      " .reg .f16 xa0, xa1, xb0, xb1, l0, h0, l1, h1, l2, h2, l3, h3;\n"
-      " mov.b32 {b0, b1, b2, b3}, %16;\n mov.b32 {c0, c1, c2, c3}, %17;\n"
-      " mov.b32 {xa0, xa1}, %18;\n mov.b32 {xb0, xb1}, %19;\n"
-      " cvt.rn.f16x2.e2m1x2 p0, b0;\n cvt.rn.f16x2.e2m1x2 p1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 p2, b2;\n cvt.rn.f16x2.e2m1x2 p3, b3;\n"
-      " mov.b32 {l0, h0}, p0;\n mov.b32 {l1, h1}, p1;\n mov.b32 {l2, h2}, p2;\n mov.b32 {l3, h3}, p3;\n"
-      " fma.rn.f32.f16 %0, l0, xa0, %0;\n fma.rn.f32.f16 %1, h0, xa0, %1;\n"
-      " fma.rn.f32.f16 %2, l1, xa0, %2;\n fma.rn.f32.f16 %3, h1, xa0, %3;\n"
-      " fma.rn.f32.f16 %4, l2, xa0, %4;\n fma.rn.f32.f16 %5, h2, xa0, %5;\n"
-      " fma.rn.f32.f16 %6, l3, xa0, %6;\n fma.rn.f32.f16 %7, h3, xa0, %7;\n"
-      " fma.rn.f32.f16 %8, l0, xb0, %8;\n fma.rn.f32.f16 %9, h0, xb0, %9;\n"
-      " fma.rn.f32.f16 %10, l1, xb0, %10;\n fma.rn.f32.f16 %11, h1, xb0, %11;\n"
-      " fma.rn.f32.f16 %12, l2, xb0, %12;\n fma.rn.f32.f16 %13, h2, xb0, %13;\n"
-      " fma.rn.f32.f16 %14, l3, xb0, %14;\n fma.rn.f32.f16 %15, h3, xb0, %15;\n"
-      " cvt.rn.f16x2.e2m1x2 q0, c0;\n cvt.rn.f16x2.e2m1x2 q1, c1;\n"
-      " cvt.rn.f16x2.e2m1x2 q2, c2;\n cvt.rn.f16x2.e2m1x2 q3, c3;\n"
-      " mov.b32 {l0, h0}, q0;\n mov.b32 {l1, h1}, q1;\n mov.b32 {l2, h2}, q2;\n mov.b32 {l3, h3}, q3;\n"
-      " fma.rn.f32.f16 %0, l0, xa1, %0;\n fma.rn.f32.f16 %1, h0, xa1, %1;\n"
-      " fma.rn.f32.f16 %2, l1, xa1, %2;\n fma.rn.f32.f16 %3, h1, xa1, %3;\n"
-      " fma.rn.f32.f16 %4, l2, xa1, %4;\n fma.rn.f32.f16 %5, h2, xa1, %5;\n"
-      " fma.rn.f32.f16 %6, l3, xa1, %6;\n fma.rn.f32.f16 %7, h3, xa1, %7;\n"
-      " fma.rn.f32.f16 %8, l0, xb1, %8;\n fma.rn.f32.f16 %9, h0, xb1, %9;\n"
-      " fma.rn.f32.f16 %10, l1, xb1, %10;\n fma.rn.f32.f16 %11, h1, xb1, %11;\n"
-      " fma.rn.f32.f16 %12, l2, xb1, %12;\n fma.rn.f32.f16 %13, h2, xb1, %13;\n"
-      " fma.rn.f32.f16 %14, l3, xb1, %14;\n fma.rn.f32.f16 %15, h3, xb1, %15; }"
-      : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3]), "+f"(a[4]), "+f"(a[5]), "+f"(a[6]), "+f"(a[7]),
-        "+f"(b[0]), "+f"(b[1]), "+f"(b[2]), "+f"(b[3]), "+f"(b[4]), "+f"(b[5]), "+f"(b[6]), "+f"(b[7])
-      : "r"(w0), "r"(w1), "r"(xa), "r"(xb));
-}
-
-// One k-group (16 rows x 8 columns) of a unit for RC activation rows: each
-// word is decoded once and used for every row.
+// The 8 block scales of a thread's column word.
 template <int FMT>
 __device__ __forceinline__ void block_scales8(uint2 sv, float (&sc)[8]) {
   bool special = false;
@@ -592,119 +588,90 @@ __device__ __forceinline__ void block_scales8(uint2 sv, float (&sc)[8]) {
   }
 }
 
+// One k-group (16 rows x 8 columns) of a unit for RC activation rows, one row
+// after the other (the words are read and decoded again for the second row:
+// measured about 5% slower than decoding once, and it keeps a single set of
+// 8 partial sums alive, which keeps the loop within its registers).
 template <int FMT, int RC>
 __device__ __forceinline__ void consume_kg(const unsigned char *rows, int row_bytes, const __half *xb, uint2 sv,
                                            float (&acc)[RC][8]) {
   static_assert(RC == 1 || RC == 2, "one or two rows per pass");
-  float bp[RC][8];
-#pragma unroll
-  for (int r = 0; r < RC; ++r)
-#pragma unroll
-    for (int c = 0; c < 8; ++c) bp[r][c] = 0.f;
-  // 8 k rows at a time; the loop is not unrolled so that the words of one
-  // half are not kept alive alongside the other's (spills would go to L2:
-  // almost all of the SM's memory is shared memory here)
-#pragma unroll 1
-  for (int g8 = 0; g8 < 16; g8 += 8) {
-    uint32_t wv[8];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) wv[kk] = *reinterpret_cast<const uint32_t *>(rows + (size_t)(g8 + kk) * row_bytes);
-    uint4 x8[RC];
-#pragma unroll
-    for (int r = 0; r < RC; ++r) x8[r] = *reinterpret_cast<const uint4 *>(xb + (size_t)r * kXsK + g8);
-#pragma unroll
-    for (int kk = 0; kk < 8; kk += 2) {
-      const uint32_t xa = kk == 0 ? x8[0].x : kk == 2 ? x8[0].y : kk == 4 ? x8[0].z : x8[0].w;
-      if (RC == 1) {
-        uint32_t p[4], q[4];
-        dec8(wv[kk], p);
-        dec8(wv[kk + 1], q);
-        fma16(p, q, xa, bp[0]);
-      } else {
-        const uint32_t xb2 = kk == 0 ? x8[RC - 1].x : kk == 2 ? x8[RC - 1].y : kk == 4 ? x8[RC - 1].z : x8[RC - 1].w;
-        dfma_r2(wv[kk], wv[kk + 1], xa, xb2, bp[0], bp[RC - 1]);
-      }
-    }
-  }
   float sc[8];
   block_scales8<FMT>(sv, sc);
 #pragma unroll
-  for (int r = 0; r < RC; ++r)
+  for (int r = 0; r < RC; ++r) {
+    float bp[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(bp[r][c], sc[c], acc[r][c]);
+    for (int c = 0; c < 8; ++c) bp[c] = 0.f;
+    // 8 k rows at a time; not unrolled, so that the words of one half are
+    // not kept alive alongside the other's (spills would go to L2: almost all
+    // of the SM's memory is shared memory here)
+#pragma unroll 1
+    for (int g8 = 0; g8 < 16; g8 += 8) {
+      uint32_t wv[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        wv[kk] = *reinterpret_cast<const uint32_t *>(rows + (size_t)(g8 + kk) * row_bytes);
+      const uint4 x8 = *reinterpret_cast<const uint4 *>(xb + (size_t)r * kXsK + g8);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk += 2) {
+        uint32_t p[4], q[4];
+        dec8(wv[kk], p);
+        dec8(wv[kk + 1], q);
+        fma16(p, q, kk == 0 ? x8.x : kk == 2 ? x8.y : kk == 4 ? x8.z : x8.w, bp);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(bp[c], sc[c], acc[r][c]);
+  }
 }
 
 struct PassCtx {
   int f, a, t, pair, c0, rows, j0, j1;
   int4 sd;
-  float *dst;  // partial rows of this segment: dst[row * NT + col], row = c0 + r
 };
 
-// Window boundary (all consumer threads): the block scales of window `wid` of
-// the pass's tile -> win[b][col].  Tensor-copied windows are read from staging
-// slot wn & 1 ([col][16] bytes) and the slot is handed back to the copy warp.
-// Out of line, arguments by value: the hot loop's state stays in registers.
-// Returns the next window count.
+// Scale windows whose runs are not 16-byte aligned (no tensor copy): all
+// consumer threads read window `wid` of the tile with byte loads into
+// win[b][col].  Out of line, arguments by value.
 template <int FMT>
-__device__ __noinline__ uint32_t enter_window(Shared &S, const LayerArgs &g, const LayerPlan &L, int f, int e, int t,
-                                              int wid, uint8_t *win, const uint8_t *stage, uint32_t wn) {
+__device__ __noinline__ void fill_window_cta(const LayerArgs &g, const LayerPlan &L, int f, int e, int t, int wid,
+                                             uint8_t *win) {
   const FcPlan &P = L.f[f];
   const int b0 = wid * P.WB, nb = min(P.WB, P.nblocks - b0);
-  if (P.tma) {
-    // Per thread, no CTA barrier: the thread's 8 columns' 16-byte runs (8
-    // loads), of which it keeps the bytes of its own blocks (u * RGS + rg for
-    // the window's 16 / RGS units), one 8-byte word (8 columns) per unit in
-    // its private slots win[u][tid].
-    const int s = (int)(wn & 1u);
-    wait_bar(S, g, &S.wfull[s], (wn >> 1) & 1u);
-    const int tid = threadIdx.x, w = tid % P.NW, rg = tid / P.NW;
-    if (rg < P.RGS) {
-      // step i: column 8w + ((i + w) % 8), so that 8 neighbouring lanes read 8
-      // different 16-byte bank groups; its bytes go to byte (column % 8) of the
-      // unit's word
-      const uint8_t *src = stage + (size_t)s * L.win_bytes + (size_t)w * 128;
-      const int upw = kTmaWB / P.RGS;  // 1, 2 or 4
-      uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+  cons_sync();  // nobody reads the previous window any more
+  const uint8_t *scol = (f == 0 ? g.s1 : g.s2) + ((size_t)e * P.N + (size_t)t * P.NT) * P.nblocks + b0;
+  const int groups = P.NT / 4, bgroups = (nb + 3) / 4;
+  for (int job = threadIdx.x; job < groups * bgroups; job += kCons) {
+    const int c4 = job / bgroups, bq = (job - c4 * bgroups) * 4;
+    uint32_t v[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = (i + w) & 7;
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + (c << 4));
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (u < upw) {
-            const int b = u * P.RGS + rg;  // block of unit u of the window
-            const uint32_t byte = (vw[b >> 2] >> (8 * (b & 3))) & 0xFFu;
-            if (c < 4) lo[u] |= byte << (8 * c); else hi[u] |= byte << (8 * (c - 4));
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (u < upw) reinterpret_cast<uint2 *>(win)[(size_t)u * kCons + threadIdx.x] = make_uint2(lo[u], hi[u]);
+    for (int i = 0; i < 4; ++i) {
+      const uint8_t *src = scol + (size_t)(4 * c4 + i) * P.nblocks + bq;
+      uint32_t x = 0;
+      for (int q = 0; q < 4 && bq + q < nb; ++q) x |= (uint32_t)__ldg(src + q) << (8 * q);
+      v[i] = x;
     }
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&S.wempty[s]);
-    ++wn;
-  } else {
-    cons_sync();
-    const uint8_t *scol = (f == 0 ? g.s1 : g.s2) + ((size_t)e * P.N + (size_t)t * P.NT) * P.nblocks + b0;
-    const int groups = P.NT / 4, bgroups = (nb + 3) / 4;
-    for (int job = threadIdx.x; job < groups * bgroups; job += kCons) {
-      const int c4 = job / bgroups, bq = (job - c4 * bgroups) * 4;
-      uint32_t v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint8_t *src = scol + (size_t)(4 * c4 + i) * P.nblocks + bq;
-        uint32_t x = 0;
-        for (int q = 0; q < 4 && bq + q < nb; ++q) x |= (uint32_t)__ldg(src + q) << (8 * q);
-        v[i] = x;
-      }
-      store_tile4x4(v[0], v[1], v[2], v[3], win + (size_t)bq * P.NT + 4 * c4, P.NT, min(4, nb - bq));
-    }
-    cons_sync();
+    store_tile4x4(v[0], v[1], v[2], v[3], win + (size_t)bq * P.NT + 4 * c4, P.NT, min(4, nb - bq));
   }
-  return wn;
+  cons_sync();
+}
+
+// A warp's share of a tensor-copied scale window: its 8 * WPW columns (stored
+// [col][16 blocks] in the staging slot) transposed into its private area
+// wp[b][col] (row stride 8 * WPW bytes), 4x4 byte tiles, two per lane.
+__device__ __forceinline__ void warp_transpose_window(const uint8_t *wstage, uint8_t *wp, int warp, int wpw) {
+  const int lane = threadIdx.x & 31;
+  const int cols = 8 * wpw, cgroups = cols / 4;  // 4-column groups of this warp
+  const uint8_t *src = wstage + (size_t)warp * cols * 16;
+  for (int t = lane; t < cgroups * 4; t += 32) {
+    const int cg = t % cgroups, bg = t / cgroups;
+    uint32_t v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint32_t *>(src + (size_t)(4 * cg + i) * 16 + 4 * bg);
+    store_tile4x4(v[0], v[1], v[2], v[3], wp + (size_t)(4 * bg) * cols + 4 * cg, cols, 4);
+  }
+  __syncwarp();
 }
 
 // a[row][k] = bf16(SwiGLU(g1 * h)) for FC2's activations, h = the FC1 partial
@@ -732,22 +699,20 @@ __device__ __forceinline__ uint16_t fc2_activation(const Shared &S, const LayerA
   return (uint16_t)f32_to_bf16_rne(swiglu(hg * g1, hl * g1, g.alpha, g.beta, g.limit));
 }
 
-// Stages activation rows [c0, c0 + rows) of the pass, k in [k0, k0 + len), as
-// fp16 in xs with a per-row power-of-two rescale; returns the shifts in sh[].
-// Raw bf16 rows come from: FC1, raw slot xn & 1 (bulk-copied by the copy
-// warp); FC2, the pre-staged buffer (row stride len) at *pre_off, or, when
-// pre-staging did not fit, they are computed here from the FC1 partials.
+// Activation rows [c0, c0 + rows) of the pass, k in [k0, k0 + len), as fp16
+// with a per-row power-of-two rescale, into this warp's own window xw
+// (row stride kXsK): every warp reads the raw bf16 rows and converts them
+// itself, so no CTA barrier is needed.  Raw rows come from: FC1, raw slot
+// xn & 1 (bulk-copied by the copy warp); FC2, the pre-staged buffer (row
+// stride len) at pre_off, or, when pre-staging did not fit, they are first
+// computed from the FC1 partials by all consumer threads into the raw buffer.
 template <int RC>
-__device__ __forceinline__ void stage_activations(Shared &S, const LayerArgs &g, const LayerPlan &L,
-                                                  const PassCtx &C, int k0, int len, __half *xs,
-                                                  const unsigned char *xraw, uint32_t &xn, int &pre_off,
-                                                  int (&sh)[RC]) {
-  const int tid = threadIdx.x, r = tid >> 8, q = tid & 255;
-  const bool valid = r < C.rows && 8 * q < len;
-  uint4 *vec = reinterpret_cast<uint4 *>(xs + (size_t)r * kXsK) + q;
-  const uint16_t *src = nullptr;
+__device__ __forceinline__ void stage_warp(Shared &S, const LayerArgs &g, const LayerPlan &L, const PassCtx &C,
+                                           int k0, int len, __half *xw, unsigned char *xraw, uint32_t &xn,
+                                           int &pre_off, int (&sh)[RC]) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t *src;
   int stride = kXsK;
-  cons_sync();  // the previous window's activations are no longer read
   if (C.f == 0) {
     const int s = (int)(xn & 1u);
     wait_bar(S, g, &S.xfull[s], (xn >> 1) & 1u);
@@ -757,35 +722,36 @@ __device__ __forceinline__ void stage_activations(Shared &S, const LayerArgs &g,
     stride = len;
     pre_off += C.rows * len;
   } else {
-    uint16_t *xb = reinterpret_cast<uint16_t *>(xs);
-    for (int i = tid; i < C.rows * len; i += kCons) {
+    cons_sync();  // every warp is done with the raw buffer
+    uint16_t *xb = reinterpret_cast<uint16_t *>(xraw);
+    for (int i = threadIdx.x; i < C.rows * len; i += kCons) {
       const int rr = i / len, kk = i - rr * len;
       xb[(size_t)rr * kXsK + kk] = fc2_activation(S, g, L, C.a, C.sd.z, C.c0 + rr, k0 + kk);
     }
     cons_sync();
     src = xb;
   }
-  const uint4 v = valid ? *reinterpret_cast<const uint4 *>(src + (size_t)r * stride + 8 * q) : make_uint4(0, 0, 0, 0);
-  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, absmax_bf16x8(v));
-  if ((tid & 31) == 0) S.wmax[tid >> 5] = m;
-  cons_sync();  // every raw value has been read
+  __syncwarp();  // this warp is done with its previous window
+#pragma unroll
+  for (int r = 0; r < RC; ++r) {
+    uint32_t m = 0;
+    if (r < C.rows)
+      for (int q = lane; q * 8 < len; q += 32)
+        m = max(m, absmax_bf16x8(*reinterpret_cast<const uint4 *>(src + (size_t)r * stride + 8 * q)));
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    sh[r] = row_shift(m);
+    const float f = pow2f(-sh[r]);
+    for (int q = lane; q * 8 < len; q += 32) {
+      const uint4 v = r < C.rows ? *reinterpret_cast<const uint4 *>(src + (size_t)r * stride + 8 * q)
+                                 : make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4 *>(xw + (size_t)r * kXsK)[q] = bf16x8_to_f16x8(v, f);
+    }
+  }
+  __syncwarp();
   if (C.f == 0) {
-    if ((tid & 31) == 0) mbar_arrive(&S.xempty[xn & 1u]);
+    if (lane == 0) mbar_arrive(&S.xempty[xn & 1u]);
     ++xn;
   }
-  uint32_t mrow[kRowsMax];
-#pragma unroll
-  for (int rr = 0; rr < kRowsMax; ++rr) {
-    uint32_t mm = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mm = max(mm, S.wmax[8 * rr + i]);
-    mrow[rr] = mm;
-  }
-#pragma unroll
-  for (int rr = 0; rr < RC; ++rr) sh[rr] = row_shift(mrow[rr]);
-  const int shr = row_shift(r == 0 ? mrow[0] : mrow[1]);
-  *vec = bf16x8_to_f16x8(v, pow2f(-shr));
-  cons_sync();
 }
 
 // FC2's activations of every pass of this CTA, computed once right after the
@@ -821,14 +787,21 @@ __device__ bool prestage_fc2(Shared &S, const LayerArgs &g, const LayerPlan &L, 
   return true;
 }
 
+// One pass (rows [c0, c0 + rows) of a segment).  Thread mapping: a warp owns
+// WPW = 32 / RGS column words (8 columns each) over all RGS row groups,
+// lane = rg * WPW + wl; the row-group partial sums are combined with warp
+// shuffles, so the pass needs no CTA barrier.
 template <int FMT, int RC>
 __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const LayerPlan &L, const PassCtx &C,
-                                         unsigned char *ring, uint8_t *win, const uint8_t *stage, __half *xs,
-                                         const unsigned char *xraw, float *red, uint32_t &it, uint32_t &wn,
-                                         uint32_t &xn, int &pre_off) {
+                                         unsigned char *ring, uint8_t *win, const uint8_t *stage, __half *xw,
+                                         unsigned char *xraw, uint32_t &it, uint32_t &wn, uint32_t &xn,
+                                         int &pre_off) {
   const FcPlan &P = L.f[C.f];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int w = tid % P.NW, rg = tid / P.NW;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wpw = 32 / P.RGS;
+  const int rg = lane / wpw, wl = lane - rg * wpw;
+  const int w = warp * wpw + wl;
+  const bool active = w < P.NW;
   const int row_bytes = P.NT / 2;
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   float acc[RC][8];
@@ -842,11 +815,12 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
   const int unit_k = 16 * P.RGS;
   const int xw_units = kXsK / unit_k;
   int cur_wid = -1;
+  uint32_t ws = 0;
   for (int xj = C.j0; xj < C.j1; xj += xw_units) {
     const int xj1 = min(C.j1, xj + xw_units);
     const int k0 = xj * unit_k, len = min(P.K, xj1 * unit_k) - k0;
     int nsh[RC];
-    stage_activations<RC>(S, g, L, C, k0, len, xs, xraw, xn, pre_off, nsh);
+    stage_warp<RC>(S, g, L, C, k0, len, xw, xraw, xn, pre_off, nsh);
     if (xj != C.j0) {
 #pragma unroll
       for (int r = 0; r < RC; ++r)
@@ -858,48 +832,62 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
     for (int j = xj; j < xj1; ++j, ++it) {
       const int wid = unit_window<FMT>(P, j);
       if (wid != cur_wid) {
-        wn = enter_window<FMT>(S, g, L, C.f, C.sd.x, C.t, wid, win, stage, wn);
+        if (P.tma) {
+          ws = wn & 1u;
+          wait_bar(S, g, &S.wfull[ws], (wn >> 1) & 1u);
+          __syncwarp();  // the warp's previous window is no longer read
+          // warps that own columns (NW is a multiple of WPW for tensor-copied
+          // windows, so these private areas fill exactly 16 * NT bytes)
+          if (warp * wpw < P.NW)
+            warp_transpose_window(stage + (size_t)ws * L.win_bytes, win + (size_t)warp * kTmaWB * 8 * wpw, warp, wpw);
+          // the staging slot can go back at once: this warp has its own copy
+          if (lane == 0) mbar_arrive(&S.wempty[ws]);
+          ++wn;
+        } else {
+          fill_window_cta<FMT>(g, L, C.f, C.sd.x, C.t, wid, win);
+        }
         cur_wid = wid;
       }
       const int s = (int)(it % kRing);
       wait_bar(S, g, &S.full[s], (it / kRing) & 1u);
       const int kg = j * P.RGS + rg;
-      if (rg < P.RGS && kg < P.nkg) {
-        const unsigned char *rows = ring + (size_t)s * L.slot_bytes + (size_t)(rg * 16) * row_bytes + 4 * w;
-        uint2 sv;
-        if (P.tma) {
-          sv = reinterpret_cast<const uint2 *>(win)[(size_t)(j % (kTmaWB / P.RGS)) * kCons + tid];
-        } else {
-          const int blk = (kg * 16) / BS - cur_wid * P.WB;
-          sv = *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
-        }
-        const __half *xb = xs + (kg * 16 - k0);
-        consume_kg<FMT, RC>(rows, row_bytes, xb, sv, acc);
+      if (active && kg < P.nkg) {
+        const unsigned char *rows = ring + (size_t)s * L.slot_bytes + (size_t)rg * P.rg_stride + 4 * w;
+        const int blk = (kg * 16) / BS - cur_wid * P.WB;
+        const uint2 sv = P.tma ? *reinterpret_cast<const uint2 *>(win + (size_t)warp * kTmaWB * 8 * wpw +
+                                                                   (size_t)blk * 8 * wpw + 8 * wl)
+                               : *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
+        consume_kg<FMT, RC>(rows, row_bytes, xw + (kg * 16 - k0), sv, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
     }
   }
-  // reduce the row groups in a fixed order and write the partial rows:
-  // red[rg][r][col], one barrier for all rows
-  const float fold = FMT == QMOE_NVFP4 ? 0x1p120f : 1.0f;
-  cons_sync();  // red is free
-  if (rg < P.RGS) {
+  // combine the row groups (a fixed butterfly over the lanes of the warp) and
+  // write the partial rows
+#pragma unroll
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      for (int m = wpw; m < 32; m <<= 1) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], m);
+  // partial rows of this segment: dst[row * NT + col], row = c0 + r (the
+  // offsets are computed by the activation copy warp after its first copies)
+  wait_bar(S, g, &S.basesready, 0u);
+  float *dst = (C.f == 0 ? g.p1 : g.p2) + S.base[C.f][C.pair] +
+               (size_t)busy_ctas(S, C.f, first_cta(S, P, C.f, C.pair), (int)blockIdx.x) * C.sd.z * P.NT;
+  if (active && rg == 0) {
+    const float fold = FMT == QMOE_NVFP4 ? 0x1p120f : 1.0f;
 #pragma unroll
     for (int r = 0; r < RC; ++r) {
-      float4 *d = reinterpret_cast<float4 *>(red + ((size_t)rg * kRowsMax + r) * P.NT + 8 * w);
-      d[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      d[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+      if (r < C.rows) {
+        // fold first: sum * 2^120 is near the rescaled row's magnitude, so
+        // undoing the 2^-shift afterwards cannot underflow
+        const float un = pow2f(sh[r]);
+        float4 *d = reinterpret_cast<float4 *>(dst + (size_t)(C.c0 + r) * P.NT + 8 * w);
+        d[0] = make_float4(acc[r][0] * fold * un, acc[r][1] * fold * un, acc[r][2] * fold * un, acc[r][3] * fold * un);
+        d[1] = make_float4(acc[r][4] * fold * un, acc[r][5] * fold * un, acc[r][6] * fold * un, acc[r][7] * fold * un);
+      }
     }
-  }
-  cons_sync();
-  for (int i = tid; i < C.rows * P.NT; i += kCons) {
-    const int r = i / P.NT, col = i - r * P.NT;
-    float sum = 0.f;
-    for (int q = 0; q < P.RGS; ++q) sum += red[((size_t)q * kRowsMax + r) * P.NT + col];
-    // fold first: sum * 2^120 is near the rescaled row's magnitude, so
-    // undoing the 2^-shift afterwards cannot underflow
-    C.dst[(size_t)(C.c0 + r) * P.NT + col] = sum * fold * pow2f(r == 0 ? sh[0] : sh[RC - 1]);
   }
 }
 
@@ -954,12 +942,11 @@ __device__ __noinline__ void finalize(Shared &S, const LayerArgs &g, const Layer
 
 template <int FMT>
 __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
-                                      uint8_t *win, const uint8_t *stage, __half *xs, unsigned char *xraw,
-                                      float *red) {
+                                      uint8_t *win, const uint8_t *stage, __half *xs, unsigned char *xraw) {
   uint32_t it = 0, wn = 0, xn = 0;
+  __half *xw = xs + (size_t)(threadIdx.x >> 5) * (kXwBytes / 2);  // this warp's activation window
   int pre_off = 0;
   for (int f = 0; f < 2; ++f) {
-    const FcPlan &P = L.f[f];
     if (f == 1) {
       grid_barrier(S, g, g.meta + 2);  // every FC1 partial is written
       wait_bar(S, g, &S.gsready, 0u);
@@ -977,15 +964,13 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const Layer
       C.sd = S.slot[sg.a];
       C.j0 = sg.j0;
       C.j1 = sg.j1;
-      C.dst = (f == 0 ? g.p1 : g.p2) + S.base[f][sg.pair] +
-              (size_t)busy_ctas(S, f, first_cta(S, P, f, sg.pair), (int)blockIdx.x) * C.sd.z * P.NT;
       for (int c0 = 0; c0 < C.sd.z; c0 += kRowsMax) {
         C.c0 = c0;
         C.rows = min(kRowsMax, C.sd.z - c0);
         if (C.rows == 1)
-          run_pass<FMT, 1>(S, g, L, C, ring, win, stage, xs, xraw, red, it, wn, xn, pre_off);
+          run_pass<FMT, 1>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
         else
-          run_pass<FMT, 2>(S, g, L, C, ring, win, stage, xs, xraw, red, it, wn, xn, pre_off);
+          run_pass<FMT, 2>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
       }
     }
   }
@@ -1013,6 +998,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
       mbar_init(&S.xempty[i], kConsWarps);
     }
     mbar_init(&S.gsready, 32);
+    mbar_init(&S.smallfirst, 1);
+    mbar_init(&S.basesready, 32);
     mbar_fence_init();
     S.abort = 0;
     S.fc2_pre = 0;
@@ -1046,7 +1033,6 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   __syncthreads();
   if (warp < 2) busy_prefix(S, warp);
   __syncthreads();
-  if (warp < 2) partial_bases(S, L.f[warp], warp);
   if (warp == 2 && (tid & 31) == 0) build_segments<FMT>(S, g, L.f[0], 0);
   if (warp == 3 && (tid & 31) == 0) build_segments<FMT>(S, g, L.f[1], 1);
   __syncthreads();
@@ -1057,11 +1043,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   uint8_t *stage = base + L.st_off;
   __half *xs = reinterpret_cast<__half *>(base + L.xs_off);
   unsigned char *xraw = base + L.xr_off;
-  float *red = reinterpret_cast<float *>(base + L.red_off);
   if (warp == kWarpW)
-    producer<FMT>(S, g, L, ring, stage, xraw);
+    producer<FMT, 0>(S, g, L, ring, stage, xraw);
+  else if (warp == kWarpS)
+    producer<FMT, 1>(S, g, L, ring, stage, xraw);
   else
-    consumer<FMT>(S, g, L, ring, win, stage, xs, xraw, red);
+    consumer<FMT>(S, g, L, ring, win, stage, xs, xraw);
 }
 
 // ---- host side ---------------------------------------------------------------------------
@@ -1108,7 +1095,12 @@ static bool make_fc_plan(int fmt, int K, int N, int BS, FcPlan &P) {
   P.WB = WB;
   P.box_rows = 256;
   while (P.NT % P.box_rows) P.box_rows /= 2;
-  if (tma && (P.box_rows < 64 || P.RGS < 4)) {  // <= 4 blocks of a window per thread
+  // row groups in a ring slot: 16 rows + a pad of 16 * max(1, WPW / 4) bytes,
+  // so that the WPW words x RGS row groups one warp reads fall in different
+  // banks (conflict-free for WPW >= 4)
+  const int wpw = 32 / P.RGS > 0 ? 32 / P.RGS : 1;
+  P.rg_stride = 16 * (P.NT / 2) + 16 * (wpw / 4 > 1 ? wpw / 4 : 1);
+  if (tma && (P.box_rows < 64 || P.RGS < 4 || P.NW % (32 / P.RGS) != 0)) {  // whole warps of columns
     return make_fc_plan(QMOE_MXFP4 + 1, K, N, BS, P);
   }
   return true;
@@ -1129,12 +1121,11 @@ qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPla
   }
   const size_t R = (size_t)T * k;
   const size_t na_max = std::min<size_t>((size_t)E, R);
-  int slot = 0, win = 0, red = 0;
+  int slot = 0, win = 0;
   for (int f = 0; f < 2; ++f) {
     const FcPlan &P = L.f[f];
-    slot = std::max(slot, 16 * P.RGS * (P.NT / 2));
+    slot = std::max(slot, P.RGS * P.rg_stride);
     win = std::max(win, (P.tma ? kTmaWB : P.WB) * P.NT);
-    red = std::max(red, P.RGS * kRowsMax * P.NT * 4);
     // segments of one CTA: at most one more than the whole pairs its units
     // span.  Its units cost at most total / G + one unit, and the total is
     // ct * ku * sum over slots of (3 + 2 rows) <= ct * ku * 5 R.
@@ -1150,9 +1141,8 @@ qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPla
   L.sw_off = kRing * L.slot_bytes;
   L.st_off = L.sw_off + L.win_bytes;
   L.xs_off = L.st_off + 2 * L.win_bytes;
-  L.xr_off = L.xs_off + kRowsMax * kXsK * 2;
-  L.red_off = L.xr_off + kXrawBytes;
-  L.smem = L.red_off + red + 1024;  // + room to align the base to 1 KB
+  L.xr_off = L.xs_off + kConsWarps * kXwBytes;
+  L.smem = L.xr_off + kXrawBytes + 1024;  // + room to align the base to 1 KB
   // Partial rows: every (slot, tile) pair once, plus one more segment of at
   // most T rows at each boundary between two CTAs.
   const size_t rows_max = std::min<size_t>((size_t)T, R);

@@ -126,11 +126,12 @@ struct FcPlan {
   int WB;       // scale window, in blocks
   int tma;      // 1: scale windows are 16-block tensor copies (nblocks % 16 == 0)
   int box_rows; // rows of one scale tensor copy
+  int rg_stride;  // bytes between row groups in a weight ring slot
 };
 struct LayerPlan {
   FcPlan f[2];
   int slot_bytes, win_bytes;
-  int sw_off, st_off, xs_off, xr_off, red_off, smem;
+  int sw_off, st_off, xs_off, xr_off, smem;
 };
 qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPlan &L, size_t &p1_floats,
                             size_t &p2_floats);
