@@ -17,6 +17,7 @@ from .build import LIB, build
 
 NVFP4 = 0
 MXFP4 = 1
+SCALES_KMAJOR = 0x100  # OR'd into fmt of the forward calls: block scales are [E, K/bs, N]
 BLOCK = {NVFP4: 16, MXFP4: 32}
 GEMV_MAX_ROWS = 64
 
@@ -25,7 +26,7 @@ STATUS = {0: "QMOE_OK", 1: "QMOE_ERR_INVALID_ARG", 2: "QMOE_ERR_MISALIGNED",
 
 # Every symbol include/qmoe.h declares.
 EXPORTS = ("qmoe_route_topk", "qmoe_fp4_moe_forward", "qmoe_fp4_dequant", "qmoe_last_error",
-           "qmoe_set_stage_events", "qmoe_fp4_moe_forward_no_alloc")
+           "qmoe_set_stage_events", "qmoe_fp4_moe_forward_no_alloc", "qmoe_fp4_scales_kmajor")
 
 
 class QMoEError(RuntimeError):
@@ -60,6 +61,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                f, f, f, P, P, P, sz, P]
             L.qmoe_fp4_dequant.restype = i
             L.qmoe_fp4_dequant.argtypes = [P, P, P, i, i, i, i, P, P]
+            L.qmoe_fp4_scales_kmajor.restype = i
+            L.qmoe_fp4_scales_kmajor.argtypes = [P, i, i, i, i, P, P]
             L.qmoe_last_error.restype = ctypes.c_char_p
             L.qmoe_last_error.argtypes = []
             L.qmoe_set_stage_events.restype = i
@@ -133,7 +136,9 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: 
                 stream=None):
     """The MoE layer.  x bf16 [T,H]; logits f32 [T,E]; w1 uint8 [E,H,I];
     s1 uint8 [E,2I,H/bs]; g1 f32 [E] or None; w2 uint8 [E,I,H/2];
-    s2 uint8 [E,H,I/bs]; g2 f32 [E] or None.  Returns out bf16 [T,H]."""
+    s2 uint8 [E,H,I/bs]; g2 f32 [E] or None.  With ``fmt | SCALES_KMAJOR``
+    s1 is [E,H/bs,2I] and s2 [E,I/bs,H] (see ``scales_kmajor``).
+    Returns out bf16 [T,H]."""
     import torch
     for t, n in ((x, "x"), (logits, "logits"), (w1, "w1"), (s1, "s1"), (g1, "g1"), (w2, "w2"),
                  (s2, "s2"), (g2, "g2"), (w1_dequant, "w1_dequant"), (w2_dequant, "w2_dequant")):
@@ -192,6 +197,21 @@ def dequant(packed, scales, gscale, fmt: int, out=None, stream=None):
     return out
 
 
+def scales_kmajor(scales, fmt: int, out=None, stream=None):
+    """Block scales uint8 [E,N,K/bs] -> k-major uint8 [E,K/bs,N] (bytes
+    unchanged), the layout the forward calls take with ``fmt | SCALES_KMAJOR``.
+    A once-per-weight-set preparation step."""
+    import torch
+    _cuda(scales, "scales")
+    E, N, nb = scales.shape
+    K = nb * BLOCK[fmt]
+    if out is None:
+        out = torch.empty((E, nb, N), dtype=torch.uint8, device=scales.device)
+    _cuda(out, "out")
+    _check(load().qmoe_fp4_scales_kmajor(_ptr(scales), E, N, K, fmt, _ptr(out), _stream(stream)))
+    return out
+
+
 def set_stage_events(events) -> int:
     """Record ``events[i]`` (torch.cuda.Event) around the forward's kernels;
     ``None`` switches it off.  Returns the number of kernels per decode call."""
@@ -209,4 +229,4 @@ _stage_keepalive = None
 
 __all__ = ["NVFP4", "MXFP4", "BLOCK", "GEMV_MAX_ROWS", "QMoEError", "build", "load", "library_path",
            "route_topk", "moe_forward", "moe_forward_no_alloc", "forward_workspace_bytes", "dequant",
-           "set_stage_events", "EXPORTS"]
+           "scales_kmajor", "SCALES_KMAJOR", "set_stage_events", "EXPORTS"]

@@ -119,6 +119,8 @@ extern "C" qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *bl
                                         uint16_t *out, cudaStream_t stream) {
   g_err[0] = 0;
   QMOE_REQUIRE(packed && block_scales && out, QMOE_ERR_INVALID_ARG, "packed, block_scales and out must be non-NULL");
+  QMOE_REQUIRE((fmt & QMOE_SCALES_KMAJOR) == 0, QMOE_ERR_UNSUPPORTED,
+               "dequant takes block scales in the [E, N, K/bs] layout (no QMOE_SCALES_KMAJOR)");
   QMOE_REQUIRE(fmt == QMOE_NVFP4 || fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
   QMOE_REQUIRE(E >= 1 && N >= 1 && K >= 1, QMOE_ERR_INVALID_ARG, "E, N, K must be >= 1 (got %d, %d, %d)", E, N, K);
   QMOE_REQUIRE(N % 64 == 0 && K % 64 == 0, QMOE_ERR_UNSUPPORTED, "N and K must be multiples of 64 (got %d, %d)", N,
@@ -128,6 +130,23 @@ extern "C" qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *bl
                QMOE_ERR_MISALIGNED, "packed, block_scales and out must be 16-byte aligned");
   return cuda_status(launch_dequant(packed, block_scales, global_scale, E, N, K, (int)fmt, out, stream),
                      "dequant launch");
+}
+
+extern "C" qmoe_status qmoe_fp4_scales_kmajor(const uint8_t *block_scales, int E, int N, int K, qmoe_fp4_format fmt,
+                                              uint8_t *out, cudaStream_t stream) {
+  g_err[0] = 0;
+  QMOE_REQUIRE(block_scales && out, QMOE_ERR_INVALID_ARG, "block_scales and out must be non-NULL");
+  QMOE_REQUIRE(fmt == QMOE_NVFP4 || fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
+  QMOE_REQUIRE(E >= 1 && N >= 1 && K >= 1, QMOE_ERR_INVALID_ARG, "E, N, K must be >= 1 (got %d, %d, %d)", E, N, K);
+  QMOE_REQUIRE(N % 64 == 0 && K % 64 == 0, QMOE_ERR_UNSUPPORTED, "N and K must be multiples of 64 (got %d, %d)", N,
+               K);
+  QMOE_REQUIRE(aligned16(block_scales) && aligned16(out), QMOE_ERR_MISALIGNED,
+               "block_scales and out must be 16-byte aligned");
+  const size_t bytes = (size_t)E * N * (K / block_size((int)fmt));
+  const uintptr_t a = (uintptr_t)block_scales, b = (uintptr_t)out;
+  QMOE_REQUIRE(a + bytes <= b || b + bytes <= a, QMOE_ERR_INVALID_ARG, "out overlaps block_scales");
+  return cuda_status(launch_scales_kmajor(block_scales, E, N, K / block_size((int)fmt), out, stream),
+                     "scales_kmajor launch");
 }
 
 namespace qmoe {
@@ -171,7 +190,9 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   qmoe_status st = check_route_args(logits, T, E, k);
   if (st != QMOE_OK) return st;
   QMOE_REQUIRE(workspace_bytes, QMOE_ERR_INVALID_ARG, "workspace_bytes is NULL");
-  QMOE_REQUIRE(fmt == QMOE_NVFP4 || fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
+  const bool kmajor = (fmt & QMOE_SCALES_KMAJOR) != 0;
+  const int base_fmt = (int)fmt & ~(int)QMOE_SCALES_KMAJOR;
+  QMOE_REQUIRE(base_fmt == QMOE_NVFP4 || base_fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
   QMOE_REQUIRE(H >= 64 && I >= 64, QMOE_ERR_INVALID_ARG, "H and I must be >= 64 (got %d, %d)", H, I);
   QMOE_REQUIRE(H % 64 == 0 && I % 64 == 0, QMOE_ERR_UNSUPPORTED, "H and I must be multiples of 64 (got %d, %d)", H,
                I);
@@ -187,7 +208,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   (void)fc2_wd;
   LayerPlan plan;
   size_t p1_floats = 0, p2_floats = 0;
-  st = make_layer_plan((int)fmt, T, H, I, E, k, plan, p1_floats, p2_floats);
+  st = make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);
   if (st != QMOE_OK) return st;
   const DecodeLayout need = decode_layout(nullptr, T, E, k, p1_floats, p2_floats);
   if (!workspace) {
@@ -218,7 +239,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   ro.n_zero_words = 3;
 
   LayerArgs g{};
-  g.fmt = (int)fmt;
+  g.fmt = base_fmt;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
   g.alpha = alpha; g.beta = beta; g.limit = limit;
   g.x = x;

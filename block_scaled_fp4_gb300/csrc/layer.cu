@@ -499,6 +499,28 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
             ++xn;
           }
           const int wid = unit_window<FMT>(P, j);
+          if (ROLE == 1 && P.kn && wid != cur) {
+            // k-major scales: the window is nb block rows of NT contiguous
+            // bytes ([b][col] in the slot, the order the consumers read)
+            const int s = (int)(wn & 1u);
+            if (wn >= 2u) {
+              if (lane == 0) wait_bar(S, g, &S.wempty[s], ((wn >> 1) + 1u) & 1u);
+              __syncwarp();
+            }
+            const int b0 = wid * P.WB, nb = min(P.WB, P.nblocks - b0);
+            uint8_t *dst = stage + (size_t)s * L.win_bytes;
+            const uint8_t *src = (f == 0 ? g.s1 : g.s2) + ((size_t)sd.x * P.nblocks + b0) * P.N + (size_t)sg.t * P.NT;
+            if (lane == 0) mbar_expect_tx(&S.wfull[s], (uint32_t)(nb * P.NT));
+            __syncwarp();
+            if (P.ct == 1) {
+              if (lane == 0) bulk_g2s(dst, src, (uint32_t)(nb * P.NT), &S.wfull[s]);
+            } else {
+              for (int b = lane; b < nb; b += 32)
+                bulk_g2s(dst + (size_t)b * P.NT, src + (size_t)b * P.N, (uint32_t)P.NT, &S.wfull[s]);
+            }
+            ++wn;
+            cur = wid;
+          }
           if (ROLE == 1 && P.tma && wid != cur) {
             const int s = (int)(wn & 1u);
             if (wn >= 2u) {
@@ -832,7 +854,17 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
     for (int j = xj; j < xj1; ++j, ++it) {
       const int wid = unit_window<FMT>(P, j);
       if (wid != cur_wid) {
-        if (P.tma) {
+        if (P.kn) {
+          // k-major: the staging slot is read in place, so it goes back
+          // only when the warp moves on to the next window
+          if (cur_wid >= 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.wempty[ws]);
+          }
+          ws = wn & 1u;
+          wait_bar(S, g, &S.wfull[ws], (wn >> 1) & 1u);
+          ++wn;
+        } else if (P.tma) {
           ws = wn & 1u;
           wait_bar(S, g, &S.wfull[ws], (wn >> 1) & 1u);
           __syncwarp();  // the warp's previous window is no longer read
@@ -854,14 +886,20 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
       if (active && kg < P.nkg) {
         const unsigned char *rows = ring + (size_t)s * L.slot_bytes + (size_t)rg * P.rg_stride + 4 * w;
         const int blk = (kg * 16) / BS - cur_wid * P.WB;
-        const uint2 sv = P.tma ? *reinterpret_cast<const uint2 *>(win + (size_t)warp * kTmaWB * 8 * wpw +
-                                                                   (size_t)blk * 8 * wpw + 8 * wl)
-                               : *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
+        const uint2 sv =
+            P.kn    ? *reinterpret_cast<const uint2 *>(stage + (size_t)ws * L.win_bytes + (size_t)blk * P.NT + 8 * w)
+            : P.tma ? *reinterpret_cast<const uint2 *>(win + (size_t)warp * kTmaWB * 8 * wpw + (size_t)blk * 8 * wpw +
+                                                       8 * wl)
+                    : *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
         consume_kg<FMT, RC>(rows, row_bytes, xw + (kg * 16 - k0), sv, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
     }
+  }
+  if (P.kn && cur_wid >= 0) {  // the pass's last window goes back
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.wempty[ws]);
   }
   // combine the row groups (a fixed butterfly over the lanes of the warp) and
   // write the partial rows
@@ -1053,11 +1091,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
 
 // ---- host side ---------------------------------------------------------------------------
 
-static bool make_fc_plan(int fmt, int K, int N, int BS, FcPlan &P) {
+static bool make_fc_plan(int fmt, bool kn, int K, int N, int BS, FcPlan &P) {
   const int nblocks = K / BS;
-  // tensor-copied scale windows: NVFP4 (one block per k-group, so a thread
-  // needs 16 / RGS <= 4 blocks of a window) with whole 16-block windows
-  bool tma = fmt == QMOE_NVFP4 && nblocks % kTmaWB == 0;
+  // tensor-copied scale windows ([E, N, nblocks] scales): NVFP4 (one block
+  // per k-group, so a thread needs 16 / RGS <= 4 blocks of a window) with
+  // whole 16-block windows.  k-major scales need no tensor copy.
+  bool tma = !kn && fmt == QMOE_NVFP4 && nblocks % kTmaWB == 0;
   int best_busy = 0;
   P = FcPlan{};
   for (int ct = 1; ct <= kMaxTiles; ++ct) {
@@ -1079,7 +1118,7 @@ static bool make_fc_plan(int fmt, int K, int N, int BS, FcPlan &P) {
   }
   if (best_busy == 0) {
     if (!tma) return false;
-    return make_fc_plan(QMOE_MXFP4 + 1, K, N, BS, P);  // no tensor-copy tiling: plain windows
+    return make_fc_plan(QMOE_MXFP4 + 1, false, K, N, BS, P);  // no tensor-copy tiling: plain windows
   }
   P.K = K;
   P.N = N;
@@ -1087,6 +1126,7 @@ static bool make_fc_plan(int fmt, int K, int N, int BS, FcPlan &P) {
   P.ku = (P.nkg + P.RGS - 1) / P.RGS;
   P.nblocks = nblocks;
   P.tma = tma ? 1 : 0;
+  P.kn = kn ? 1 : 0;
   int WB = kTmaWB;
   if (!tma)
     while (WB * P.NT > kMaxWinBytes) WB /= 2;
@@ -1101,16 +1141,16 @@ static bool make_fc_plan(int fmt, int K, int N, int BS, FcPlan &P) {
   const int wpw = 32 / P.RGS > 0 ? 32 / P.RGS : 1;
   P.rg_stride = 16 * (P.NT / 2) + 16 * (wpw / 4 > 1 ? wpw / 4 : 1);
   if (tma && (P.box_rows < 64 || P.RGS < 4 || P.NW % (32 / P.RGS) != 0)) {  // whole warps of columns
-    return make_fc_plan(QMOE_MXFP4 + 1, K, N, BS, P);
+    return make_fc_plan(QMOE_MXFP4 + 1, false, K, N, BS, P);
   }
   return true;
 }
 
-qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPlan &L, size_t &p1_floats,
-                            size_t &p2_floats) {
+qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, int k, LayerPlan &L,
+                            size_t &p1_floats, size_t &p2_floats) {
   const int BS = block_size(fmt);
   L = LayerPlan{};
-  if (!make_fc_plan(fmt, H, 2 * I, BS, L.f[0]) || !make_fc_plan(fmt, I, H, BS, L.f[1])) {
+  if (!make_fc_plan(fmt, kmajor, H, 2 * I, BS, L.f[0]) || !make_fc_plan(fmt, kmajor, I, H, BS, L.f[1])) {
     set_error("no column tiling of N = %d / %d fits the decode kernel", 2 * I, H);
     return QMOE_ERR_UNSUPPORTED;
   }
@@ -1139,7 +1179,10 @@ qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPla
   L.slot_bytes = (slot + 1023) & ~1023;
   L.win_bytes = (win + 1023) & ~1023;
   L.sw_off = kRing * L.slot_bytes;
-  L.st_off = L.sw_off + L.win_bytes;
+  // the consumers' own window area: not needed when both FCs read k-major
+  // windows in place from the staging slots
+  const bool own_win = !(L.f[0].kn && L.f[1].kn);
+  L.st_off = L.sw_off + (own_win ? L.win_bytes : 0);
   L.xs_off = L.st_off + 2 * L.win_bytes;
   L.xr_off = L.xs_off + kConsWarps * kXwBytes;
   L.smem = L.xr_off + kXrawBytes + 1024;  // + room to align the base to 1 KB

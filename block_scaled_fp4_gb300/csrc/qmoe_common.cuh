@@ -127,14 +127,15 @@ struct FcPlan {
   int tma;      // 1: scale windows are 16-block tensor copies (nblocks % 16 == 0)
   int box_rows; // rows of one scale tensor copy
   int rg_stride;  // bytes between row groups in a weight ring slot
+  int kn;       // 1: block scales are k-major [E, nblocks, N]; a window is WB rows of NT bytes
 };
 struct LayerPlan {
   FcPlan f[2];
   int slot_bytes, win_bytes;
   int sw_off, st_off, xs_off, xr_off, smem;
 };
-qmoe_status make_layer_plan(int fmt, int T, int H, int I, int E, int k, LayerPlan &L, size_t &p1_floats,
-                            size_t &p2_floats);
+qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, int k, LayerPlan &L,
+                            size_t &p1_floats, size_t &p2_floats);
 cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, cudaStream_t stream);
 
 // Programmatic dependent launch: let the next kernel in the stream start while
@@ -144,5 +145,6 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const float *g, int E, int N, int K,
                            int fmt, uint16_t *out, cudaStream_t stream);
+cudaError_t launch_scales_kmajor(const uint8_t *in, int E, int N, int nb, uint8_t *out, cudaStream_t stream);
 
 }  // namespace qmoe

@@ -25,7 +25,10 @@
  *    element (n = 2j) in its low nibble and (n = 2j + 1) in its high nibble.
  *    E2M1 code: bit 3 sign, bits 2:0 select 0, 0.5, 1, 1.5, 2, 3, 4, 6.
  *  - Block scales: uint8 [E, N, K/bs]: E4M3FN with bs = 16 (QMOE_NVFP4) or
- *    E8M0 (bias 127, 0xFF = NaN) with bs = 32 (QMOE_MXFP4).
+ *    E8M0 (bias 127, 0xFF = NaN) with bs = 32 (QMOE_MXFP4).  The forward
+ *    entry points also take the k-major layout [E, K/bs, N] (the same bytes
+ *    transposed per expert, written once by qmoe_fp4_scales_kmajor) when
+ *    QMOE_SCALES_KMAJOR is OR'd into their format argument.
  *  - Global scales: fp32 [E]; NULL means 1.0 for every expert.
  *  - Weights, scales and activations must be 16-byte aligned
  *    (QMOE_ERR_MISALIGNED otherwise).
@@ -63,7 +66,13 @@ typedef enum {
 
 typedef enum {
     QMOE_NVFP4 = 0, /* E2M1 + E4M3FN scale per 16 k + fp32 global scale per expert */
-    QMOE_MXFP4 = 1  /* E2M1 + E8M0 scale per 32 k (+ optional fp32 global scale) */
+    QMOE_MXFP4 = 1, /* E2M1 + E8M0 scale per 32 k (+ optional fp32 global scale) */
+    /* Flag, OR'd into QMOE_NVFP4 or QMOE_MXFP4 for the forward entry points:
+     * the block scales are k-major, [E, K/bs, N].  One scale window of the
+     * decode kernel (16 or fewer consecutive blocks of a column tile) is then
+     * one contiguous run of bytes per block row instead of N runs of <= 16
+     * bytes, which is what lets it stream at full bandwidth. */
+    QMOE_SCALES_KMAJOR = 0x100
 } qmoe_fp4_format;
 
 /* Largest number of expanded rows (T * k) the decode GEMV path takes; more rows
@@ -116,16 +125,21 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   x            bf16 [T, H] activations.
  *   logits       fp32 [T, E] router logits (routed as in qmoe_route_topk).
  *   fc1_w        uint8 [E, H, I]  packed e2m1, K = H, N = 2I.
- *   fc1_s        uint8 [E, 2I, H/bs] block scales.
+ *   fc1_s        uint8 [E, 2I, H/bs] block scales ([E, H/bs, 2I] with
+ *                QMOE_SCALES_KMAJOR).
  *   fc1_g        fp32 [E] global scales, or NULL.
  *   fc2_w        uint8 [E, I, H/2] packed e2m1, K = I, N = H.
- *   fc2_s        uint8 [E, H, I/bs] block scales.
+ *   fc2_s        uint8 [E, H, I/bs] block scales ([E, I/bs, H] with
+ *                QMOE_SCALES_KMAJOR).
  *   fc2_g        fp32 [E] global scales, or NULL.
  *   fc1_wd       bf16 [E, 2I, H] already-dequantised FC1 weights, or NULL;
  *   fc2_wd       bf16 [E, H, I] already-dequantised FC2 weights, or NULL.
  *                (Used only when T * k > QMOE_GEMV_MAX_ROWS; when NULL that
  *                path dequantises into the workspace.)
- *   fmt          QMOE_NVFP4 or QMOE_MXFP4.
+ *   fmt          QMOE_NVFP4 or QMOE_MXFP4, optionally | QMOE_SCALES_KMAJOR
+ *                (both FCs' block scales in the k-major layout).  The result
+ *                does not depend on the layout beyond the order of the fp32
+ *                partial sums (the two layouts may tile N differently).
  *   T, H, I, E, k  sizes: T >= 1; H, I multiples of 64; 1 <= E <= 256;
  *                1 <= k <= min(8, E).
  *   normalize    as in qmoe_route_topk.
@@ -163,13 +177,31 @@ qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits,
  *   block_scales  uint8 [E, N, K/bs].
  *   global_scale  fp32 [E], or NULL (1.0).
  *   E, N, K       E >= 1; N a multiple of 64; K a multiple of 64.
- *   fmt           QMOE_NVFP4 or QMOE_MXFP4.
+ *   fmt           QMOE_NVFP4 or QMOE_MXFP4 (block scales in the [E, N, K/bs]
+ *                 layout; QMOE_SCALES_KMAJOR is QMOE_ERR_UNSUPPORTED here).
  *   out           bf16 [E, N, K].
  * Needs no workspace.
  */
 qmoe_status qmoe_fp4_dequant(const uint8_t *packed, const uint8_t *block_scales,
                              const float *global_scale, int E, int N, int K,
                              qmoe_fp4_format fmt, uint16_t *out, cudaStream_t stream);
+
+/*
+ * qmoe_fp4_scales_kmajor -- block scales [E, N, K/bs] -> k-major [E, K/bs, N]:
+ *   out[e][b][n] = block_scales[e][n][b]   (bytes copied unchanged).
+ * A weight-load-time preparation step for the forward entry points
+ * (QMOE_SCALES_KMAJOR); the pages store scales row-major per output column
+ * (operator doc §6.5, §9b), and this is the same data transposed per expert.
+ *
+ *   block_scales  uint8 [E, N, K/bs], 16-byte aligned.
+ *   E, N, K       E >= 1; N a multiple of 64; K a multiple of 64.
+ *   fmt           QMOE_NVFP4 (bs = 16) or QMOE_MXFP4 (bs = 32).
+ *   out           uint8 [E, K/bs, N], 16-byte aligned; must not overlap the
+ *                 input.
+ * Needs no workspace.  Asynchronous on `stream`.
+ */
+qmoe_status qmoe_fp4_scales_kmajor(const uint8_t *block_scales, int E, int N, int K,
+                                   qmoe_fp4_format fmt, uint8_t *out, cudaStream_t stream);
 
 /*
  * qmoe_fp4_moe_forward_no_alloc -- the same layer as qmoe_fp4_moe_forward for

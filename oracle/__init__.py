@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_dequant_element.argtypes = [P, P, P, i, i, i, i, i, i]
             L.oracle_dequant.restype = i
             L.oracle_dequant.argtypes = [P, P, P, i, i, i, i, P]
+            L.oracle_scales_kmajor.restype = i
+            L.oracle_scales_kmajor.argtypes = [P, i, i, i, P]
             L.oracle_route.restype = i
             L.oracle_route.argtypes = [P, i, i, i, i, P, P, P, P, P]
             L.oracle_expert_fc1.restype = i
@@ -137,6 +139,15 @@ def dequant(packed, scales, gscale, fmt) -> np.ndarray:
     out = np.empty((E, N, K), dtype=np.uint16)
     _check(lib().oracle_dequant(_ptr(packed), _ptr(scales), _ptr(gscale), E, N, K, fmt,
                                 _ptr(out)), "dequant")
+    return out
+
+
+def scales_kmajor(scales) -> np.ndarray:
+    """Block scales uint8 [E,N,nb] -> uint8 [E,nb,N], out[e,b,n] = in[e,n,b]."""
+    scales = _c(scales, np.uint8)
+    E, N, nb = scales.shape
+    out = np.empty((E, nb, N), dtype=np.uint8)
+    _check(lib().oracle_scales_kmajor(_ptr(scales), E, N, nb, _ptr(out)), "scales_kmajor")
     return out
 
 

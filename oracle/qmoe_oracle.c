@@ -155,6 +155,19 @@ int oracle_dequant(const uint8_t *packed, const uint8_t *scales, const float *gs
     return ORACLE_OK;
 }
 
+/* Block scales [E][N][nb] -> the k-major layout [E][nb][N] the forward path
+ * also accepts: out[e][b][n] = in[e][n][b], every byte copied unchanged.  (A
+ * storage order of this library, not of the pages; the pages index scales as
+ * [e][n][k / block], PR #31349.) */
+int oracle_scales_kmajor(const uint8_t *in, int E, int N, int nb, uint8_t *out) {
+    if (!in || !out || E < 1 || N < 1 || nb < 1) return 1;
+    for (int e = 0; e < E; ++e)
+        for (int b = 0; b < nb; ++b)
+            for (int n = 0; n < N; ++n)
+                out[((size_t)e * nb + b) * N + n] = in[((size_t)e * N + n) * nb + b];
+    return 0;
+}
+
 /* ---- routing ------------------------------------------------------------- */
 
 typedef struct { float logit; int idx; } key_t_;

@@ -138,3 +138,28 @@ def test_nan_scale_gives_nan(oracle):
     out = oracle.dequant(np.full((1, 32, 1), 0x21, np.uint8),
                          np.array([[[0xFF], [127]]], np.uint8), None, MX)
     assert np.all(out[0, 0] == 0x7FC0) and np.all(_f(out[0, 1]) == 1.0)
+
+
+def test_scales_kmajor_hand_example(oracle):
+    # two experts, three columns, two blocks, written out by hand:
+    # column n of expert e holds blocks (b0, b1); k-major puts block rows first
+    s = np.array([[[1, 2], [3, 4], [5, 6]],
+                  [[7, 8], [9, 10], [11, 12]]], np.uint8)
+    want = np.array([[[1, 3, 5], [2, 4, 6]],
+                     [[7, 9, 11], [8, 10, 12]]], np.uint8)
+    assert np.array_equal(oracle.scales_kmajor(s), want)
+
+
+def test_scales_kmajor_keeps_dequant(oracle):
+    # dequantising through the k-major copy (read back at [e, k // bs, n])
+    # gives the same bf16 weights as the page layout
+    rng = np.random.default_rng(5)
+    E, K, N = 2, 64, 64
+    packed = rng.integers(0, 256, (E, K, N // 2), dtype=np.uint8)
+    scales = syn.block_scales(rng, NV, (E, N, K // 16))
+    km = oracle.scales_kmajor(scales)
+    back = np.ascontiguousarray(km.transpose(0, 2, 1))
+    assert np.array_equal(oracle.dequant(packed, back, None, NV), oracle.dequant(packed, scales, None, NV))
+    # and every scale byte appears once at its transposed place
+    assert km.shape == (E, K // 16, N)
+    assert np.array_equal(np.sort(km.ravel()), np.sort(scales.ravel()))
