@@ -199,7 +199,16 @@ def run_gpu(args):
     global LAYERS
     LAYERS = args.layers
     wl, layers = make_layers(LAYERS, seed=1234 + rank, device=device)
-    ws_bytes = q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, wl.fmt)
+    fmt = wl.fmt
+    if args.scales == "kmajor":
+        # weight-load-time preparation, outside every timed region: the block
+        # scales of both FCs in the k-major layout
+        for L in layers:
+            L["s1"] = q.scales_kmajor(L["s1"], wl.fmt)
+            L["s2"] = q.scales_kmajor(L["s2"], wl.fmt)
+        fmt = wl.fmt | q.SCALES_KMAJOR
+        torch.cuda.synchronize()
+    ws_bytes = q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, fmt)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
     ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=device) for _ in layers]
@@ -208,7 +217,7 @@ def run_gpu(args):
     def step(lst=layers):
         for i, L in enumerate(lst):
             q.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
-                          wl.fmt, wl.k, wl.normalize, out=outs[i], topk_ids=ids[i], workspace=ws)
+                          fmt, wl.k, wl.normalize, out=outs[i], topk_ids=ids[i], workspace=ws)
 
     # --- graph capture of one step (40 layers)
     with torch.cuda.stream(stream):
@@ -269,7 +278,7 @@ def run_gpu(args):
                 e.record(stream)  # create the event objects
             q.set_stage_events(evs[j])
             q.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
-                          wl.fmt, wl.k, wl.normalize, out=outs[j % LAYERS], workspace=ws)
+                          fmt, wl.k, wl.normalize, out=outs[j % LAYERS], workspace=ws)
         q.set_stage_events(None)
     torch.cuda.synchronize()
     names = ["route", "layer"]
@@ -297,7 +306,7 @@ def run_gpu(args):
         for i, L in enumerate(layers):
             dx[i].copy_(hx[i], non_blocking=True)
             dl[i].copy_(hl[i], non_blocking=True)
-            q.moe_forward(dx[i], dl[i], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], wl.fmt,
+            q.moe_forward(dx[i], dl[i], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], fmt,
                           wl.k, wl.normalize, out=outs[i], workspace=ws)
             ho[i].copy_(outs[i], non_blocking=True)
 
@@ -328,7 +337,9 @@ def run_gpu(args):
             "config": {"workload": f"{WORKLOAD}: T=4 E=256 k=8 H=2048 I=512 NVFP4 SwiGLU",
                        "layers_per_step": LAYERS, "global_batch_tokens": wl.T * world,
                        "l2": "inputs larger than L2: 40 distinct layers, 17.3 GB of weights per step",
-                       "graph": True, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "graph": True, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "scale_layout": ("k-major [E, K/16, N], converted once at weight load"
+                                        if args.scales == "kmajor" else "[E, N, K/16] as stored")},
             "weight_stream": {"alg_bytes_per_layer": int(mean_alg),
                               "mean_active_experts": statistics.mean(act),
                               "gbs": round(stream_gbs, 1), "frac_of_hbm": round(stream_gbs / (peak * world), 4),
@@ -421,6 +432,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="distinct layers per step (default 40; fewer only for small profiler runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],
+                    help="block-scale layout the layer reads (default: k-major, prepared once at load)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
