@@ -59,14 +59,15 @@ constexpr int kConsWarps = kCons / 32;
 constexpr int kLayerThreads = kCons + 64;  // + the weight-copy warp + the activation/scale-copy warp
 constexpr int kWarpW = kConsWarps;
 constexpr int kWarpS = kConsWarps + 1;
-constexpr int kRing = 3;                   // weight ring slots (96 KB in flight per SM)
+constexpr int kRingMax = 4;                // weight ring slots (LayerPlan::ring: 4 when shared memory allows, else 3)
 constexpr int kTmaWB = 16;                 // blocks per scale window copied by the tensor unit
 constexpr int kTmaMaxNT = 1024;            // so that a window is at most 16 KB
 constexpr int kMaxWinBytes = 16 * 1024;
+constexpr int kSmemOptin = 232448;         // shared memory per block (opt-in) on sm_100 / sm_103
 constexpr int kMaxSegs = 16;               // segments of one FC in one CTA
 constexpr int kMaxCtas = 256;              // grid size (one CTA per SM)
 constexpr int kXsK = 512;                  // activations staged per row at a time (per warp)
-constexpr int kRowsMax = 2;                // rows decoded together (more rows: more passes)
+constexpr int kRowsMax = 1;                // rows per pass: a row of an expert is one pass over its units
 constexpr int kXrawSlot = kRowsMax * kXsK * 2;  // bytes of one raw (bf16) activation slot
 constexpr int kXrawBytes = 16 * 1024;            // FC1: two slots at the start; FC2: pre-staged activations
 constexpr int kXwBytes = kRowsMax * kXsK * 2;    // one warp's fp16 activation window
@@ -113,6 +114,16 @@ __device__ __forceinline__ void tensor_g2s_2d(void *dst, const CUtensorMap *map,
           smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+// 16-byte copy global -> shared through the load/store path (not the bulk
+// copy engine, so it does not queue behind the weight stream).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued before has landed
+// (the arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 // Consumer threads only (the copy and scale warps never take part).
 __device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
@@ -198,11 +209,11 @@ __device__ __forceinline__ void store_tile4x4(uint32_t v0, uint32_t v1, uint32_t
 // ---- work geometry ------------------------------------------------------------------
 
 // Work split: the units of FC f, in (expert slot, column tile, k) order, are
-// cut into gridDim.x ranges of about equal cost, cost(unit) = 3 + 2 * rows for
-// an expert with `rows` rows (decoding a unit for two rows takes about 1.4x
-// one row; more rows are decoded two at a time); CTA c gets units
-// [bnd[f][c], bnd[f][c + 1]).
-__host__ __device__ __forceinline__ int unit_cost(int rows) { return 3 + 2 * rows; }
+// cut into gridDim.x ranges of about equal cost, cost(unit) = 1 + 4 * rows for
+// an expert with `rows` rows (each row is one pass over the unit, decoded on
+// its own; the constant stands for the unit's copy and bookkeeping); CTA c
+// gets units [bnd[f][c], bnd[f][c + 1]).
+__host__ __device__ __forceinline__ int unit_cost(int rows) { return 1 + 4 * rows; }
 
 struct FcWork {
   int lo, hi;
@@ -230,7 +241,7 @@ struct Seg {
 };
 
 struct Shared {
-  uint64_t full[kRing], empty[kRing];  // weight ring
+  uint64_t full[kRingMax], empty[kRingMax];  // weight ring
   uint64_t wfull[2], wempty[2];        // scale-window staging
   uint64_t xfull[2], xempty[2];        // raw FC1 activation slots
   uint64_t gsready, smallfirst, basesready;
@@ -442,6 +453,7 @@ __device__ void partial_bases(Shared &S, const FcPlan &P, int f) {
 template <int FMT, int ROLE>
 __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
                                       uint8_t *stage, unsigned char *xraw) {
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   const int lane = (int)lane_id();
   // the weight stream starts once the first small copies are on their way:
   // small copies issued behind a GPU-wide burst of bulk copies wait for it
@@ -489,38 +501,18 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
               if (lane == 0) wait_bar(S, g, &S.xempty[s], ((xn >> 1) + 1u) & 1u);
               __syncwarp();
             }
-            if (lane == 0) mbar_expect_tx(&S.xfull[s], (uint32_t)(rows_p * len * 2));
-            __syncwarp();
-            if (lane < rows_p) {
-              const int tok = S.row_tok[sd.y + c0 + lane];
-              bulk_g2s(xraw + (size_t)s * kXrawSlot + (size_t)lane * kXsK * 2, g.x + (size_t)tok * g.H + k0,
-                       (uint32_t)(len * 2), &S.xfull[s]);
+            // 16-byte pieces, all 32 lanes; each lane arrives once its own have landed
+            const int cpr = len / 8;  // pieces per row
+            for (int i = lane; i < rows_p * cpr; i += 32) {
+              const int r = i / cpr, c = i - r * cpr;
+              const int tok = S.row_tok[sd.y + c0 + r];
+              cp_async16(xraw + (size_t)s * kXrawSlot + (size_t)r * kXsK * 2 + (size_t)c * 16,
+                         g.x + (size_t)tok * g.H + k0 + (size_t)c * 8);
             }
+            cp_async_arrive(&S.xfull[s]);
             ++xn;
           }
           const int wid = unit_window<FMT>(P, j);
-          if (ROLE == 1 && P.kn && wid != cur) {
-            // k-major scales: the window is nb block rows of NT contiguous
-            // bytes ([b][col] in the slot, the order the consumers read)
-            const int s = (int)(wn & 1u);
-            if (wn >= 2u) {
-              if (lane == 0) wait_bar(S, g, &S.wempty[s], ((wn >> 1) + 1u) & 1u);
-              __syncwarp();
-            }
-            const int b0 = wid * P.WB, nb = min(P.WB, P.nblocks - b0);
-            uint8_t *dst = stage + (size_t)s * L.win_bytes;
-            const uint8_t *src = (f == 0 ? g.s1 : g.s2) + ((size_t)sd.x * P.nblocks + b0) * P.N + (size_t)sg.t * P.NT;
-            if (lane == 0) mbar_expect_tx(&S.wfull[s], (uint32_t)(nb * P.NT));
-            __syncwarp();
-            if (P.ct == 1) {
-              if (lane == 0) bulk_g2s(dst, src, (uint32_t)(nb * P.NT), &S.wfull[s]);
-            } else {
-              for (int b = lane; b < nb; b += 32)
-                bulk_g2s(dst + (size_t)b * P.NT, src + (size_t)b * P.N, (uint32_t)P.NT, &S.wfull[s]);
-            }
-            ++wn;
-            cur = wid;
-          }
           if (ROLE == 1 && P.tma && wid != cur) {
             const int s = (int)(wn & 1u);
             if (wn >= 2u) {
@@ -528,7 +520,9 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
               __syncwarp();
             }
             uint8_t *dst = stage + (size_t)s * L.win_bytes;
+            // the barrier counts 32 arrivals (one per lane, as for the cp.async windows)
             if (lane == 0) mbar_expect_tx(&S.wfull[s], (uint32_t)(P.NT * kTmaWB));
+            else mbar_arrive(&S.wfull[s]);
             __syncwarp();
             for (int r = lane * P.box_rows; r < P.NT; r += 32 * P.box_rows)
               tensor_g2s_2d(dst + (size_t)r * kTmaWB, map, wid * kTmaWB, col0 + r, &S.wfull[s]);
@@ -539,17 +533,31 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
             if (!first_done) after_first();
             continue;
           }
-          const int s = (int)(it % kRing);
-          if (it >= (uint32_t)kRing) {
-            if (lane == 0) wait_bar(S, g, &S.empty[s], ((it / kRing) + 1u) & 1u);
+          const uint32_t ring_n = (uint32_t)L.ring;
+          const int s = (int)(it % ring_n);
+          if (it >= ring_n) {
+            if (lane == 0) wait_bar(S, g, &S.empty[s], ((it / ring_n) + 1u) & 1u);
             __syncwarp();
           }
           unsigned char *dst = ring + (size_t)s * L.slot_bytes;
           const int r0 = j * 16 * P.RGS, rows = unit_rows(P, j);
           // the slot was only read by the consumers (generic loads) before they
-          // released it: no proxy fence is needed before the async copy writes it
-          if (lane == 0) mbar_expect_tx(&S.full[s], (uint32_t)rows * row_bytes);
+          // released it: no proxy fence is needed before the async copy writes it.
+          // k-major scales: the unit's block rows travel in the same slot, at
+          // bytes [sc_off, sc_off + nbu * NT), counted on the same barrier
+          const int b0 = (r0 / BS), nbu = P.kn ? min(P.bpu, P.nblocks - b0) : 0;
+          if (lane == 0) mbar_expect_tx(&S.full[s], (uint32_t)rows * row_bytes + (uint32_t)(nbu * P.NT));
           __syncwarp();
+          if (P.kn) {
+            const uint8_t *ssrc =
+                (f == 0 ? g.s1 : g.s2) + ((size_t)sd.x * P.nblocks + b0) * P.N + (size_t)sg.t * P.NT;
+            if (P.ct == 1) {
+              if (lane == 31) bulk_g2s(dst + P.sc_off, ssrc, (uint32_t)(nbu * P.NT), &S.full[s]);
+            } else {
+              for (int b = lane; b < nbu; b += 32)
+                bulk_g2s(dst + P.sc_off + (size_t)b * P.NT, ssrc + (size_t)b * P.N, (uint32_t)P.NT, &S.full[s]);
+            }
+          }
           // row group rg (16 k rows) at dst + rg * rg_stride: the padding puts
           // the row groups read by one warp in different banks
           if (P.ct == 1) {
@@ -853,18 +861,8 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
     for (int r = 0; r < RC; ++r) sh[r] = nsh[r];
     for (int j = xj; j < xj1; ++j, ++it) {
       const int wid = unit_window<FMT>(P, j);
-      if (wid != cur_wid) {
-        if (P.kn) {
-          // k-major: the staging slot is read in place, so it goes back
-          // only when the warp moves on to the next window
-          if (cur_wid >= 0) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.wempty[ws]);
-          }
-          ws = wn & 1u;
-          wait_bar(S, g, &S.wfull[ws], (wn >> 1) & 1u);
-          ++wn;
-        } else if (P.tma) {
+      if (!P.kn && wid != cur_wid) {  // k-major scales come with the unit
+        if (P.tma) {
           ws = wn & 1u;
           wait_bar(S, g, &S.wfull[ws], (wn >> 1) & 1u);
           __syncwarp();  // the warp's previous window is no longer read
@@ -880,14 +878,15 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
         }
         cur_wid = wid;
       }
-      const int s = (int)(it % kRing);
-      wait_bar(S, g, &S.full[s], (it / kRing) & 1u);
+      const int s = (int)(it % (uint32_t)L.ring);
+      wait_bar(S, g, &S.full[s], (it / (uint32_t)L.ring) & 1u);
       const int kg = j * P.RGS + rg;
       if (active && kg < P.nkg) {
         const unsigned char *rows = ring + (size_t)s * L.slot_bytes + (size_t)rg * P.rg_stride + 4 * w;
         const int blk = (kg * 16) / BS - cur_wid * P.WB;
         const uint2 sv =
-            P.kn    ? *reinterpret_cast<const uint2 *>(stage + (size_t)ws * L.win_bytes + (size_t)blk * P.NT + 8 * w)
+            P.kn    ? *reinterpret_cast<const uint2 *>(ring + (size_t)s * L.slot_bytes + P.sc_off +
+                                                       (size_t)((kg * 16) / BS - (j * 16 * P.RGS) / BS) * P.NT + 8 * w)
             : P.tma ? *reinterpret_cast<const uint2 *>(win + (size_t)warp * kTmaWB * 8 * wpw + (size_t)blk * 8 * wpw +
                                                        8 * wl)
                     : *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
@@ -896,10 +895,6 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
     }
-  }
-  if (P.kn && cur_wid >= 0) {  // the pass's last window goes back
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.wempty[ws]);
   }
   // combine the row groups (a fixed butterfly over the lanes of the warp) and
   // write the partial rows
@@ -1005,10 +1000,7 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const Layer
       for (int c0 = 0; c0 < C.sd.z; c0 += kRowsMax) {
         C.c0 = c0;
         C.rows = min(kRowsMax, C.sd.z - c0);
-        if (C.rows == 1)
-          run_pass<FMT, 1>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
-        else
-          run_pass<FMT, 2>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
+        run_pass<FMT, kRowsMax>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
       }
     }
   }
@@ -1023,16 +1015,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   __shared__ Shared S;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kRingMax; ++i) {
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], kConsWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.wfull[i], 1);
+      mbar_init(&S.wfull[i], 32);  // one arrival per lane of the activation/scale-copy warp
       mbar_init(&S.wempty[i], kConsWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.xfull[i], 1);
+      mbar_init(&S.xfull[i], 32);
       mbar_init(&S.xempty[i], kConsWarps);
     }
     mbar_init(&S.gsready, 32);
@@ -1127,6 +1119,7 @@ static bool make_fc_plan(int fmt, bool kn, int K, int N, int BS, FcPlan &P) {
   P.nblocks = nblocks;
   P.tma = tma ? 1 : 0;
   P.kn = kn ? 1 : 0;
+  P.bpu = (P.RGS * 16) / BS > 0 ? (P.RGS * 16) / BS : 1;  // block rows a unit touches (k-major scales)
   int WB = kTmaWB;
   if (!tma)
     while (WB * P.NT > kMaxWinBytes) WB /= 2;
@@ -1140,6 +1133,7 @@ static bool make_fc_plan(int fmt, bool kn, int K, int N, int BS, FcPlan &P) {
   // banks (conflict-free for WPW >= 4)
   const int wpw = 32 / P.RGS > 0 ? 32 / P.RGS : 1;
   P.rg_stride = 16 * (P.NT / 2) + 16 * (wpw / 4 > 1 ? wpw / 4 : 1);
+  P.sc_off = P.RGS * P.rg_stride;  // k-major scales after the unit's row groups (16-byte aligned)
   if (tma && (P.box_rows < 64 || P.RGS < 4 || P.NW % (32 / P.RGS) != 0)) {  // whole warps of columns
     return make_fc_plan(QMOE_MXFP4 + 1, false, K, N, BS, P);
   }
@@ -1164,11 +1158,11 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
   int slot = 0, win = 0;
   for (int f = 0; f < 2; ++f) {
     const FcPlan &P = L.f[f];
-    slot = std::max(slot, P.RGS * P.rg_stride);
+    slot = std::max(slot, P.RGS * P.rg_stride + (P.kn ? P.bpu * P.NT : 0));
     win = std::max(win, (P.tma ? kTmaWB : P.WB) * P.NT);
     // segments of one CTA: at most one more than the whole pairs its units
     // span.  Its units cost at most total / G + one unit, and the total is
-    // ct * ku * sum over slots of (3 + 2 rows) <= ct * ku * 5 R.
+    // ct * ku * sum over slots of (1 + 4 rows) <= ct * ku * 5 R.
     const size_t total = (size_t)P.ct * P.ku * 5 * R;
     const size_t upc = total / (G * (size_t)unit_cost(1)) + 2;
     if ((upc + P.ku - 1) / P.ku + 1 > (size_t)kMaxSegs) {
@@ -1178,14 +1172,26 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
   }
   L.slot_bytes = (slot + 1023) & ~1023;
   L.win_bytes = (win + 1023) & ~1023;
-  L.sw_off = kRing * L.slot_bytes;
   // the consumers' own window area: not needed when both FCs read k-major
   // windows in place from the staging slots
-  const bool own_win = !(L.f[0].kn && L.f[1].kn);
-  L.st_off = L.sw_off + (own_win ? L.win_bytes : 0);
-  L.xs_off = L.st_off + 2 * L.win_bytes;
-  L.xr_off = L.xs_off + kConsWarps * kXwBytes;
-  L.smem = L.xr_off + kXrawBytes + 1024;  // + room to align the base to 1 KB
+  const bool kn = L.f[0].kn && L.f[1].kn;  // no window buffers: scales ride in the ring
+  if (kn) L.win_bytes = 0;
+  const bool own_win = !kn;
+  // the deepest weight ring that fits next to everything else (a deeper ring
+  // keeps more bytes in flight per SM)
+  const int limit = kSmemOptin - (int)sizeof(Shared) - 1024;
+  for (L.ring = kRingMax; L.ring >= 3; --L.ring) {
+    L.sw_off = L.ring * L.slot_bytes;
+    L.st_off = L.sw_off + (own_win ? L.win_bytes : 0);
+    L.xs_off = L.st_off + 2 * L.win_bytes;
+    L.xr_off = L.xs_off + kConsWarps * kXwBytes;
+    L.smem = L.xr_off + kXrawBytes + 1024;  // + room to align the base to 1 KB
+    if (L.smem <= limit) break;
+  }
+  if (L.ring < 3) {
+    set_error("the decode kernel's buffers do not fit in shared memory (N = %d / %d)", 2 * I, H);
+    return QMOE_ERR_UNSUPPORTED;
+  }
   // Partial rows: every (slot, tile) pair once, plus one more segment of at
   // most T rows at each boundary between two CTAs.
   const size_t rows_max = std::min<size_t>((size_t)T, R);

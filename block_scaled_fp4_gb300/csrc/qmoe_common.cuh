@@ -127,10 +127,13 @@ struct FcPlan {
   int tma;      // 1: scale windows are 16-block tensor copies (nblocks % 16 == 0)
   int box_rows; // rows of one scale tensor copy
   int rg_stride;  // bytes between row groups in a weight ring slot
-  int kn;       // 1: block scales are k-major [E, nblocks, N]; a window is WB rows of NT bytes
+  int kn;       // 1: block scales are k-major [E, nblocks, N]; a unit's scale rows ride in its ring slot
+  int bpu;      // scale block rows one unit touches (k-major)
+  int sc_off;   // offset of those rows in a ring slot
 };
 struct LayerPlan {
   FcPlan f[2];
+  int ring;  // weight ring slots (3 or 4)
   int slot_bytes, win_bytes;
   int sw_off, st_off, xs_off, xr_off, smem;
 };
