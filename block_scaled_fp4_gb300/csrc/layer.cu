@@ -64,7 +64,7 @@ constexpr int kTmaWB = 16;                 // blocks per scale window copied by 
 constexpr int kTmaMaxNT = 1024;            // so that a window is at most 16 KB
 constexpr int kMaxWinBytes = 16 * 1024;
 constexpr int kSmemOptin = 232448;         // shared memory per block (opt-in) on sm_100 / sm_103
-constexpr int kMaxSegs = 16;               // segments of one FC in one CTA
+constexpr int kMaxSegs = 32;               // segments of one FC in one CTA
 constexpr int kMaxCtas = 256;              // grid size (one CTA per SM)
 constexpr int kXsK = 512;                  // activations staged per row at a time (per warp)
 constexpr int kRowsMax = 1;                // rows per pass: a row of an expert is one pass over its units
@@ -214,6 +214,13 @@ __device__ __forceinline__ void store_tile4x4(uint32_t v0, uint32_t v1, uint32_t
 // its own; the constant stands for the unit's copy and bookkeeping); CTA c
 // gets units [bnd[f][c], bnd[f][c + 1]).
 __host__ __device__ __forceinline__ int unit_cost(int rows) { return 1 + 4 * rows; }
+// A pass start (one per row of each (expert slot, tile) pair: partial-sum
+// write of the previous pass, activation staging, first copy) costs about two
+// units; it is charged at the pair's start.
+constexpr int kPassCost = 8;
+__host__ __device__ __forceinline__ int pair_cost(const FcPlan &P, int rows) {
+  return rows * kPassCost + P.ku * unit_cost(rows);
+}
 
 struct FcWork {
   int lo, hi;
@@ -237,7 +244,8 @@ __device__ __forceinline__ int unit_rows(const FcPlan &P, int j) { return min(16
 
 // A CTA's consecutive units of one (expert slot, column tile) pair.
 struct Seg {
-  int pair, a, t, j0, j1, wid0, wid1, pad;
+  int pair, a, t, j0, j1, wid0, wid1;
+  int dst;  // offset (floats) of this CTA's partial rows of the pair (set with the partial-sum bases)
 };
 
 struct Shared {
@@ -332,7 +340,7 @@ __device__ void build_segments(Shared &S, const LayerArgs &g, const FcPlan &P, i
     sg.j1 = end - pair * P.ku;
     sg.wid0 = unit_window<FMT>(P, sg.j0);
     sg.wid1 = unit_window<FMT>(P, sg.j1 - 1);
-    sg.pad = 0;
+    sg.dst = 0;
     S.seg[f][n++] = sg;
     u = end;
   }
@@ -347,7 +355,7 @@ __device__ void cost_prefix(Shared &S, const FcPlan &P, int f) {
   int sum = 0;
   for (int q = 0; q < per; ++q) {
     const int a = lane * per + q;
-    if (a < S.na) sum += P.ct * P.ku * unit_cost(S.slot[a].z);
+    if (a < S.na) sum += P.ct * pair_cost(P, S.slot[a].z);
   }
   int incl = sum;
 #pragma unroll
@@ -360,7 +368,7 @@ __device__ void cost_prefix(Shared &S, const FcPlan &P, int f) {
     const int a = lane * per + q;
     if (a < S.na) {
       S.scum[f][a] = run;
-      run += P.ct * P.ku * unit_cost(S.slot[a].z);
+      run += P.ct * pair_cost(P, S.slot[a].z);
     }
   }
   if (lane == 31) S.scum[f][S.na] = run;
@@ -405,9 +413,18 @@ __device__ void split_bound(Shared &S, const FcPlan &P, int f, int c) {
     const int mid = (lo + hi + 1) >> 1;
     if (S.scum[f][mid] <= x) lo = mid; else hi = mid - 1;
   }
-  const int cu = unit_cost(S.slot[lo].z);
-  const long long du = (x - S.scum[f][lo] + cu - 1) / cu;
-  S.bnd[f][c] = lo * P.ct * P.ku + (int)min(du, (long long)P.ct * P.ku);
+  // inside slot lo: pairs of cost pc, each a pass-start charge then ku units
+  const int r = S.slot[lo].z, cu = unit_cost(r), pc = pair_cost(P, r);
+  const long long rem = x - S.scum[f][lo];
+  const int q = (int)(rem / pc);
+  int u;
+  if (q >= P.ct) {
+    u = P.ct * P.ku;
+  } else {
+    const long long v = rem - (long long)q * pc - (long long)r * kPassCost;
+    u = q * P.ku + (v <= 0 ? 0 : (int)min((long long)P.ku, (v + cu - 1) / cu));
+  }
+  S.bnd[f][c] = lo * P.ct * P.ku + u;
 }
 
 // Exclusive prefix of the partial-sum sizes of all (slot, tile) pairs of FC f (one warp).
@@ -474,6 +491,15 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
     mbar_arrive(&S.gsready);
     partial_bases(S, L.f[0], 0);
     partial_bases(S, L.f[1], 1);
+    __syncwarp();
+    // this CTA's partial-row offset in each of its segments
+    for (int i = lane; i < S.nseg[0] + S.nseg[1]; i += 32) {
+      const int f = i < S.nseg[0] ? 0 : 1, si = f == 0 ? i : i - S.nseg[0];
+      const FcPlan &P = L.f[f];
+      Seg &sg = S.seg[f][si];
+      sg.dst = S.base[f][sg.pair] +
+               busy_ctas(S, f, first_cta(S, P, f, sg.pair), (int)blockIdx.x) * S.slot[sg.a].z * P.NT;
+    }
     mbar_arrive(&S.basesready);
     first_done = true;
   };
@@ -657,7 +683,7 @@ __device__ __forceinline__ void consume_kg(const unsigned char *rows, int row_by
 }
 
 struct PassCtx {
-  int f, a, t, pair, c0, rows, j0, j1;
+  int f, si, a, t, pair, c0, rows, j0, j1;
   int4 sd;
 };
 
@@ -906,8 +932,7 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
   // partial rows of this segment: dst[row * NT + col], row = c0 + r (the
   // offsets are computed by the activation copy warp after its first copies)
   wait_bar(S, g, &S.basesready, 0u);
-  float *dst = (C.f == 0 ? g.p1 : g.p2) + S.base[C.f][C.pair] +
-               (size_t)busy_ctas(S, C.f, first_cta(S, P, C.f, C.pair), (int)blockIdx.x) * C.sd.z * P.NT;
+  float *dst = (C.f == 0 ? g.p1 : g.p2) + S.seg[C.f][C.si].dst;
   if (active && rg == 0) {
     const float fold = FMT == QMOE_NVFP4 ? 0x1p120f : 1.0f;
 #pragma unroll
@@ -991,6 +1016,7 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const Layer
       const Seg sg = S.seg[f][si];
       PassCtx C;
       C.f = f;
+      C.si = si;
       C.pair = sg.pair;
       C.a = sg.a;
       C.t = sg.t;
@@ -1160,12 +1186,15 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
     const FcPlan &P = L.f[f];
     slot = std::max(slot, P.RGS * P.rg_stride + (P.kn ? P.bpu * P.NT : 0));
     win = std::max(win, (P.tma ? kTmaWB : P.WB) * P.NT);
-    // segments of one CTA: at most one more than the whole pairs its units
-    // span.  Its units cost at most total / G + one unit, and the total is
-    // ct * ku * sum over slots of (1 + 4 rows) <= ct * ku * 5 R.
-    const size_t total = (size_t)P.ct * P.ku * 5 * R;
-    const size_t upc = total / (G * (size_t)unit_cost(1)) + 2;
-    if ((upc + P.ku - 1) / P.ku + 1 > (size_t)kMaxSegs) {
+    // segments of one CTA: at most the pairs that exist, and at most two more
+    // (the first and the last) than the pairs lying wholly inside its cost
+    // range [c * total / G, (c + 1) * total / G], each of which costs at
+    // least kPassCost + 5 ku.  The total is ct * sum over slots of
+    // (rows * kPassCost + ku * (1 + 4 rows)) <= ct * (kPassCost + 5 ku) R.
+    const size_t pc_min = kPassCost + 5 * (size_t)P.ku;
+    const size_t total = (size_t)P.ct * pc_min * R;
+    const size_t segs = std::min<size_t>(na_max * (size_t)P.ct, 2 + (total / G + 1) / pc_min);
+    if (segs > (size_t)kMaxSegs) {
       set_error("too many experts per CTA for the decode kernel (N = %d, K = %d)", P.N, P.K);
       return QMOE_ERR_UNSUPPORTED;
     }
