@@ -644,42 +644,36 @@ __device__ __forceinline__ void block_scales8(uint2 sv, float (&sc)[8]) {
   }
 }
 
-// One k-group (16 rows x 8 columns) of a unit for RC activation rows, one row
-// after the other (the words are read and decoded again for the second row:
-// measured about 5% slower than decoding once, and it keeps a single set of
-// 8 partial sums alive, which keeps the loop within its registers).
+// One k-group (16 rows x 8 columns) of a unit for one activation row: the 16
+// words are loaded first, rows 4i, 4i+1 go to one set of 8 partial sums and
+// rows 4i+2, 4i+3 to a second set (two independent FMA chains per column);
+// the 16-row partial is multiplied once by its block scale.
 template <int FMT, int RC>
 __device__ __forceinline__ void consume_kg(const unsigned char *rows, int row_bytes, const __half *xb, uint2 sv,
                                            float (&acc)[RC][8]) {
-  static_assert(RC == 1 || RC == 2, "one or two rows per pass");
+  static_assert(RC == 1, "one row per pass");
   float sc[8];
   block_scales8<FMT>(sv, sc);
+  uint32_t wv[16];
 #pragma unroll
-  for (int r = 0; r < RC; ++r) {
-    float bp[8];
+  for (int kk = 0; kk < 16; ++kk) wv[kk] = *reinterpret_cast<const uint32_t *>(rows + (size_t)kk * row_bytes);
+  const uint4 xa = *reinterpret_cast<const uint4 *>(xb), xc = *reinterpret_cast<const uint4 *>(xb + 8);
+  const uint32_t xx[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+  float bp[8], bq[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) bp[c] = 0.f;
-    // 8 k rows at a time; not unrolled, so that the words of one half are
-    // not kept alive alongside the other's (spills would go to L2: almost all
-    // of the SM's memory is shared memory here)
-#pragma unroll 1
-    for (int g8 = 0; g8 < 16; g8 += 8) {
-      uint32_t wv[8];
+  for (int c = 0; c < 8; ++c) bp[c] = bq[c] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        wv[kk] = *reinterpret_cast<const uint32_t *>(rows + (size_t)(g8 + kk) * row_bytes);
-      const uint4 x8 = *reinterpret_cast<const uint4 *>(xb + (size_t)r * kXsK + g8);
-#pragma unroll
-      for (int kk = 0; kk < 8; kk += 2) {
-        uint32_t p[4], q[4];
-        dec8(wv[kk], p);
-        dec8(wv[kk + 1], q);
-        fma16(p, q, kk == 0 ? x8.x : kk == 2 ? x8.y : kk == 4 ? x8.z : x8.w, bp);
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(bp[c], sc[c], acc[r][c]);
+  for (int kk = 0; kk < 16; kk += 4) {
+    uint32_t p[4], q[4], r[4], t[4];
+    dec8(wv[kk], p);
+    dec8(wv[kk + 1], q);
+    dec8(wv[kk + 2], r);
+    dec8(wv[kk + 3], t);
+    fma16(p, q, xx[kk >> 1], bp);
+    fma16(r, t, xx[(kk >> 1) + 1], bq);
   }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[0][c] = fmaf(bp[c] + bq[c], sc[c], acc[0][c]);
 }
 
 struct PassCtx {
@@ -847,7 +841,7 @@ __device__ bool prestage_fc2(Shared &S, const LayerArgs &g, const LayerPlan &L, 
 // WPW = 32 / RGS column words (8 columns each) over all RGS row groups,
 // lane = rg * WPW + wl; the row-group partial sums are combined with warp
 // shuffles, so the pass needs no CTA barrier.
-template <int FMT, int RC>
+template <int FMT, int RC, int KN>
 __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const LayerPlan &L, const PassCtx &C,
                                          unsigned char *ring, uint8_t *win, const uint8_t *stage, __half *xw,
                                          unsigned char *xraw, uint32_t &it, uint32_t &wn, uint32_t &xn,
@@ -872,6 +866,11 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
   const int xw_units = kXsK / unit_k;
   int cur_wid = -1;
   uint32_t ws = 0;
+  // ring position of the pass's first unit; advanced without division
+  const uint32_t ring_n = (uint32_t)L.ring;
+  uint32_t slot = it % ring_n, phase = (it / ring_n) & 1u;
+  // k-major scales: this lane's 8 scale bytes sit at a fixed offset in every slot
+  const int sc_lane = P.sc_off + ((rg * 16) / BS) * P.NT + 8 * w;
   for (int xj = C.j0; xj < C.j1; xj += xw_units) {
     const int xj1 = min(C.j1, xj + xw_units);
     const int k0 = xj * unit_k, len = min(P.K, xj1 * unit_k) - k0;
@@ -886,8 +885,23 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
 #pragma unroll
     for (int r = 0; r < RC; ++r) sh[r] = nsh[r];
     for (int j = xj; j < xj1; ++j, ++it) {
+      if (KN) {  // k-major scales come with the unit: no windows
+        wait_bar(S, g, &S.full[slot], phase);
+        const int kg = j * P.RGS + rg;
+        const unsigned char *sb = ring + (size_t)slot * L.slot_bytes;
+        if (active && kg < P.nkg)
+          consume_kg<FMT, RC>(sb + (size_t)rg * P.rg_stride + 4 * w, row_bytes, xw + (kg * 16 - k0),
+                              *reinterpret_cast<const uint2 *>(sb + sc_lane), acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+        if (++slot == ring_n) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        continue;
+      }
       const int wid = unit_window<FMT>(P, j);
-      if (!P.kn && wid != cur_wid) {  // k-major scales come with the unit
+      if (wid != cur_wid) {
         if (P.tma) {
           ws = wn & 1u;
           wait_bar(S, g, &S.wfull[ws], (wn >> 1) & 1u);
@@ -910,12 +924,9 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
       if (active && kg < P.nkg) {
         const unsigned char *rows = ring + (size_t)s * L.slot_bytes + (size_t)rg * P.rg_stride + 4 * w;
         const int blk = (kg * 16) / BS - cur_wid * P.WB;
-        const uint2 sv =
-            P.kn    ? *reinterpret_cast<const uint2 *>(ring + (size_t)s * L.slot_bytes + P.sc_off +
-                                                       (size_t)((kg * 16) / BS - (j * 16 * P.RGS) / BS) * P.NT + 8 * w)
-            : P.tma ? *reinterpret_cast<const uint2 *>(win + (size_t)warp * kTmaWB * 8 * wpw + (size_t)blk * 8 * wpw +
-                                                       8 * wl)
-                    : *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
+        const uint2 sv = P.tma ? *reinterpret_cast<const uint2 *>(win + (size_t)warp * kTmaWB * 8 * wpw +
+                                                                   (size_t)blk * 8 * wpw + 8 * wl)
+                               : *reinterpret_cast<const uint2 *>(win + (size_t)blk * P.NT + 8 * w);
         consume_kg<FMT, RC>(rows, row_bytes, xw + (kg * 16 - k0), sv, acc);
       }
       __syncwarp();
@@ -998,7 +1009,7 @@ __device__ __noinline__ void finalize(Shared &S, const LayerArgs &g, const Layer
   }
 }
 
-template <int FMT>
+template <int FMT, int KN>
 __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
                                       uint8_t *win, const uint8_t *stage, __half *xs, unsigned char *xraw) {
   uint32_t it = 0, wn = 0, xn = 0;
@@ -1026,7 +1037,7 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const Layer
       for (int c0 = 0; c0 < C.sd.z; c0 += kRowsMax) {
         C.c0 = c0;
         C.rows = min(kRowsMax, C.sd.z - c0);
-        run_pass<FMT, kRowsMax>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
+        run_pass<FMT, kRowsMax, KN>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
       }
     }
   }
@@ -1103,8 +1114,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
     producer<FMT, 0>(S, g, L, ring, stage, xraw);
   else if (warp == kWarpS)
     producer<FMT, 1>(S, g, L, ring, stage, xraw);
+  else if (L.f[0].kn)  // both FCs share the scale layout
+    consumer<FMT, 1>(S, g, L, ring, win, stage, xs, xraw);
   else
-    consumer<FMT>(S, g, L, ring, win, stage, xs, xraw);
+    consumer<FMT, 0>(S, g, L, ring, win, stage, xs, xraw);
 }
 
 // ---- host side ---------------------------------------------------------------------------
