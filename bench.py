@@ -355,11 +355,52 @@ def run_gpu(args):
                     "d2h_bytes_per_step": d2h},
             "clocks": clocks.summary(t_host0, t_host1),
             "cpu_baseline": cpu,
+            "dequant": bench_dequant(device, peak) if not args.no_dequant else None,
         }
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return res
+
+
+# ---------------------------------------------------------------- prefill dequant
+
+def bench_dequant(device, peak: float, reps: int = 10) -> dict:
+    """The prefill FP4 -> bf16 dequantisation on the NVFP4 prefill shape's FC1
+    weights (E=128, K=2048, N=3072): 384 MiB codes + 48 MiB scales read,
+    1.5 GiB bf16 written per launch (far above L2).  Event-timed on the
+    launching stream, after warm-up."""
+    import torch
+    import block_scaled_fp4_gb300 as q
+    E, K, N = 128, 2048, 3072
+    gen = torch.Generator(device=device)
+    gen.manual_seed(77)
+    packed = torch.randint(0, 256, (E, K, N // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    idx = torch.randint(0, 32, (E, N, K // 16), generator=gen, device=device, dtype=torch.int32)
+    scales = (((idx // 8) + 5) << 3 | (idx % 8)).to(torch.uint8)
+    g = torch.ldexp(torch.ones(E, device=device),
+                    -torch.randint(0, 5, (E,), generator=gen, device=device).float()).float()
+    out = torch.empty((E, N, K), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            q.dequant(packed, scales, g, q.NVFP4, out=out, stream=stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record(stream)
+        for i in range(reps):
+            q.dequant(packed, scales, g, q.NVFP4, out=out, stream=stream)
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    us = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(reps))
+    med = us[len(us) // 2]
+    alg = E * K * (N // 2) + E * N * (K // 16) + E * N * K * 2 + E * 4
+    gbs = alg / (med * 1e-6) / 1e9
+    del packed, scales, out
+    return {"kernel": "dequant_kernel<NVFP4> (FP4 -> bf16, [E,K,N/2] -> [E,N,K])",
+            "workload": f"E={E} K={K} N={N} NVFP4 (prefill FC1 weights)", "us": round(med, 2),
+            "us_p10_p90": [round(us[max(0, len(us) // 10)], 2), round(us[min(len(us) - 1, 9 * len(us) // 10)], 2)],
+            "bound": "hbm", "alg_bytes": alg, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "launches": reps}
 
 
 # ---------------------------------------------------------------- CPU (oracle)
@@ -432,6 +473,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="distinct layers per step (default 40; fewer only for small profiler runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dequant", action="store_true", help="skip the prefill dequant measurement")
     ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],
                     help="block-scale layout the layer reads (default: k-major, prepared once at load)")
     args = ap.parse_args(argv)
