@@ -356,6 +356,7 @@ def run_gpu(args):
             "clocks": clocks.summary(t_host0, t_host1),
             "cpu_baseline": cpu,
             "dequant": bench_dequant(device, peak) if not args.no_dequant else None,
+            "prefill": bench_prefill(device, peak) if not args.no_prefill else None,
         }
     if world > 1:
         import torch.distributed as dist
@@ -401,6 +402,79 @@ def bench_dequant(device, peak: float, reps: int = 10) -> dict:
             "us_p10_p90": [round(us[max(0, len(us) // 10)], 2), round(us[min(len(us) - 1, 9 * len(us) // 10)], 2)],
             "bound": "hbm", "alg_bytes": alg, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(gbs / peak, 4), "launches": reps}
+
+
+# ---------------------------------------------------------------- prefill
+
+def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
+    """The prefill path on the NVFP4 prefill workload (2048 tokens, 128
+    experts, top-8, H=2048, I=1536): the whole forward call (routing, FP4 ->
+    bf16 dequantisation of both FCs, two grouped GEMMs, un-permute) and the
+    same call with the dequantised weights given (routing + GEMMs +
+    un-permute).  Event-timed on the launching stream after warm-up."""
+    import numpy as np
+    import torch
+    import block_scaled_fp4_gb300 as q
+    import synthetic as syn
+    wl = syn.WORKLOADS["nvfp4_prefill"]
+    T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
+    gen = torch.Generator(device=device)
+    gen.manual_seed(99)
+
+    def codes(shape):
+        return torch.randint(0, 256, shape, generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+
+    def e4m3(shape):
+        idx = torch.randint(0, 32, shape, generator=gen, device=device, dtype=torch.int32)
+        return (((idx // 8) + 5) << 3 | (idx % 8)).to(torch.uint8)
+
+    def gscale():
+        return torch.ldexp(torch.ones(E, device=device),
+                           -torch.randint(0, 5, (E,), generator=gen, device=device).float()).float()
+
+    rng = syn.rng_for(1234, 7)
+    x = torch.from_numpy(syn.activations(rng, T, H).view(np.int16)).to(device).view(torch.bfloat16)
+    lg = torch.from_numpy(syn.logits(rng, T, E, wl.logit_std)).to(device)
+    w1, s1, g1 = codes((E, H, I)), e4m3((E, 2 * I, H // 16)), gscale()
+    w2, s2, g2 = codes((E, I, H // 2)), e4m3((E, H, I // 16)), gscale()
+    w1d, w2d = q.dequant(w1, s1, g1, q.NVFP4), q.dequant(w2, s2, g2, q.NVFP4)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device=device)
+    ws_full = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4), dtype=torch.uint8, device=device)
+    ws_gemm = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4, True), dtype=torch.uint8, device=device)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+            ev[0].record(stream)
+            for i in range(reps):
+                fn()
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        us = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(reps))
+        return us[len(us) // 2]
+
+    full = timed(lambda: q.moe_forward(x, lg, w1, s1, g1, w2, s2, g2, q.NVFP4, k, out=out, workspace=ws_full,
+                                       stream=stream))
+    gemm = timed(lambda: q.moe_forward(x, lg, w1, s1, g1, w2, s2, g2, q.NVFP4, k, w1_dequant=w1d,
+                                       w2_dequant=w2d, out=out, workspace=ws_gemm, stream=stream))
+    R = T * k
+    flops = 2.0 * R * (H * 2 * I + I * H)
+    wbytes = E * (2 * I * H + H * I) * 2  # bf16 weights streamed by the GEMMs
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    tflops = flops / (gemm * 1e-6) / 1e12
+    del w1d, w2d, ws_full, ws_gemm
+    return {"workload": f"nvfp4_prefill: T={T} E={E} k={k} H={H} I={I} NVFP4 SwiGLU",
+            "us_forward": round(full, 1), "us_forward_predequantised": round(gemm, 1),
+            "gemm_flops": int(flops), "tflops": round(tflops, 1), "tensor_peak_tflops": tc_peak,
+            "tensor_frac": round(tflops / tc_peak, 4),
+            "bf16_weight_bytes": int(wbytes), "weight_gbs": round(wbytes / (gemm * 1e-6) / 1e9, 1),
+            "hbm_frac": round(wbytes / (gemm * 1e-6) / 1e9 / hbm_peak, 4),
+            "kernels": "route, dequant x2 (full call only), grouped_gemm_kernel x2 (mma.sync bf16), unpermute"}
 
 
 # ---------------------------------------------------------------- CPU (oracle)
@@ -474,6 +548,7 @@ def main(argv=None):
                     help="distinct layers per step (default 40; fewer only for small profiler runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dequant", action="store_true", help="skip the prefill dequant measurement")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill forward measurement")
     ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],
                     help="block-scale layout the layer reads (default: k-major, prepared once at load)")
     args = ap.parse_args(argv)

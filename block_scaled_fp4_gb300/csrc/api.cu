@@ -145,7 +145,7 @@ extern "C" qmoe_status qmoe_fp4_scales_kmajor(const uint8_t *block_scales, int E
   const size_t bytes = (size_t)E * N * (K / block_size((int)fmt));
   const uintptr_t a = (uintptr_t)block_scales, b = (uintptr_t)out;
   QMOE_REQUIRE(a + bytes <= b || b + bytes <= a, QMOE_ERR_INVALID_ARG, "out overlaps block_scales");
-  return cuda_status(launch_scales_kmajor(block_scales, E, N, K / block_size((int)fmt), out, stream),
+  return cuda_status(launch_transpose_bytes(block_scales, E, N, K / block_size((int)fmt), out, stream),
                      "scales_kmajor launch");
 }
 
@@ -179,6 +179,109 @@ static DecodeLayout decode_layout(void *ws, int T, int E, int k, size_t p1_float
 
 }  // namespace qmoe
 
+namespace qmoe {
+
+// Prefill workspace: routing results, the dequantised weights (unless the
+// caller passes them), page-layout scales reconstituted from k-major ones
+// (only then), FC1 activations and FC2 rows in permuted order.
+struct PrefillLayout {
+  int32_t *ids, *offsets, *p2e, *e2p;
+  float *weights, *y;
+  uint16_t *w1d, *w2d, *act;
+  uint8_t *s1p, *s2p;
+  size_t bytes;
+};
+
+static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k, int bs, bool need_w1, bool need_w2,
+                                    bool kmajor) {
+  const size_t R = (size_t)T * k;
+  Carve c(ws);
+  PrefillLayout L{};
+  L.ids = c.take<int32_t>(R);
+  L.weights = c.take<float>(R);
+  L.offsets = c.take<int32_t>((size_t)E + 1);
+  L.p2e = c.take<int32_t>(R);
+  L.e2p = c.take<int32_t>(R);
+  L.act = c.take<uint16_t>(R * I);
+  L.y = c.take<float>(R * H);
+  if (need_w1) L.w1d = c.take<uint16_t>((size_t)E * 2 * I * H);
+  if (need_w2) L.w2d = c.take<uint16_t>((size_t)E * H * I);
+  if (need_w1 && kmajor) L.s1p = c.take<uint8_t>((size_t)E * 2 * I * (H / bs));
+  if (need_w2 && kmajor) L.s2p = c.take<uint8_t>((size_t)E * H * (I / bs));
+  L.bytes = (c.off + 255) & ~(size_t)255;
+  return L;
+}
+
+// T * k > QMOE_GEMV_MAX_ROWS: route, dequantise (unless given), grouped GEMMs,
+// weighted un-permute.  Arguments already checked by the caller: routing
+// sizes, format, H and I, swiglu_fusion, alpha / beta / limit.
+static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w, const uint8_t *fc1_s,
+                                   const float *fc1_g, const uint8_t *fc2_w, const uint8_t *fc2_s, const float *fc2_g,
+                                   const uint16_t *fc1_wd, const uint16_t *fc2_wd, int fmt, bool kmajor, int T, int H,
+                                   int I, int E, int k, int normalize, float alpha, float beta, float limit,
+                                   uint16_t *out, int32_t *topk_ids_out, void *workspace, size_t *workspace_bytes,
+                                   cudaStream_t stream) {
+  QMOE_REQUIRE((long long)T * k <= (1LL << 30), QMOE_ERR_UNSUPPORTED, "T*k too large");
+  const int bs = block_size(fmt);
+  const bool need_w1 = fc1_wd == nullptr, need_w2 = fc2_wd == nullptr;
+  const PrefillLayout need = prefill_layout(nullptr, T, H, I, E, k, bs, need_w1, need_w2, kmajor);
+  if (!workspace) {
+    *workspace_bytes = need.bytes;
+    return QMOE_OK;
+  }
+  QMOE_REQUIRE(*workspace_bytes >= need.bytes, QMOE_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes",
+               *workspace_bytes, need.bytes);
+  QMOE_REQUIRE(x && out, QMOE_ERR_INVALID_ARG, "x and out must be non-NULL");
+  QMOE_REQUIRE((!need_w1 || (fc1_w && fc1_s)) && (!need_w2 || (fc2_w && fc2_s)), QMOE_ERR_INVALID_ARG,
+               "weights and scales must be non-NULL when no dequantised weights are given");
+  QMOE_REQUIRE(aligned16(x) && aligned16(out) && aligned16(workspace) && (!fc1_wd || aligned16(fc1_wd)) &&
+                   (!fc2_wd || aligned16(fc2_wd)) && (!need_w1 || (aligned16(fc1_w) && aligned16(fc1_s))) &&
+                   (!need_w2 || (aligned16(fc2_w) && aligned16(fc2_s))),
+               QMOE_ERR_MISALIGNED, "x, out, workspace, weights and scales must be 16-byte aligned");
+  QMOE_REQUIRE((fc1_g == nullptr || ((uintptr_t)fc1_g & 3u) == 0) && (fc2_g == nullptr || ((uintptr_t)fc2_g & 3u) == 0),
+               QMOE_ERR_MISALIGNED, "global scales must be 4-byte aligned");
+  const PrefillLayout L = prefill_layout(workspace, T, H, I, E, k, bs, need_w1, need_w2, kmajor);
+  RouteOut ro{};
+  ro.ids = topk_ids_out ? topk_ids_out : L.ids;
+  ro.weights = L.weights;
+  ro.offsets = L.offsets;
+  ro.p2e = L.p2e;
+  ro.e2p = L.e2p;
+  cudaError_t err = launch_route(logits, T, E, k, normalize, ro, stream);
+  if (err != cudaSuccess) return cuda_status(err, "route launch");
+  const uint16_t *w1d = fc1_wd, *w2d = fc2_wd;
+  if (need_w1) {
+    const uint8_t *s1 = fc1_s;
+    if (kmajor) {  // [E, H/bs, 2I] -> [E, 2I, H/bs]
+      err = launch_transpose_bytes(fc1_s, E, H / bs, 2 * I, L.s1p, stream);
+      if (err != cudaSuccess) return cuda_status(err, "scale transpose launch");
+      s1 = L.s1p;
+    }
+    err = launch_dequant(fc1_w, s1, fc1_g, E, 2 * I, H, fmt, L.w1d, stream);
+    if (err != cudaSuccess) return cuda_status(err, "dequant launch");
+    w1d = L.w1d;
+  }
+  if (need_w2) {
+    const uint8_t *s2 = fc2_s;
+    if (kmajor) {  // [E, I/bs, H] -> [E, H, I/bs]
+      err = launch_transpose_bytes(fc2_s, E, I / bs, H, L.s2p, stream);
+      if (err != cudaSuccess) return cuda_status(err, "scale transpose launch");
+      s2 = L.s2p;
+    }
+    err = launch_dequant(fc2_w, s2, fc2_g, E, H, I, fmt, L.w2d, stream);
+    if (err != cudaSuccess) return cuda_status(err, "dequant launch");
+    w2d = L.w2d;
+  }
+  PrefillArgs a{};
+  a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
+  a.alpha = alpha; a.beta = beta; a.limit = limit;
+  a.x = x; a.offsets = L.offsets; a.p2e = L.p2e; a.e2p = L.e2p; a.weights = L.weights;
+  a.w1d = w1d; a.w2d = w2d; a.act = L.act; a.y = L.y; a.out = out;
+  return cuda_status(launch_prefill(a, stream), "prefill launch");
+}
+
+}  // namespace qmoe
+
 extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w,
                                             const uint8_t *fc1_s, const float *fc1_g, const uint8_t *fc2_w,
                                             const uint8_t *fc2_s, const float *fc2_g, const uint16_t *fc1_wd,
@@ -201,11 +304,11 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   QMOE_REQUIRE(!std::isnan(alpha) && !std::isnan(beta) && !std::isnan(limit), QMOE_ERR_INVALID_ARG,
                "alpha, beta and limit must not be NaN");
   const long long R = (long long)T * k;
-  const bool gemv = R <= QMOE_GEMV_MAX_ROWS;
-  QMOE_REQUIRE(gemv, QMOE_ERR_UNSUPPORTED, "T*k = %lld > %d needs the prefill path", R, QMOE_GEMV_MAX_ROWS);
+  if (R > QMOE_GEMV_MAX_ROWS)
+    return prefill_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, fc1_wd, fc2_wd, base_fmt, kmajor, T, H,
+                           I, E, k, normalize, alpha, beta, limit, out, topk_ids_out, workspace, workspace_bytes,
+                           stream);
   QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
-  (void)fc1_wd;
-  (void)fc2_wd;
   LayerPlan plan;
   size_t p1_floats = 0, p2_floats = 0;
   st = make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);

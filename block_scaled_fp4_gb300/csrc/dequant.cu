@@ -158,40 +158,41 @@ cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const f
 
 namespace qmoe {
 
-// Block scales [E, N, nb] -> [E, nb, N], bytes unchanged: 64 x 64 byte tiles
-// through shared memory (reads along nb and writes along N both coalesced).
-constexpr int kKmTile = 64;
-constexpr int kKmThreads = 256;
+// out[e][c][r] = in[e][r][c], bytes unchanged: 64 x 64 byte tiles through
+// shared memory (reads along c and writes along r both coalesced), ragged
+// edges in both dimensions.  Block scales [E, N, nb] -> [E, nb, N] and back.
+constexpr int kTrTile = 64;
+constexpr int kTrThreads = 256;
 
-__global__ void __launch_bounds__(kKmThreads) scales_kmajor_kernel(const uint8_t *__restrict__ in, int E, int N,
-                                                                   int nb, uint8_t *__restrict__ out) {
-  __shared__ uint8_t t[kKmTile][kKmTile + 4];
-  const int tn = N / kKmTile, tb = (nb + kKmTile - 1) / kKmTile;
-  const long long ntiles = (long long)E * tn * tb;
+__global__ void __launch_bounds__(kTrThreads) transpose_bytes_kernel(const uint8_t *__restrict__ in, int E, int rows,
+                                                                     int cols, uint8_t *__restrict__ out) {
+  __shared__ uint8_t t[kTrTile][kTrTile + 4];
+  const int tr = (rows + kTrTile - 1) / kTrTile, tc = (cols + kTrTile - 1) / kTrTile;
+  const long long ntiles = (long long)E * tr * tc;
   for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int e = (int)(tile / ((long long)tn * tb));
-    const int rem = (int)(tile - (long long)e * tn * tb);
-    const int n0 = (rem / tb) * kKmTile, b0 = (rem % tb) * kKmTile;
-    const int bw = min(kKmTile, nb - b0);
+    const int e = (int)(tile / ((long long)tr * tc));
+    const int rem = (int)(tile - (long long)e * tr * tc);
+    const int r0 = (rem / tc) * kTrTile, c0 = (rem % tc) * kTrTile;
+    const int rh = min(kTrTile, rows - r0), cw = min(kTrTile, cols - c0);
     __syncthreads();  // the previous tile's reads are done
-    for (int i = threadIdx.x; i < kKmTile * kKmTile; i += kKmThreads) {
-      const int r = i / kKmTile, c = i % kKmTile;  // r: column n0 + r, c: block b0 + c
-      if (c < bw) t[r][c] = in[((size_t)e * N + n0 + r) * nb + b0 + c];
+    for (int i = threadIdx.x; i < kTrTile * kTrTile; i += kTrThreads) {
+      const int r = i / kTrTile, c = i % kTrTile;
+      if (r < rh && c < cw) t[r][c] = in[((size_t)e * rows + r0 + r) * cols + c0 + c];
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < kKmTile * kKmTile; i += kKmThreads) {
-      const int r = i / kKmTile, c = i % kKmTile;  // r: block b0 + r, c: column n0 + c
-      if (r < bw) out[((size_t)e * nb + b0 + r) * N + n0 + c] = t[c][r];
+    for (int i = threadIdx.x; i < kTrTile * kTrTile; i += kTrThreads) {
+      const int c = i / kTrTile, r = i % kTrTile;
+      if (r < rh && c < cw) out[((size_t)e * cols + c0 + c) * rows + r0 + r] = t[r][c];
     }
   }
 }
 
-cudaError_t launch_scales_kmajor(const uint8_t *in, int E, int N, int nb, uint8_t *out, cudaStream_t stream) {
-  const long long ntiles = (long long)E * (N / kKmTile) * ((nb + kKmTile - 1) / kKmTile);
+cudaError_t launch_transpose_bytes(const uint8_t *in, int E, int rows, int cols, uint8_t *out, cudaStream_t stream) {
+  const long long ntiles = (long long)E * ((rows + kTrTile - 1) / kTrTile) * ((cols + kTrTile - 1) / kTrTile);
   if (ntiles == 0) return cudaSuccess;
   long long grid = (long long)num_sms() * 8;
   if (grid > ntiles) grid = ntiles;
-  scales_kmajor_kernel<<<(unsigned)grid, kKmThreads, 0, stream>>>(in, E, N, nb, out);
+  transpose_bytes_kernel<<<(unsigned)grid, kTrThreads, 0, stream>>>(in, E, rows, cols, out);
   return cudaGetLastError();
 }
 

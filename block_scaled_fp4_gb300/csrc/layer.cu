@@ -163,11 +163,6 @@ __device__ __forceinline__ float ldexp2(float x, int d) {
   return x * pow2f(h) * pow2f(d - h);
 }
 
-__device__ __forceinline__ float swiglu(float gate, float lin, float alpha, float beta, float limit) {
-  const float G = fminf(gate, limit);
-  const float L = fmaxf(fminf(lin, limit), -limit);
-  return G * (1.0f / (1.0f + expf(-alpha * G))) * (L + beta);
-}
 
 // Shift that puts the largest |x| (bf16 bits, sign cleared) in [2^14, 2^15).
 __device__ __forceinline__ int row_shift(uint32_t m) {

@@ -68,6 +68,15 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// SwiGLU of one (gate, linear) pair ("MoE and QMoE - CUDA Operator
+// Documentation" §8): G = min(gate, limit), L = clamp(linear, -limit, limit),
+// G * sigmoid(alpha * G) * (L + beta).
+__device__ __forceinline__ float swiglu(float gate, float lin, float alpha, float beta, float limit) {
+  const float G = fminf(gate, limit);
+  const float L = fmaxf(fminf(lin, limit), -limit);
+  return G * (1.0f / (1.0f + expf(-alpha * G))) * (L + beta);
+}
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 // ---- host side -------------------------------------------------------------------
@@ -148,6 +157,24 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const float *g, int E, int N, int K,
                            int fmt, uint16_t *out, cudaStream_t stream);
-cudaError_t launch_scales_kmajor(const uint8_t *in, int E, int N, int nb, uint8_t *out, cudaStream_t stream);
+// out[e][c][r] = in[e][r][c] for an [E, rows, cols] byte array (both
+// directions of the block-scale layout conversion).
+cudaError_t launch_transpose_bytes(const uint8_t *in, int E, int rows, int cols, uint8_t *out, cudaStream_t stream);
+
+// Prefill (T * k > 64): grouped GEMMs over dequantised bf16 weights.
+struct PrefillArgs {
+  int T, H, I, E, k;
+  float alpha, beta, limit;
+  const uint16_t *x;         // bf16 [T, H]
+  const int32_t *offsets;    // [E + 1]
+  const int32_t *p2e, *e2p;  // [T * k] permute maps
+  const float *weights;      // [T * k] routing weights
+  const uint16_t *w1d;       // bf16 [E, 2I, H]
+  const uint16_t *w2d;       // bf16 [E, H, I]
+  uint16_t *act;             // bf16 [T * k, I] FC1 activations, permuted order
+  float *y;                  // fp32 [T * k, H] FC2 rows, permuted order
+  uint16_t *out;             // bf16 [T, H]
+};
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
 
 }  // namespace qmoe

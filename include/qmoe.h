@@ -135,7 +135,8 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   fc1_wd       bf16 [E, 2I, H] already-dequantised FC1 weights, or NULL;
  *   fc2_wd       bf16 [E, H, I] already-dequantised FC2 weights, or NULL.
  *                (Used only when T * k > QMOE_GEMV_MAX_ROWS; when NULL that
- *                path dequantises into the workspace.)
+ *                path dequantises into the workspace, so its workspace holds
+ *                E * 3 * H * I bf16 values more.)
  *   fmt          QMOE_NVFP4 or QMOE_MXFP4, optionally | QMOE_SCALES_KMAJOR
  *                (both FCs' block scales in the k-major layout).  The result
  *                does not depend on the layout beyond the order of the fp32
@@ -150,9 +151,16 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   workspace, workspace_bytes: see the conventions above.
  * T * k <= QMOE_GEMV_MAX_ROWS runs the decode path (routing kernel, then one
  * persistent kernel for FC1, SwiGLU, FC2 and the un-permute, dequantising in
- * registers); larger T * k runs the prefill path.  The decode kernel is a
- * cooperative launch of one CTA per SM: it needs the whole GPU's residency
- * and returns QMOE_ERR_CUDA if another context keeps it from launching.
+ * registers).  The decode kernel is a cooperative launch of one CTA per SM:
+ * it needs the whole GPU's residency and returns QMOE_ERR_CUDA if another
+ * context keeps it from launching.  Larger T * k runs the prefill path
+ * ("[CUDA] Coalesce QMoE MXFP4/NVFP4 weight dequantization", PR #31349;
+ * operator doc §4.3, §9b.1): routing, FP4 -> bf16 dequantisation of both FCs
+ * (skipped for the FCs whose fc*_wd is given), two grouped bf16 GEMMs on the
+ * tensor cores with fp32 accumulation (the gather folded into the first, the
+ * SwiGLU into its epilogue; the activation rounded to bf16), and the weighted
+ * un-permute.  Numerically the two paths agree within the tolerance of fp32
+ * accumulation, not bit for bit.
  */
 qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits,
                                  const uint8_t *fc1_w, const uint8_t *fc1_s, const float *fc1_g,
