@@ -89,7 +89,7 @@ extern "C" const char *qmoe_last_error(void) { return g_err; }
 extern "C" int qmoe_set_stage_events(cudaEvent_t *events, int n_events) {
   g_stage_events = events;
   g_stage_nevents = events ? n_events : 0;
-  return 2;
+  return 1;
 }
 
 extern "C" qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normalize, int32_t *topk_ids,
@@ -329,36 +329,25 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
                QMOE_ERR_MISALIGNED, "global scales must be 4-byte aligned");
 
   const DecodeLayout L = decode_layout(workspace, T, E, k, p1_floats, p2_floats);
-  RouteOut ro{};
-  ro.ids = topk_ids_out ? topk_ids_out : L.ids;
-  ro.weights = L.weights;
-  ro.offsets = L.offsets;
-  ro.p2e = L.p2e;
-  ro.e2p = L.e2p;
-  ro.active = L.active;
-  ro.meta = L.meta;
-  ro.slots = L.slots;
-  ro.zero_words = L.meta + 1;  // error flag and grid-barrier counters start every call at 0
-  ro.n_zero_words = 3;
-
   LayerArgs g{};
   g.fmt = base_fmt;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
   g.alpha = alpha; g.beta = beta; g.limit = limit;
+  g.logits = logits; g.normalize = normalize; g.route_n = route_keys_per_lane(E, k);
+  g.ids_out = topk_ids_out;
   g.x = x;
   g.w1 = fc1_w; g.s1 = fc1_s; g.g1 = fc1_g;
   g.w2 = fc2_w; g.s2 = fc2_s; g.g2 = fc2_g;
-  g.e2p = L.e2p; g.p2e = L.p2e; g.meta = L.meta; g.slots = L.slots;
-  g.weights = L.weights;
+  g.meta = L.meta;
   g.p1 = L.p1; g.p2 = L.p2; g.out = out;
 
   stage_event(0, stream);
-  cudaError_t err = launch_route(logits, T, E, k, normalize, ro, stream);
-  if (err != cudaSuccess) return cuda_status(err, "route launch");
-  stage_event(1, stream);
+  // the error flag and the two grid-barrier counters start every call at 0
+  cudaError_t err = cudaMemsetAsync(L.meta + 1, 0, 3 * sizeof(int32_t), stream);
+  if (err != cudaSuccess) return cuda_status(err, "counter reset");
   err = launch_layer(g, plan, E, stream);
   if (err == cudaErrorCooperativeLaunchTooLarge && g_err[0]) return QMOE_ERR_CUDA;  // message already set
   if (err != cudaSuccess) return cuda_status(err, "layer launch");
-  stage_event(2, stream);
+  stage_event(1, stream);
   return QMOE_OK;
 }

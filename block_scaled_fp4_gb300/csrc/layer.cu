@@ -1,6 +1,6 @@
-// Decode path of the FP4 MoE layer in one persistent kernel: FC1 GEMV with
-// SwiGLU, FC2 GEMV and the weighted un-permute, with the E2M1 weights
-// dequantised in registers.
+// Decode path of the FP4 MoE layer in one persistent kernel: top-k softmax
+// routing and the permute maps, FC1 GEMV with SwiGLU, FC2 GEMV and the
+// weighted un-permute, with the E2M1 weights dequantised in registers.
 //
 // Prior art on the pages ("[CUDA] Speed up the NVFP4 QMoE decode GEMV and
 // enable it for MTP verify", PR #31159; operator doc §9b.2/§9b.3): coalesced
@@ -8,23 +8,23 @@
 // table-free E2M1 decode, the block scale applied to a per-block partial sum
 // instead of to every weight, fp32 accumulation for bf16 activations, and a
 // 64-expanded-row window.  Design here (sm_103a, one CTA per SM):
+//  * every CTA routes the (at most 64) expanded rows itself with the routing
+//    kernel's warp top-k and ranking code, so all CTAs hold identical maps
+//    and no separate launch sits between the call and the weight stream;
 //  * work unit = 16*RGS k rows x NT columns of one active expert's weights
 //    (about 32 KB).  The units of all active experts are laid end to end
-//    (expert slot, column tile, k) and split evenly over the CTAs
-//    ("stream-K"): every CTA streams the same number of bytes whatever the
-//    number of rows each expert received.  A CTA's consecutive units of one
+//    (expert slot, column tile, k) and split over the CTAs by cost
+//    ("stream-K"): every CTA streams about the same bytes whatever the number
+//    of rows each expert received.  A CTA's consecutive units of one
 //    (expert, tile) form a segment, which it reduces to a partial sum;
 //  * one warp issues the bulk async copies (cp.async.bulk, completion counted
 //    on an mbarrier) of the CTA's FC1 units and then, without waiting for FC1
-//    to finish anywhere, of its FC2 units into a 4-slot ring.  Just before
-//    the first unit of each window of 16 scale blocks it issues a 2-D tensor
-//    copy (cp.async.bulk.tensor) of that window's block scales, [NT][16]
-//    bytes, so scales and weights arrive in one ordered stream; the
-//    consumers transpose the window in shared memory at the window boundary
-//    so that a thread reads the 8 scale bytes of its 8 columns with one load.
-//    Scales whose rows are not 16-byte multiples are read with byte loads;
-//  * the copy warp starts once the first activations are staged: small loads
-//    issued behind a GPU-wide burst of bulk copies wait for all of it;
+//    to finish anywhere, of its FC2 units into a 3- or 4-slot ring.  With
+//    k-major block scales ([E, K/bs, N]) a unit's scale rows travel in its
+//    slot; with the [E, N, K/bs] layout, windows of 16 blocks are 2-D tensor
+//    copies transposed per warp (NVFP4) or byte loads;
+//  * a second warp copies each pass's activation rows with cp.async (the
+//    load/store path, so they do not queue behind the weight stream);
 //  * 16 consumer warps: thread (w, rg) owns column word w (8 columns) of
 //    k-group rg (16 rows) of a unit, decodes with the hardware
 //    cvt.rn.f16x2.e2m1x2 and multiplies with fma.rn.f32.f16 (fp16 operands,
@@ -34,15 +34,15 @@
 //  * activations are staged in fp16 after an exact power-of-two rescale per
 //    row (largest |x| in [2^14, 2^15)), so every finite bf16 activation is
 //    exact in fp16; the rescale is undone on the fp32 partial;
-//  * partial sums are reduced over row groups in shared memory and written to
-//    global memory (fp32).  After a grid barrier, FC2 forms its bf16
+//  * partial sums are reduced over row groups with warp shuffles and written
+//    to global memory (fp32).  After a grid barrier, FC2 forms its bf16
 //    activations a = SwiGLU(g1 * sum of FC1 partials) for the k range it
 //    needs; after a second grid barrier, out[t] = bf16(sum_j w[t][j] * g2 *
 //    sum of FC2 partials of (t, j)).  All sums run in a fixed order, so the
 //    result is deterministic;
 //  * the kernel is launched cooperatively (all CTAs resident, so the grid
-//    barriers cannot deadlock) and with programmatic dependent launch after
-//    the routing kernel, which also clears the barrier counters;
+//    barriers cannot deadlock); the barrier counters and the error flag are
+//    cleared by a 12-byte memset issued just before it;
 //  * every wait is bounded: a wait that gives up sets the device error flag
 //    meta[1] and the CTA carries on without waiting again, so no CTA hangs.
 #include <cuda.h>
@@ -97,6 +97,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                    smem_addr(dst)),
                "l"(src), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
+}
+// The same with an L2 eviction-priority policy (createpolicy): the weight
+// stream is read once per call, so it is marked evict-first and leaves the
+// kernel's code, activations and partial sums in L2 across calls.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_stream(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t done;
@@ -259,8 +275,15 @@ struct Shared {
   int scum[2][kMaxSlots + 1];          // cost prefix over expert slots
   int row2slot[kMaxSlots];
   int row_tok[kMaxSlots];              // token of each permuted row
-  int r_e2p[kMaxSlots];                 // routing results of the routing kernel
+  // routing (computed by every CTA for itself): expert and weight of each
+  // expanded row t * k + j, the permute maps, per-expert counts and offsets
+  int r_ids[kMaxSlots];
   float r_w[kMaxSlots];
+  int r_e2p[kMaxSlots];
+  int r_p2e[kMaxSlots];
+  int r_off[kMaxExperts + 1];
+  int r_cnt[kMaxExperts];
+  int r_off2[kMaxExperts];
   uint32_t wmax[kConsWarps];
   int na;
   int abort;
@@ -288,7 +311,6 @@ __device__ __forceinline__ bool wait_bar(Shared &S, const LayerArgs &g, uint64_t
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   *(volatile int *)&S.abort = 1;
-  pdl_wait();  // the routing kernel clears the flag: set it only after that
   atomicExch(g.meta + 1, 1);
   return false;
 }
@@ -302,7 +324,7 @@ __device__ void grid_barrier(Shared &S, const LayerArgs &g, int32_t *ctr) {
     for (uint32_t i = 0; ld_acquire(ctr) < (int)gridDim.x; ++i) {
       if (i >= limit) {
         *(volatile int *)&S.abort = 1;
-        atomicExch(g.meta + 1, 1);  // after pdl_wait (grid_barrier's caller)
+        atomicExch(g.meta + 1, 1);
         break;
       }
       __nanosleep(64);
@@ -321,7 +343,6 @@ __device__ void build_segments(Shared &S, const LayerArgs &g, const FcPlan &P, i
   for (int u = W.lo; u < W.hi;) {
     if (n == kMaxSegs) {  // the host bounds this; report rather than drop work
       *(volatile int *)&S.abort = 1;
-      pdl_wait();
       atomicExch(g.meta + 1, 1);
       break;
     }
@@ -467,6 +488,7 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
                                       uint8_t *stage, unsigned char *xraw) {
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   const int lane = (int)lane_id();
+  const uint64_t pol = l2_evict_first_policy();
   // the weight stream starts once the first small copies are on their way:
   // small copies issued behind a GPU-wide burst of bulk copies wait for it
   if (ROLE == 0) {
@@ -573,10 +595,11 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
             const uint8_t *ssrc =
                 (f == 0 ? g.s1 : g.s2) + ((size_t)sd.x * P.nblocks + b0) * P.N + (size_t)sg.t * P.NT;
             if (P.ct == 1) {
-              if (lane == 31) bulk_g2s(dst + P.sc_off, ssrc, (uint32_t)(nbu * P.NT), &S.full[s]);
+              if (lane == 31) bulk_g2s_stream(dst + P.sc_off, ssrc, (uint32_t)(nbu * P.NT), &S.full[s], pol);
             } else {
               for (int b = lane; b < nbu; b += 32)
-                bulk_g2s(dst + P.sc_off + (size_t)b * P.NT, ssrc + (size_t)b * P.N, (uint32_t)P.NT, &S.full[s]);
+                bulk_g2s_stream(dst + P.sc_off + (size_t)b * P.NT, ssrc + (size_t)b * P.N, (uint32_t)P.NT,
+                                &S.full[s], pol);
             }
           }
           // row group rg (16 k rows) at dst + rg * rg_stride: the padding puts
@@ -584,12 +607,12 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
           if (P.ct == 1) {
             const int nr = min(16, rows - 16 * lane);
             if (lane < P.RGS && nr > 0)
-              bulk_g2s(dst + (size_t)lane * P.rg_stride, wexp + (size_t)(r0 + 16 * lane) * row_bytes,
-                       (uint32_t)nr * row_bytes, &S.full[s]);
+              bulk_g2s_stream(dst + (size_t)lane * P.rg_stride, wexp + (size_t)(r0 + 16 * lane) * row_bytes,
+                              (uint32_t)nr * row_bytes, &S.full[s], pol);
           } else {
             for (int r = lane; r < rows; r += 32)
-              bulk_g2s(dst + (size_t)(r >> 4) * P.rg_stride + (size_t)(r & 15) * row_bytes,
-                       wexp + (size_t)(r0 + r) * (P.N / 2), row_bytes, &S.full[s]);
+              bulk_g2s_stream(dst + (size_t)(r >> 4) * P.rg_stride + (size_t)(r & 15) * row_bytes,
+                              wexp + (size_t)(r0 + r) * (P.N / 2), row_bytes, &S.full[s], pol);
           }
         }
       }
@@ -1066,37 +1089,51 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
     S.abort = 0;
     S.fc2_pre = 0;
   }
-  pdl_wait();  // the routing results (and the cleared counters) are complete
-  // one round of loads: the active-expert count, every slot (read before the
-  // count is known), and per row its token, permuted position and weight
+  // Routing, in every CTA with the routing kernel's code (so every CTA holds
+  // the same, bit-identical result and no separate launch is needed): warp w
+  // routes tokens w, w + 18, ...; then one warp ranks the T * k <= 64 rows by
+  // expert into the maps and the active-expert slots.
   const int R = g.T * g.k;
-  const int nslots = min(min(g.E, R), kMaxSlots);
-  int4 sd = make_int4(0, 0, 0, 0);
-  if (tid < nslots) sd = __ldcg(reinterpret_cast<const int4 *>(g.slots) + tid);
-  if (tid >= 64 && tid - 64 < R) S.row_tok[tid - 64] = __ldcg(g.p2e + (tid - 64)) / g.k;
-  if (tid >= 128 && tid - 128 < R) S.r_e2p[tid - 128] = __ldcg(g.e2p + (tid - 128));
-  if (tid >= 192 && tid - 192 < R) S.r_w[tid - 192] = __ldcg(g.weights + (tid - 192));
-  if (tid == 256) S.na = min(__ldcg(g.meta), kMaxSlots);
+  for (int t = warp; t < g.T; t += kLayerThreads / 32) {
+    if (g.route_n == 1) route_one_token<1>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else if (g.route_n == 2) route_one_token<2>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else if (g.route_n == 4) route_one_token<4>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else route_one_token<8>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+  }
   __syncthreads();
-  const int na = S.na;
+  if (warp == 0) {
+    RouteOut o{};
+    o.offsets = S.r_off;
+    o.p2e = S.r_p2e;
+    o.e2p = S.r_e2p;
+    o.meta = &S.na;
+    o.slots = reinterpret_cast<SlotDesc *>(S.slot);
+    build_maps_small(S.r_ids, R, g.E, o, S.r_cnt, S.r_off2);
+  } else if (blockIdx.x == 0 && g.ids_out && tid - 32 < R) {
+    g.ids_out[tid - 32] = S.r_ids[tid - 32];
+  }
+  __syncthreads();
+  const int na = min(S.na, kMaxSlots);
   if (na <= 0) return;  // every CTA sees the same count
+  if (tid < R) S.row_tok[tid] = S.r_p2e[tid] / g.k;
   if (tid < na) {
-    S.slot[tid] = sd;
+    const int4 sd = S.slot[tid];
     for (int q = 0; q < sd.z; ++q) S.row2slot[sd.y + q] = tid;
   }
   __syncthreads();
   if (warp < 2) cost_prefix(S, L.f[warp], warp);
   __syncthreads();
-  {
+  {  // the split of both FCs, one boundary per thread
     const int G = (int)gridDim.x;
     if (tid <= G) split_bound(S, L.f[0], 0, tid);
     else if (tid <= 2 * G + 1) split_bound(S, L.f[1], 1, tid - G - 1);
   }
   __syncthreads();
-  if (warp < 2) busy_prefix(S, warp);
-  __syncthreads();
-  if (warp == 2 && (tid & 31) == 0) build_segments<FMT>(S, g, L.f[0], 0);
-  if (warp == 3 && (tid & 31) == 0) build_segments<FMT>(S, g, L.f[1], 1);
+  // this CTA's segments, and (beside them) the CTAs holding units, which the
+  // partial-sum offsets need
+  if (tid == 0) build_segments<FMT>(S, g, L.f[0], 0);
+  if (tid == 32) build_segments<FMT>(S, g, L.f[1], 1);
+  if (warp == 2 || warp == 3) busy_prefix(S, warp - 2);
   __syncthreads();
   // 1 KB-aligned regions (the tensor and bulk copies need 16-byte alignment)
   unsigned char *base = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
@@ -1300,13 +1337,11 @@ static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, cuda
   cfg.blockDim = dim3(kLayerThreads);
   cfg.dynamicSmemBytes = L.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kfn, a, L);
 }
 

@@ -108,18 +108,20 @@ struct RouteOut {
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize, const RouteOut &o,
                          cudaStream_t stream);
+// Keys per lane of the warp top-k for E experts and top-k (1, 2, 4 or 8).
+int route_keys_per_lane(int E, int k);
 
 // Decode layer (R = T*k <= 64 rows): arguments of the fused kernel.
 struct LayerArgs {
   int fmt, T, H, I, E, k;
   float alpha, beta, limit;
+  const float *logits;     // fp32 [T, E] router logits
+  int normalize, route_n;  // routing: renormalise over the k; keys per lane (1, 2, 4, 8)
+  int32_t *ids_out;        // [T, k] selected experts, or null
   const uint16_t *x;       // bf16 [T, H]
   const uint8_t *w1, *s1, *w2, *s2;
   const float *g1, *g2;
-  const int32_t *e2p, *p2e;
-  int32_t *meta;           // [0] active experts, [1] device error flag, [2], [3] grid barrier counters
-  const SlotDesc *slots;
-  const float *weights;
+  int32_t *meta;           // [1] device error flag, [2], [3] grid barrier counters (zero at launch)
   float *p1, *p2;          // fp32 partial sums of FC1 / FC2 (split-K segments)
   uint16_t *out;           // [T, H] bf16
   CUtensorMap tm_s1, tm_s2;  // block scales as 2-D byte arrays (when FcPlan::tma)

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(1024) maps_kernel(int R, int E, RouteOut o) {
   build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
 }
 
-static int keys_per_lane(int E, int k) {
+int route_keys_per_lane(int E, int k) {
   int n = 1;
   while (n * 32 < E) n <<= 1;
   while (n < k) n <<= 1;
@@ -166,7 +166,7 @@ static cudaError_t launch_route_n(const float *logits, int T, int E, int k, int 
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize, const RouteOut &o,
                          cudaStream_t stream) {
-  switch (keys_per_lane(E, k)) {
+  switch (route_keys_per_lane(E, k)) {
     case 1: return launch_route_n<1>(logits, T, E, k, normalize, o, stream);
     case 2: return launch_route_n<2>(logits, T, E, k, normalize, o, stream);
     case 4: return launch_route_n<4>(logits, T, E, k, normalize, o, stream);

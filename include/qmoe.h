@@ -149,9 +149,11 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   out          bf16 [T, H] result.
  *   topk_ids_out int32 [T, k] selected experts, or NULL.
  *   workspace, workspace_bytes: see the conventions above.
- * T * k <= QMOE_GEMV_MAX_ROWS runs the decode path (routing kernel, then one
- * persistent kernel for FC1, SwiGLU, FC2 and the un-permute, dequantising in
- * registers).  The decode kernel is a cooperative launch of one CTA per SM:
+ * T * k <= QMOE_GEMV_MAX_ROWS runs the decode path: one persistent kernel for
+ * routing, FC1, SwiGLU, FC2 and the un-permute, dequantising in registers
+ * (after a 12-byte memset of its counters in the workspace).  Its routing
+ * is the code of qmoe_route_topk, so the selected experts are identical.
+ * The decode kernel is a cooperative launch of one CTA per SM:
  * it needs the whole GPU's residency and returns QMOE_ERR_CUDA if another
  * context keeps it from launching.  Larger T * k runs the prefill path
  * ("[CUDA] Coalesce QMoE MXFP4/NVFP4 weight dequantization", PR #31349;
@@ -257,8 +259,8 @@ const char *qmoe_last_error(void);
  * are created by the caller (cudaEventCreate) and must outlive the calls.
  * Pass NULL to switch it off.  Process-wide setting; not thread-safe.
  * Returns the number of kernels one forward call launches for decode shapes
- * (routing, then the fused FC1 + FC2 + un-permute kernel), i.e. how many
- * events after the first are used.
+ * (one: the fused routing + FC1 + FC2 + un-permute kernel, after a 12-byte
+ * memset of its counters), i.e. how many events after the first are used.
  */
 int qmoe_set_stage_events(cudaEvent_t *events, int n_events);
 
