@@ -489,9 +489,12 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   const int lane = (int)lane_id();
   const uint64_t pol = l2_evict_first_policy();
-  // the weight stream starts once the first small copies are on their way:
-  // small copies issued behind a GPU-wide burst of bulk copies wait for it
-  if (ROLE == 0) {
+  // With [E, N, K/bs] scales the weight stream starts once the first scale
+  // window (a tensor copy, in the same bulk-copy queue) is on its way: small
+  // copies issued behind a GPU-wide burst of bulk copies wait for all of it.
+  // With k-major scales every small copy goes through cp.async and the
+  // weight stream starts at once.
+  if (ROLE == 0 && !L.f[0].kn) {
     if (lane == 0) wait_bar(S, g, &S.smallfirst, 0u);
     __syncwarp();
   }
