@@ -33,6 +33,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "nvfp4_mtp_decode"
+# DRAM bytes (read + write) of one moe_layer_kernel launch on this workload,
+# from one ncu capture of the current kernel; None whenever the kernel changes
+# and has not been captured again.
+LAYER_TRAFFIC_BYTES = 55_235_072
+LAYER_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
+                        "(55.02 MB + 0.21 MB), bench.py --layers 3")
 LAYERS = 40
 METRIC = "us per MoE layer (NVFP4 MTP decode, T=4 E=256 top-8 H=2048 I=512)"
 UNIT = "us/layer"
@@ -292,7 +298,9 @@ def run_gpu(args):
     layer_bytes = [a * (fc1_b + fc2_b) + 2 * wl.T * wl.H * 2 for a in act]
     layer_alg = sum(layer_bytes) / len(layer_bytes)
     peak, peak_src = _peaks()
-    layer_gbs = layer_alg / (kern_us["layer"] * 1e-6) / 1e9
+    # achieved: the kernel's average duration over the timed region, where it
+    # is the only kernel (one launch per layer, after a 12-byte memset node)
+    layer_gbs = layer_alg / (us_layer * 1e-6) / 1e9
 
     # --- end to end: host buffers, H2D of each layer's inputs, D2H of each output
     hx = [L["x"].cpu().pin_memory() for L in layers]
@@ -346,9 +354,10 @@ def run_gpu(args):
                               "peak_gbs": peak, "peak_source": peak_src},
             "eager_us_per_layer": round(eager_us, 3),
             "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},
-            "roofline": {"kernel": "moe_layer_kernel (FC1 + SwiGLU + FC2 + un-permute, E2M1 decode)",
+            "roofline": {"kernel": "moe_layer_kernel (routing + FC1 + SwiGLU + FC2 + un-permute, E2M1 decode)",
                          "bound": "hbm", "achieved": round(layer_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(layer_gbs / peak, 4), "traffic": None,
+                         "frac": round(layer_gbs / peak, 4), "traffic": LAYER_TRAFFIC_BYTES,
+                         "traffic_source": LAYER_TRAFFIC_SOURCE,
                          "alg_bytes_per_launch": int(layer_alg), "peak_source": peak_src},
             "gpu_launches": args.steps * LAYERS,
             "e2e": {"value": round(e2e_agg["us_per_layer"], 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
