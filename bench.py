@@ -483,7 +483,8 @@ def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
             "tensor_frac": round(tflops / tc_peak, 4),
             "bf16_weight_bytes": int(wbytes), "weight_gbs": round(wbytes / (gemm * 1e-6) / 1e9, 1),
             "hbm_frac": round(wbytes / (gemm * 1e-6) / 1e9 / hbm_peak, 4),
-            "kernels": "route, dequant x2 (full call only), grouped_gemm_kernel x2 (mma.sync bf16), unpermute"}
+            "kernels": "route, dequant x2 (full call only), grouped_gemm_tc_kernel x2 (tcgen05.mma bf16, "
+                       "TMEM accumulator), unpermute"}
 
 
 # ---------------------------------------------------------------- CPU (oracle)

@@ -5,29 +5,18 @@
 // kernel forms the weighted sum over each token's experts (§1 pipeline:
 // GEMM1 -> activation -> GEMM2 -> un-permute -> weighted sum).
 //
-// Grouped GEMM (bf16 operands, fp32 accumulation, mma.sync m16n8k16):
-//  * the rows of every expert are contiguous in expert order (the permute
-//    maps); a CTA computes a 128-row x 128-column tile of one expert, the
-//    tiles of all experts numbered expert by expert (each CTA finds its own
-//    from the expert offsets with a warp prefix sum);
-//  * GEMM1's left operand is gathered on the fly: permuted row p reads token
-//    perm_to_expanded[p] / k of x (no expanded copy of the activations);
-//  * operands are staged by cp.async (16 bytes per thread, zero-filled past
-//    the expert's last row) into a 3-stage ring of 128 x 32 bf16 tiles whose
-//    16-byte chunks are XOR-swizzled so that ldmatrix reads are free of bank
-//    conflicts;
-//  * 8 warps, each a 32 x 64 sub-tile (2 x 8 m16n8 accumulators);
-//  * GEMM1's epilogue applies SwiGLU to the adjacent (gate, linear) columns
-//    that an accumulator fragment holds and writes a = bf16(SwiGLU) [R, I];
-//    GEMM2's writes y (fp32) [R, H].
+// Grouped GEMM: bf16 operands, fp32 accumulation on the 5th-generation tensor
+// cores (tcgen05.mma, accumulator in tensor memory); the rows of every expert
+// are contiguous in expert order (the permute maps) and a CTA computes a
+// 128-row x 128-column tile of one expert, the tiles of all experts numbered
+// expert by expert.  GEMM1's left operand is gathered on the fly (permuted
+// row p reads token perm_to_expanded[p] / k of x: no expanded copy of the
+// activations) and its epilogue applies SwiGLU to the adjacent (gate,
+// linear) columns of a row, writing a = bf16(SwiGLU) [R, I]; GEMM2 writes
+// y (fp32) [R, H].
 #include "qmoe_common.cuh"
 
 namespace qmoe {
-
-constexpr int kBM = 128, kBN = 128, kBK = 32, kStages = 3, kGemmThreads = 256;
-constexpr int kTileA = kBM * kBK;  // bf16 elements of one stage's left tile
-constexpr int kTileB = kBN * kBK;
-constexpr int kGemmSmem = kStages * (kTileA + kTileB) * 2;
 
 struct GroupedGemm {
   const uint16_t *A;       // bf16 left-operand rows
@@ -54,32 +43,71 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// Element offset of 16-byte chunk c of row r in a swizzled [rows][kBK] tile.
-__device__ __forceinline__ int swz(int r, int c) { return r * kBK + ((c ^ ((r >> 1) & 3)) << 3); }
+// ---- tcgen05 grouped GEMM ------------------------------------------------------
+//
+// The same grouped GEMM on the 5th-generation tensor cores: a CTA of 4 warps
+// computes a 128 x 128 tile with tcgen05.mma (kind::f16, bf16 operands, fp32
+// accumulator in tensor memory, M = 128, N = 128, K = 16 per instruction).
+//  * operands: 3-stage ring of 128 x 64 bf16 tiles per operand, K-major with
+//    the 128-byte swizzle (16-byte chunk c of row r at r * 128 + ((c ^ (r & 7))
+//    * 16), 8-row groups 1 KB apart); filled by cp.async from every thread (the
+//    left operand's rows gathered), made visible to the tensor core with
+//    fence.proxy.async before the barrier that precedes the MMA issue;
+//  * one thread issues the 4 MMAs of a stage and tcgen05.commit's an mbarrier,
+//    which releases the stage for its next fill;
+//  * epilogue: each warp reads its 32 accumulator rows (tensor-memory lanes
+//    32w..32w+31) 32 columns at a time with tcgen05.ld, applies SwiGLU (first
+//    GEMM) and stores;
+//  * every wait is bounded; the tensor memory is always released.
+constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 3, kTcThreads = 128;
+constexpr int kTcTileBytes = kTcBM * kTcBK * 2;                      // 16 KB per operand tile
+constexpr int kTcSmem = kTcStages * 2 * kTcTileBytes + 1024;         // + room to align to 1 KB
+constexpr uint32_t kTcWaitLimit = 1u << 22;
+// instruction descriptor: fp32 accumulator (bits 4-5 = 1), bf16 A (bits 7-9 = 1)
+// and B (bits 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTcBN >> 3) << 17) |
+                              ((uint32_t)(kTcBM >> 4) << 24);
+static_assert(kTcBM == 128 && kTcBN % 16 == 0 && kTcBN <= 256, "tcgen05.mma M = 128 shape");
 
-__global__ void __launch_bounds__(kGemmThreads) grouped_gemm_kernel(const __grid_constant__ GroupedGemm p) {
-  extern __shared__ __align__(128) uint16_t gsm[];
-  __shared__ int s_e, s_row0, s_rows;
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile: start
+// address >> 4 (bits 0-13), leading byte offset 16 (unused with this swizzle),
+// stride byte offset 1024 between 8-row groups (bits 32-45), descriptor
+// version 1 (bits 46-47), swizzle mode 128 B (value 2, bits 61-63).
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ uint32_t tc_sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void tc_mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool tc_mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kTcWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(kTcThreads) grouped_gemm_tc_kernel(const __grid_constant__ GroupedGemm p,
+                                                                    int32_t *err_flag) {
+  extern __shared__ __align__(1024) unsigned char tsm[];
+  __shared__ uint64_t mma_done[kTcStages];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int s_e, s_row0, s_rows, s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // this CTA's (expert, row tile): tiles of expert e are [pre_e, pre_e + ceil(rows_e / kBM))
-  if (warp == 0) {
+  if (warp == 0) {  // this CTA's (expert, row tile), as in the mma.sync kernel
     const int per = (p.E + 31) / 32;
     int sum = 0;
     for (int q = 0; q < per; ++q) {
       const int e = lane * per + q;
-      if (e < p.E) sum += (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e) + kBM - 1) / kBM;
+      if (e < p.E) sum += (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e) + kTcBM - 1) / kTcBM;
     }
     int incl = sum;
 #pragma unroll
@@ -94,123 +122,168 @@ __global__ void __launch_bounds__(kGemmThreads) grouped_gemm_kernel(const __grid
       const int e = lane * per + q;
       if (e < p.E) {
         const int o0 = __ldg(p.offsets + e), o1 = __ldg(p.offsets + e + 1);
-        const int c = (o1 - o0 + kBM - 1) / kBM;
+        const int c = (o1 - o0 + kTcBM - 1) / kTcBM;
         if (bx >= run && bx < run + c) {
           s_e = e;
-          s_row0 = o0 + (bx - run) * kBM;
-          s_rows = min(kBM, o1 - s_row0);
+          s_row0 = o0 + (bx - run) * kTcBM;
+          s_rows = min(kTcBM, o1 - s_row0);
         }
         run += c;
       }
     }
     __syncwarp();
-    if (lane == 0 && bx >= total) s_e = -1;  // more CTAs than tiles
+    if (lane == 0) {
+      if (bx >= total) s_e = -1;
+      s_abort = 0;
+    }
   }
   __syncthreads();
   const int e = s_e;
-  if (e < 0) return;
+  if (e < 0) return;  // CTA-uniform, before any tensor memory is held
   const int row0 = s_row0, rows = s_rows;
-  const int n0 = (int)blockIdx.y * kBN;
-  const int KT = p.K / kBK;
+  const int n0 = (int)blockIdx.y * kTcBN;
+  const int KT = p.K / kTcBK;
+  unsigned char *base = tsm + ((1024u - (smem_u32(tsm) & 1023u)) & 1023u);
 
-  auto load_stage = [&](int st, int k0) {
-    uint16_t *As = gsm + st * (kTileA + kTileB);
-    uint16_t *Bs = As + kTileA;
-    for (int i = tid; i < kBM * 4; i += kGemmThreads) {
-      const int r = i >> 2, c = i & 3;
-      const uint16_t *src = p.A;
-      uint32_t bytes = 0;
-      if (r < rows) {
-        const int g = row0 + r;
-        const int arow = p.perm ? __ldg(p.perm + g) / p.ktop : g;
-        src = p.A + (size_t)arow * p.lda + k0 + c * 8;
-        bytes = 16;
-      }
-      cp_async16_zfill(smem_u32(As + swz(r, c)), src, bytes);
+  if (warp == 0) {  // 128 fp32 columns of tensor memory: the 128 x 128 accumulator
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
+                 "r"(128u)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 32) {
+    for (int i = 0; i < kTcStages; ++i) tc_mbar_init(&mma_done[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_base_s;
+
+  // The rows a thread copies are the same at every k step (row (tid >> 3) +
+  // 16 q, chunk tid & 7): their sources (the gathered token rows included)
+  // are found once, so no k step waits on an index load.
+  constexpr int kQ = (kTcBM * 8) / kTcThreads;
+  static_assert(kTcBM == kTcBN, "one row set for both operands");
+  const int cth = tid & 7, rth = tid >> 3;
+  const uint16_t *a_src[kQ];
+  const uint16_t *b_src[kQ];
+  uint32_t a_ok = 0, b_ok = 0;
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    const int r = rth + 16 * q;
+    a_src[q] = p.A;
+    b_src[q] = p.B;
+    if (r < rows) {
+      const int g = row0 + r;
+      const int arow = p.perm ? __ldg(p.perm + g) / p.ktop : g;
+      a_src[q] = p.A + (size_t)arow * p.lda + cth * 8;
+      a_ok |= 1u << q;
     }
-    for (int i = tid; i < kBN * 4; i += kGemmThreads) {
-      const int r = i >> 2, c = i & 3;
-      const uint16_t *src = p.B;
-      uint32_t bytes = 0;
-      if (n0 + r < p.N) {
-        src = p.B + ((size_t)e * p.N + n0 + r) * p.K + k0 + c * 8;
-        bytes = 16;
-      }
-      cp_async16_zfill(smem_u32(Bs + swz(r, c)), src, bytes);
+    if (n0 + r < p.N) {
+      b_src[q] = p.B + ((size_t)e * p.N + n0 + r) * p.K + cth * 8;
+      b_ok |= 1u << q;
+    }
+  }
+  auto load_stage = [&](int st, int k0) {
+    unsigned char *As = base + (size_t)st * 2 * kTcTileBytes;
+    unsigned char *Bs = As + kTcTileBytes;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int r = rth + 16 * q;
+      const bool ao = (a_ok >> q) & 1u, bo = (b_ok >> q) & 1u;
+      cp_async16_zfill(smem_u32(As + tc_sw128(r, cth)), ao ? a_src[q] + k0 : p.A, ao ? 16u : 0u);
+      cp_async16_zfill(smem_u32(Bs + tc_sw128(r, cth)), bo ? b_src[q] + k0 : p.B, bo ? 16u : 0u);
     }
   };
 
-  float acc[2][8][4];
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 8; ++ni)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[mi][ni][q] = 0.f;
-
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < KT) load_stage(s, s * kBK);
+  for (int s = 0; s < kTcStages - 1; ++s) {
+    if (s < KT) load_stage(s, s * kTcBK);
     cp_async_commit();
   }
-  const int wm = warp & 3, wn = warp >> 2;  // 4 x 2 warps of 32 x 64
   for (int kt = 0; kt < KT; ++kt) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();  // stage kt landed for every thread; stage kt - 1 is no longer read
-    {
-      const int nk = kt + kStages - 1;
-      if (nk < KT) load_stage(nk % kStages, nk * kBK);
-      cp_async_commit();
-    }
-    const uint16_t *As = gsm + (kt % kStages) * (kTileA + kTileB);
-    const uint16_t *Bs = As + kTileA;
+    cp_async_wait<kTcStages - 2>();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile is read by the tensor core
+    __syncthreads();
+    if (tid == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int st = kt % kTcStages;
+      const uint32_t a_addr = smem_u32(base + (size_t)st * 2 * kTcTileBytes), b_addr = a_addr + kTcTileBytes;
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      uint32_t a[2][4], b[8][2];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const int r = wm * 32 + mi * 16 + (lane & 15);
-        ldmatrix_x4(smem_u32(As + swz(r, ks * 2 + (lane >> 4))), a[mi]);
+      for (int kk = 0; kk < kTcBK / 16; ++kk) {
+        const uint64_t da = tc_desc_sw128(a_addr + kk * 32), db = tc_desc_sw128(b_addr + kk * 32);
+        const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+            "l"(da), "l"(db), "r"(kTcIdesc), "r"(acc)
+            : "memory");
       }
-#pragma unroll
-      for (int nj = 0; nj < 4; ++nj) {
-        const int r = wn * 64 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
-        uint32_t t4[4];
-        ldmatrix_x4(smem_u32(Bs + swz(r, ks * 2 + ((lane >> 3) & 1))), t4);
-        b[2 * nj][0] = t4[0];
-        b[2 * nj][1] = t4[1];
-        b[2 * nj + 1][0] = t4[2];
-        b[2 * nj + 1][1] = t4[3];
-      }
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 8; ++ni) mma_bf16(acc[mi][ni], a[mi], b[ni][0], b[ni][1]);
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(&mma_done[st]))
+                   : "memory");
     }
+    const int nk = kt + kTcStages - 1;
+    if (nk < KT) {
+      const int ns = nk % kTcStages;
+      // stage ns was read by the MMAs of k step kt - 1: wait for them
+      if (kt >= 1 && !s_abort && !tc_mbar_wait(&mma_done[ns], (uint32_t)((kt - 1) / kTcStages) & 1u)) {
+        s_abort = 1;
+        atomicExch(err_flag, 1);
+      }
+      load_stage(ns, nk * kTcBK);
+    }
+    cp_async_commit();
   }
   cp_async_wait<0>();
+  if (!s_abort && !tc_mbar_wait(&mma_done[(KT - 1) % kTcStages], (uint32_t)((KT - 1) / kTcStages) & 1u)) {
+    s_abort = 1;
+    atomicExch(err_flag, 1);
+  }
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-  // epilogue: fragment (mi, ni) holds rows r, r + 8 and the column pair (c, c + 1)
+  // epilogue: warp w holds accumulator rows 32w + lane
+  const int r = warp * 32 + lane;
+#pragma unroll 1
+  for (int cc = 0; cc < kTcBN / 32; ++cc) {
+    uint32_t v[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cc * 32)));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    const int c0 = n0 + cc * 32;
+    if (r >= rows || c0 >= p.N) continue;  // N is a multiple of 64: a 32-column chunk is all in or all out
+    const size_t prow = (size_t)(row0 + r);
+    if (p.swiglu) {
+      uint32_t o[8];
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi) {
-#pragma unroll
-    for (int ni = 0; ni < 8; ++ni) {
-      const int c = n0 + wn * 64 + ni * 8 + 2 * (lane & 3);
-      if (c >= p.N) continue;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = wm * 32 + mi * 16 + (lane >> 2) + 8 * h;
-        if (r >= rows) continue;
-        const float v0 = acc[mi][ni][2 * h], v1 = acc[mi][ni][2 * h + 1];
-        const size_t prow = (size_t)(row0 + r);
-        if (p.swiglu) {
-          p.out_a[prow * (p.N / 2) + c / 2] = (uint16_t)f32_to_bf16_rne(swiglu(v0, v1, p.alpha, p.beta, p.limit));
-        } else {
-          *reinterpret_cast<float2 *>(p.out_y + prow * p.N + c) = make_float2(v0, v1);
-        }
+      for (int m = 0; m < 16; m += 2) {
+        const float a0 = swiglu(__uint_as_float(v[2 * m]), __uint_as_float(v[2 * m + 1]), p.alpha, p.beta, p.limit);
+        const float a1 =
+            swiglu(__uint_as_float(v[2 * m + 2]), __uint_as_float(v[2 * m + 3]), p.alpha, p.beta, p.limit);
+        o[m / 2] = f32_to_bf16_rne(a0) | (f32_to_bf16_rne(a1) << 16);
       }
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out_a + prow * (p.N / 2) + c0 / 2);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      float4 *dst = reinterpret_cast<float4 *>(p.out_y + prow * p.N + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                             __uint_as_float(v[4 * q + 3]));
     }
   }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128u) : "memory");
 }
 
 // out[t][h] = bf16(sum_j w[t][j] * y[expanded_to_perm[t * k + j]][h]), j in order.
@@ -234,28 +307,37 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const float *__restrict_
   }
 }
 
+__device__ int32_t g_prefill_error;  // set by a tcgen05 GEMM CTA whose wait gave up
+
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   static bool smem_set = false;
+  static int32_t *err_flag = nullptr;
   if (!smem_set) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (err != cudaSuccess) return err;
+    void *ptr = nullptr;
+    err = cudaGetSymbolAddress(&ptr, g_prefill_error);
+    if (err != cudaSuccess) return err;
+    err_flag = static_cast<int32_t *>(ptr);
     smem_set = true;
   }
   const int R = a.T * a.k;
   const int na_max = a.E < R ? a.E : R;
-  const unsigned mtiles = (unsigned)((R + kBM - 1) / kBM + na_max);  // >= the sum over experts of ceil(rows / kBM)
+  const unsigned mtiles = (unsigned)((R + kTcBM - 1) / kTcBM + na_max);  // >= the sum over experts of ceil(rows / kTcBM)
   GroupedGemm g1{};
   g1.A = a.x; g1.perm = a.p2e; g1.ktop = a.k; g1.lda = a.H;
   g1.B = a.w1d; g1.offsets = a.offsets; g1.E = a.E; g1.N = 2 * a.I; g1.K = a.H;
   g1.swiglu = 1; g1.out_a = a.act; g1.alpha = a.alpha; g1.beta = a.beta; g1.limit = a.limit;
-  grouped_gemm_kernel<<<dim3(mtiles, (unsigned)((g1.N + kBN - 1) / kBN)), kGemmThreads, kGemmSmem, stream>>>(g1);
+  grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g1.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
+      g1, err_flag);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   GroupedGemm g2{};
   g2.A = a.act; g2.perm = nullptr; g2.ktop = 1; g2.lda = a.I;
   g2.B = a.w2d; g2.offsets = a.offsets; g2.E = a.E; g2.N = a.H; g2.K = a.I;
   g2.swiglu = 0; g2.out_y = a.y;
-  grouped_gemm_kernel<<<dim3(mtiles, (unsigned)((g2.N + kBN - 1) / kBN)), kGemmThreads, kGemmSmem, stream>>>(g2);
+  grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g2.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
+      g2, err_flag);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const long long work = (long long)a.T * (a.H / 2);
