@@ -220,17 +220,16 @@ __device__ __forceinline__ void store_tile4x4(uint32_t v0, uint32_t v1, uint32_t
 // ---- work geometry ------------------------------------------------------------------
 
 // Work split: the units of FC f, in (expert slot, column tile, k) order, are
-// cut into gridDim.x ranges of about equal cost, cost(unit) = 1 + 4 * rows for
-// an expert with `rows` rows (each row is one pass over the unit, decoded on
-// its own; the constant stands for the unit's copy and bookkeeping); CTA c
-// gets units [bnd[f][c], bnd[f][c + 1]).
-__host__ __device__ __forceinline__ int unit_cost(int rows) { return 1 + 4 * rows; }
+// cut into gridDim.x ranges of about equal cost, cost(unit) = 4 * rows for an
+// expert with `rows` rows (each row is one pass over the unit, decoded on its
+// own); CTA c gets units [bnd[f][c], bnd[f][c + 1]).
+__host__ __device__ __forceinline__ int unit_cost(int rows) { return 4 * rows; }
 // A pass start (one per row of each (expert slot, tile) pair: partial-sum
-// write of the previous pass, activation staging, first copy) costs about two
-// units; it is charged at the pair's start.
-constexpr int kPassCost = 8;
+// write of the previous pass, activation staging, first copy) costs
+// P.pass_cost in the same units (fitted to per-CTA timings: about 3 units of
+// decode in FC1, 1.5 in FC2); it is charged at the pair's start.
 __host__ __device__ __forceinline__ int pair_cost(const FcPlan &P, int rows) {
-  return rows * kPassCost + P.ku * unit_cost(rows);
+  return rows * P.pass_cost + P.ku * unit_cost(rows);
 }
 
 struct FcWork {
@@ -437,7 +436,7 @@ __device__ void split_bound(Shared &S, const FcPlan &P, int f, int c) {
   if (q >= P.ct) {
     u = P.ct * P.ku;
   } else {
-    const long long v = rem - (long long)q * pc - (long long)r * kPassCost;
+    const long long v = rem - (long long)q * pc - (long long)r * P.pass_cost;
     u = q * P.ku + (v <= 0 ? 0 : (int)min((long long)P.ku, (v + cu - 1) / cu));
   }
   S.bnd[f][c] = lo * P.ct * P.ku + u;
@@ -1222,6 +1221,10 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
     set_error("no column tiling of N = %d / %d fits the decode kernel", 2 * I, H);
     return QMOE_ERR_UNSUPPORTED;
   }
+  // pass-start charges of the split, in units of a quarter of a unit-pass
+  // (FC1's pass change also waits for its activation rows from memory)
+  L.f[0].pass_cost = 12;
+  L.f[1].pass_cost = 6;
   const size_t G = (size_t)num_sms();
   if (G > (size_t)kMaxCtas) {
     set_error("the decode kernel supports at most %d SMs (this GPU has %zu)", kMaxCtas, G);
@@ -1237,9 +1240,9 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
     // segments of one CTA: at most the pairs that exist, and at most two more
     // (the first and the last) than the pairs lying wholly inside its cost
     // range [c * total / G, (c + 1) * total / G], each of which costs at
-    // least kPassCost + 5 ku.  The total is ct * sum over slots of
-    // (rows * kPassCost + ku * (1 + 4 rows)) <= ct * (kPassCost + 5 ku) R.
-    const size_t pc_min = kPassCost + 5 * (size_t)P.ku;
+    // least pass_cost + 4 ku.  The total is ct * sum over slots of
+    // rows * (pass_cost + 4 ku) <= ct * (pass_cost + 4 ku) R.
+    const size_t pc_min = (size_t)P.pass_cost + 4 * (size_t)P.ku;
     const size_t total = (size_t)P.ct * pc_min * R;
     const size_t segs = std::min<size_t>(na_max * (size_t)P.ct, 2 + (total / G + 1) / pc_min);
     if (segs > (size_t)kMaxSegs) {

@@ -141,6 +141,7 @@ struct FcPlan {
   int kn;       // 1: block scales are k-major [E, nblocks, N]; a unit's scale rows ride in its ring slot
   int bpu;      // scale block rows one unit touches (k-major)
   int sc_off;   // offset of those rows in a ring slot
+  int pass_cost;  // split charge of one pass start (see pair_cost)
 };
 struct LayerPlan {
   FcPlan f[2];
