@@ -5,9 +5,10 @@ fraction of the measured HBM bandwidth) on the NVFP4 MTP decode workload:
 T=4 token rows, E=256 experts, top-8, hidden 2048, intermediate 512, SwiGLU.
 
 A step is one decode step of a 40-layer model: 40 calls of
-qmoe_fp4_moe_forward (a 12-byte counter memset, then one kernel for routing -> FC1 GEMV +
-SwiGLU -> FC2 GEMV -> weighted un-permute), each on its own layer's weights (17 GB in total, far
-larger than the 129 MB L2), replayed as one CUDA graph.  Inputs are seeded
+qmoe_fp4_moe_forward (one kernel each for routing -> FC1 GEMV + SwiGLU -> FC2 GEMV ->
+weighted un-permute, on a primed workspace: no per-call counter reset, each kernel launched
+with programmatic dependent launch behind the previous one), each on its own layer's weights
+(17 GB in total, far larger than the 129 MB L2), replayed as one CUDA graph.  Inputs are seeded
 synthetic data with the workload's shapes and distributions.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -36,9 +37,9 @@ WORKLOAD = "nvfp4_mtp_decode"
 # DRAM bytes (read + write) of one moe_layer_kernel launch on this workload,
 # from one ncu capture of the current kernel; None whenever the kernel changes
 # and has not been captured again.
-LAYER_TRAFFIC_BYTES = 55_304_192
+LAYER_TRAFFIC_BYTES = 55_330_304
 LAYER_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
-                        "(55.026 MB + 0.278 MB), bench.py --layers 3")
+                        "(55.021 MB + 0.310 MB), bench.py --layers 3")
 LAYERS = 40
 METRIC = "us per MoE layer (NVFP4 MTP decode, T=4 E=256 top-8 H=2048 I=512)"
 UNIT = "us/layer"
@@ -214,8 +215,10 @@ def run_gpu(args):
             L["s2"] = q.scales_kmajor(L["s2"], wl.fmt)
         fmt = wl.fmt | q.SCALES_KMAJOR
         torch.cuda.synchronize()
+    if not args.no_primed:
+        fmt |= q.WORKSPACE_PRIMED  # the header is zeroed here, once; the kernels keep it zero
     ws_bytes = q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, fmt)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
     ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=device) for _ in layers]
     stream = torch.cuda.Stream(device=device)
@@ -287,7 +290,7 @@ def run_gpu(args):
                           fmt, wl.k, wl.normalize, out=outs[j % LAYERS], workspace=ws)
         q.set_stage_events(None)
     torch.cuda.synchronize()
-    names = ["layer"]  # one kernel per call (routing inside), after a 12-byte counter memset
+    names = ["layer"]  # one kernel per call (routing inside); without --no-primed no memset before it
     dur = {n: [] for n in names}
     for j in range(len(evs)):
         e = evs[j]
@@ -299,7 +302,7 @@ def run_gpu(args):
     layer_alg = sum(layer_bytes) / len(layer_bytes)
     peak, peak_src = _peaks()
     # achieved: the kernel's average duration over the timed region, where it
-    # is the only kernel (one launch per layer, after a 12-byte memset node)
+    # is the only kernel (one launch per layer)
     layer_gbs = layer_alg / (us_layer * 1e-6) / 1e9
 
     # --- end to end: host buffers, H2D of each layer's inputs, D2H of each output
@@ -347,7 +350,9 @@ def run_gpu(args):
                        "l2": "inputs larger than L2: 40 distinct layers, 17.3 GB of weights per step",
                        "graph": True, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "scale_layout": ("k-major [E, K/16, N], converted once at weight load"
-                                        if args.scales == "kmajor" else "[E, N, K/16] as stored")},
+                                        if args.scales == "kmajor" else "[E, N, K/16] as stored"),
+                       "workspace": ("primed: zeroed once, no per-call reset, programmatic dependent launch"
+                                     if not args.no_primed else "header reset by a memset before every call")},
             "weight_stream": {"alg_bytes_per_layer": int(mean_alg),
                               "mean_active_experts": statistics.mean(act),
                               "gbs": round(stream_gbs, 1), "frac_of_hbm": round(stream_gbs / (peak * world), 4),
@@ -557,6 +562,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="distinct layers per step (default 40; fewer only for small profiler runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-primed", action="store_true",
+                    help="reset the workspace header before every call (no programmatic dependent launch)")
     ap.add_argument("--no-dequant", action="store_true", help="skip the prefill dequant measurement")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill forward measurement")
     ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],

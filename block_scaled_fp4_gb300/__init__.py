@@ -18,6 +18,11 @@ from .build import LIB, build
 NVFP4 = 0
 MXFP4 = 1
 SCALES_KMAJOR = 0x100  # OR'd into fmt of the forward calls: block scales are [E, K/bs, N]
+# OR'd into fmt of moe_forward: the workspace's first WORKSPACE_HEADER_BYTES
+# bytes are zero (zeroed once by the caller; the library keeps them zero), so
+# decode calls skip their header reset and chain by programmatic dependent launch
+WORKSPACE_PRIMED = 0x200
+WORKSPACE_HEADER_BYTES = 64
 BLOCK = {NVFP4: 16, MXFP4: 32}
 GEMV_MAX_ROWS = 64
 

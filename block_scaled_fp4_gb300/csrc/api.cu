@@ -163,6 +163,8 @@ static DecodeLayout decode_layout(void *ws, int T, int E, int k, size_t p1_float
   const size_t S = (size_t)(E < (int)R ? E : (int)R);
   Carve c(ws);
   DecodeLayout L{};
+  // [0] unused, [1] device error flag, [2], [3] grid barriers, [4] CTAs out
+  L.meta = c.take<int32_t>(QMOE_WORKSPACE_HEADER_BYTES / sizeof(int32_t));
   L.ids = c.take<int32_t>(R);
   L.weights = c.take<float>(R);
   L.offsets = c.take<int32_t>((size_t)E + 1);
@@ -170,7 +172,6 @@ static DecodeLayout decode_layout(void *ws, int T, int E, int k, size_t p1_float
   L.e2p = c.take<int32_t>(R);
   L.active = c.take<int32_t>(S);
   L.slots = c.take<SlotDesc>(S);
-  L.meta = c.take<int32_t>(4);  // [0] active experts, [1] device error flag, [2], [3] grid barriers
   L.p1 = c.take<float>(p1_floats);
   L.p2 = c.take<float>(p2_floats);
   L.bytes = (c.off + 255) & ~(size_t)255;
@@ -197,6 +198,7 @@ static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k,
   const size_t R = (size_t)T * k;
   Carve c(ws);
   PrefillLayout L{};
+  c.take<uint8_t>(QMOE_WORKSPACE_HEADER_BYTES);  // the decode kernel's header: never written here
   L.ids = c.take<int32_t>(R);
   L.weights = c.take<float>(R);
   L.offsets = c.take<int32_t>((size_t)E + 1);
@@ -294,7 +296,8 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   if (st != QMOE_OK) return st;
   QMOE_REQUIRE(workspace_bytes, QMOE_ERR_INVALID_ARG, "workspace_bytes is NULL");
   const bool kmajor = (fmt & QMOE_SCALES_KMAJOR) != 0;
-  const int base_fmt = (int)fmt & ~(int)QMOE_SCALES_KMAJOR;
+  const bool primed = (fmt & QMOE_WORKSPACE_PRIMED) != 0;
+  const int base_fmt = (int)fmt & ~(int)(QMOE_SCALES_KMAJOR | QMOE_WORKSPACE_PRIMED);
   QMOE_REQUIRE(base_fmt == QMOE_NVFP4 || base_fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
   QMOE_REQUIRE(H >= 64 && I >= 64, QMOE_ERR_INVALID_ARG, "H and I must be >= 64 (got %d, %d)", H, I);
   QMOE_REQUIRE(H % 64 == 0 && I % 64 == 0, QMOE_ERR_UNSUPPORTED, "H and I must be multiples of 64 (got %d, %d)", H,
@@ -342,10 +345,14 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   g.p1 = L.p1; g.p2 = L.p2; g.out = out;
 
   stage_event(0, stream);
-  // the error flag and the two grid-barrier counters start every call at 0
-  cudaError_t err = cudaMemsetAsync(L.meta + 1, 0, 3 * sizeof(int32_t), stream);
-  if (err != cudaSuccess) return cuda_status(err, "counter reset");
-  err = launch_layer(g, plan, E, stream);
+  // the error flag and the grid-barrier counters start every call at 0: reset
+  // here, or (primed workspace) left at 0 by the previous decode kernel
+  cudaError_t err = cudaSuccess;
+  if (!primed) {
+    err = cudaMemsetAsync(L.meta, 0, QMOE_WORKSPACE_HEADER_BYTES, stream);
+    if (err != cudaSuccess) return cuda_status(err, "counter reset");
+  }
+  err = launch_layer(g, plan, E, primed, stream);
   if (err == cudaErrorCooperativeLaunchTooLarge && g_err[0]) return QMOE_ERR_CUDA;  // message already set
   if (err != cudaSuccess) return cuda_status(err, "layer launch");
   stage_event(1, stream);

@@ -41,8 +41,10 @@
 //    sum of FC2 partials of (t, j)).  All sums run in a fixed order, so the
 //    result is deterministic;
 //  * the kernel is launched cooperatively (all CTAs resident, so the grid
-//    barriers cannot deadlock); the barrier counters and the error flag are
-//    cleared by a 12-byte memset issued just before it;
+//    barriers cannot deadlock).  Its barrier counters live in the workspace
+//    header; the last CTA out returns them to zero, so a call on a workspace
+//    whose header is known to be zero needs no reset and is launched with
+//    programmatic dependent launch right behind the previous kernel;
 //  * every wait is bounded: a wait that gives up sets the device error flag
 //    meta[1] and the CTA carries on without waiting again, so no CTA hangs.
 #include <cuda.h>
@@ -275,14 +277,11 @@ struct Shared {
   int row2slot[kMaxSlots];
   int row_tok[kMaxSlots];              // token of each permuted row
   // routing (computed by every CTA for itself): expert and weight of each
-  // expanded row t * k + j, the permute maps, per-expert counts and offsets
+  // expanded row t * k + j and the permute maps
   int r_ids[kMaxSlots];
   float r_w[kMaxSlots];
   int r_e2p[kMaxSlots];
   int r_p2e[kMaxSlots];
-  int r_off[kMaxExperts + 1];
-  int r_cnt[kMaxExperts];
-  int r_off2[kMaxExperts];
   uint32_t wmax[kConsWarps];
   int na;
   int abort;
@@ -332,34 +331,48 @@ __device__ void grid_barrier(Shared &S, const LayerArgs &g, int32_t *ctr) {
   cons_sync();
 }
 
+// Called by each CTA's barrier thread after its last poll of a barrier
+// counter (those polls are acquire loads, so they stay before it): the last
+// CTA to count itself out returns both barrier counters and this counter to
+// zero, so the next call on the workspace starts from zero without a reset.
+__device__ void leave_counters(const LayerArgs &g) {
+  if (atomicAdd(g.meta + 4, 1) == (int)gridDim.x - 1) {
+    atomicExch(g.meta + 2, 0);
+    atomicExch(g.meta + 3, 0);
+    atomicExch(g.meta + 4, 0);
+  }
+}
+
 // ---- set-up ----------------------------------------------------------------------------
 
-// This CTA's segments of FC f (one thread).
+// This CTA's segments of FC f (one warp, one lane per segment): the pairs
+// its unit range [lo, hi) touches, each cut to that range.
 template <int FMT>
 __device__ void build_segments(Shared &S, const LayerArgs &g, const FcPlan &P, int f) {
+  const int lane = (int)lane_id();
   const FcWork W = fc_work(S, f);
-  int n = 0;
-  for (int u = W.lo; u < W.hi;) {
-    if (n == kMaxSegs) {  // the host bounds this; report rather than drop work
+  const int p0 = W.lo / P.ku, n = W.lo < W.hi ? (W.hi - 1) / P.ku - p0 + 1 : 0;
+  if (n > kMaxSegs) {  // the host bounds this; report rather than drop work
+    if (lane == 0) {
       *(volatile int *)&S.abort = 1;
       atomicExch(g.meta + 1, 1);
-      break;
     }
-    const int pair = u / P.ku;
-    const int end = min(W.hi, (pair + 1) * P.ku);
+  }
+  const int nseg = min(n, kMaxSegs);
+  if (lane < nseg) {
+    const int pair = p0 + lane;
     Seg sg;
     sg.pair = pair;
     sg.a = pair / P.ct;
     sg.t = pair - sg.a * P.ct;
-    sg.j0 = u - pair * P.ku;
-    sg.j1 = end - pair * P.ku;
+    sg.j0 = max(W.lo, pair * P.ku) - pair * P.ku;
+    sg.j1 = min(W.hi, (pair + 1) * P.ku) - pair * P.ku;
     sg.wid0 = unit_window<FMT>(P, sg.j0);
     sg.wid1 = unit_window<FMT>(P, sg.j1 - 1);
     sg.dst = 0;
-    S.seg[f][n++] = sg;
-    u = end;
+    S.seg[f][lane] = sg;
   }
-  S.nseg[f] = n;
+  if (lane == 0) S.nseg[f] = nseg;
 }
 
 // Cost prefix over the expert slots and the split boundaries of FC f.
@@ -1062,6 +1075,7 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const Layer
     }
   }
   grid_barrier(S, g, g.meta + 3);  // every FC2 partial is written
+  if (threadIdx.x == 0) leave_counters(g);
   finalize(S, g, L);
 }
 
@@ -1071,6 +1085,13 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Shared S;
   const int tid = threadIdx.x, warp = tid >> 5;
+  // Launched with programmatic dependent launch, the kernel may start while
+  // the previous kernel of the stream still runs: nothing in global memory
+  // (inputs, workspace) is touched before that kernel's results are visible.
+  // The next kernel may then be scheduled at once: it cannot become resident
+  // on an SM before this kernel's CTA there has exited.
+  pdl_wait();
+  pdl_launch_dependents();
   if (tid == 0) {
     for (int i = 0; i < kRingMax; ++i) {
       mbar_init(&S.full[i], 1);
@@ -1091,10 +1112,11 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
     S.abort = 0;
     S.fc2_pre = 0;
   }
-  // Routing, in every CTA with the routing kernel's code (so every CTA holds
-  // the same, bit-identical result and no separate launch is needed): warp w
-  // routes tokens w, w + 18, ...; then one warp ranks the T * k <= 64 rows by
-  // expert into the maps and the active-expert slots.
+  // Routing, in every CTA with the routing kernel's top-k code (so every CTA
+  // holds the same, bit-identical result and no separate launch is needed):
+  // warp w routes tokens w, w + 18, ...; then one warp ranks the T * k <= 64
+  // rows by expert into the maps and the active-expert slots and forms the
+  // cost prefix of both FCs over those slots.
   const int R = g.T * g.k;
   for (int t = warp; t < g.T; t += kLayerThreads / 32) {
     if (g.route_n == 1) route_one_token<1>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
@@ -1104,27 +1126,25 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   }
   __syncthreads();
   if (warp == 0) {
-    RouteOut o{};
-    o.offsets = S.r_off;
-    o.p2e = S.r_p2e;
+    RankOut o;
     o.e2p = S.r_e2p;
-    o.meta = &S.na;
-    o.slots = reinterpret_cast<SlotDesc *>(S.slot);
-    build_maps_small(S.r_ids, R, g.E, o, S.r_cnt, S.r_off2);
+    o.p2e = S.r_p2e;
+    o.row_tok = S.row_tok;
+    o.row2slot = S.row2slot;
+    o.slots = S.slot;
+    o.na = &S.na;
+    rank_rows_small(S.r_ids, R, g.E, g.k, o);
+    __syncwarp();
+    if (S.na > 0) {
+      cost_prefix(S, L.f[0], 0);
+      cost_prefix(S, L.f[1], 1);
+    }
   } else if (blockIdx.x == 0 && g.ids_out && tid - 32 < R) {
     g.ids_out[tid - 32] = S.r_ids[tid - 32];
   }
   __syncthreads();
   const int na = min(S.na, kMaxSlots);
   if (na <= 0) return;  // every CTA sees the same count
-  if (tid < R) S.row_tok[tid] = S.r_p2e[tid] / g.k;
-  if (tid < na) {
-    const int4 sd = S.slot[tid];
-    for (int q = 0; q < sd.z; ++q) S.row2slot[sd.y + q] = tid;
-  }
-  __syncthreads();
-  if (warp < 2) cost_prefix(S, L.f[warp], warp);
-  __syncthreads();
   {  // the split of both FCs, one boundary per thread
     const int G = (int)gridDim.x;
     if (tid <= G) split_bound(S, L.f[0], 0, tid);
@@ -1133,9 +1153,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   __syncthreads();
   // this CTA's segments, and (beside them) the CTAs holding units, which the
   // partial-sum offsets need
-  if (tid == 0) build_segments<FMT>(S, g, L.f[0], 0);
-  if (tid == 32) build_segments<FMT>(S, g, L.f[1], 1);
-  if (warp == 2 || warp == 3) busy_prefix(S, warp - 2);
+  if (warp == 0) build_segments<FMT>(S, g, L.f[0], 0);
+  else if (warp == 1) build_segments<FMT>(S, g, L.f[1], 1);
+  else if (warp == 2 || warp == 3) busy_prefix(S, warp - 2);
   __syncthreads();
   // 1 KB-aligned regions (the tensor and bulk copies need 16-byte alignment)
   unsigned char *base = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
@@ -1314,7 +1334,7 @@ static cudaError_t encode_scale_map(CUtensorMap *m, const uint8_t *scales, int E
 }
 
 template <int FMT>
-static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, cudaStream_t stream) {
+static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, bool pdl, cudaStream_t stream) {
   static int smem_set = 0, smem_ok = 0;
   auto kfn = moe_layer_kernel<FMT>;
   if (L.smem > smem_set) {
@@ -1343,15 +1363,17 @@ static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, cuda
   cfg.blockDim = dim3(kLayerThreads);
   cfg.dynamicSmemBytes = L.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kfn, a, L);
 }
 
-cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, cudaStream_t stream) {
+cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, bool pdl, cudaStream_t stream) {
   if (L.f[0].tma) {
     cudaError_t err = encode_scale_map(&a.tm_s1, a.s1, E, L.f[0]);
     if (err != cudaSuccess) return err;
@@ -1360,8 +1382,8 @@ cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, cudaStream_t s
     cudaError_t err = encode_scale_map(&a.tm_s2, a.s2, E, L.f[1]);
     if (err != cudaSuccess) return err;
   }
-  if (a.fmt == QMOE_NVFP4) return launch_layer_fmt<QMOE_NVFP4>(a, L, stream);
-  return launch_layer_fmt<QMOE_MXFP4>(a, L, stream);
+  if (a.fmt == QMOE_NVFP4) return launch_layer_fmt<QMOE_NVFP4>(a, L, pdl, stream);
+  return launch_layer_fmt<QMOE_MXFP4>(a, L, pdl, stream);
 }
 
 }  // namespace qmoe

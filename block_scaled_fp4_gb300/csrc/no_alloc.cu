@@ -81,7 +81,10 @@ extern "C" qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const fl
   st = scratch_address(&scratch);
   if (st != QMOE_OK) return st;
   size_t have = kStaticScratchBytes;
-  return qmoe_fp4_moe_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, nullptr, nullptr, fmt, T, H, I,
-                              E, k, normalize, swiglu_fusion, alpha, beta, limit, out, topk_ids_out, scratch, &have,
-                              stream);
+  // The array is zero when the module loads and its header stays zero between
+  // calls (decode kernels leave it so; the prefill path never writes it).
+  const qmoe_fp4_format primed = (qmoe_fp4_format)((int)fmt | (int)QMOE_WORKSPACE_PRIMED);
+  return qmoe_fp4_moe_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, nullptr, nullptr, primed, T, H,
+                              I, E, k, normalize, swiglu_fusion, alpha, beta, limit, out, topk_ids_out, scratch,
+                              &have, stream);
 }

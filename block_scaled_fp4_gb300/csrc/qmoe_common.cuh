@@ -121,7 +121,8 @@ struct LayerArgs {
   const uint16_t *x;       // bf16 [T, H]
   const uint8_t *w1, *s1, *w2, *s2;
   const float *g1, *g2;
-  int32_t *meta;           // [1] device error flag, [2], [3] grid barrier counters (zero at launch)
+  int32_t *meta;           // workspace header: [1] device error flag, [2], [3] grid barrier counters,
+                           // [4] CTAs out; [2..4] are zero at launch and the kernel leaves them zero
   float *p1, *p2;          // fp32 partial sums of FC1 / FC2 (split-K segments)
   uint16_t *out;           // [T, H] bf16
   CUtensorMap tm_s1, tm_s2;  // block scales as 2-D byte arrays (when FcPlan::tma)
@@ -151,7 +152,9 @@ struct LayerPlan {
 };
 qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, int k, LayerPlan &L,
                             size_t &p1_floats, size_t &p2_floats);
-cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, cudaStream_t stream);
+// pdl: launch with programmatic dependent launch (the header is already zero,
+// so no memset sits between this kernel and the previous one).
+cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, bool pdl, cudaStream_t stream);
 
 // Programmatic dependent launch: let the next kernel in the stream start while
 // this one runs / wait here until the previous kernel's results are visible.

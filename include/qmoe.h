@@ -72,8 +72,27 @@ typedef enum {
      * decode kernel (16 or fewer consecutive blocks of a column tile) is then
      * one contiguous run of bytes per block row instead of N runs of <= 16
      * bytes, which is what lets it stream at full bandwidth. */
-    QMOE_SCALES_KMAJOR = 0x100
+    QMOE_SCALES_KMAJOR = 0x100,
+    /* Flag, OR'd into the format of qmoe_fp4_moe_forward: the workspace's
+     * header (its first QMOE_WORKSPACE_HEADER_BYTES bytes) is already zero.
+     * The caller zeroes it once (cudaMemsetAsync) when it sets the workspace
+     * aside; after that the library keeps it zero: a decode call leaves it so
+     * when its kernel returns (the last CTA out clears the counters) and the
+     * prefill path never writes it.  With the flag a decode call launches its
+     * kernel alone, without the per-call header reset, and with programmatic
+     * dependent launch: the kernel may start on an SM while the previous
+     * kernel of the stream is still finishing elsewhere, and waits until that
+     * kernel's results are visible before it touches global memory.  Back-to-
+     * back layers then pay no memset node and no full launch gap.  Header
+     * word 1 (int32) is the decode kernel's error flag, set to 1 when a
+     * bounded wait inside the kernel gave up (its results are then not to be
+     * trusted); with the flag it stays set until the caller clears it. */
+    QMOE_WORKSPACE_PRIMED = 0x200
 } qmoe_fp4_format;
+
+/* Bytes at the start of every forward workspace reserved for the decode
+ * kernel's error flag and grid-barrier counters (see QMOE_WORKSPACE_PRIMED). */
+#define QMOE_WORKSPACE_HEADER_BYTES 64
 
 /* Largest number of expanded rows (T * k) the decode GEMV path takes; more rows
  * take the prefill path (dequantise + tensor-core grouped GEMM).  The window
@@ -151,8 +170,9 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   workspace, workspace_bytes: see the conventions above.
  * T * k <= QMOE_GEMV_MAX_ROWS runs the decode path: one persistent kernel for
  * routing, FC1, SwiGLU, FC2 and the un-permute, dequantising in registers
- * (after a 12-byte memset of its counters in the workspace).  Its routing
- * is the code of qmoe_route_topk, so the selected experts are identical.
+ * (after a memset of the workspace header, unless fmt carries
+ * QMOE_WORKSPACE_PRIMED).  Its top-k is the code of qmoe_route_topk, so the
+ * selected experts are identical.
  * The decode kernel is a cooperative launch of one CTA per SM:
  * it needs the whole GPU's residency and returns QMOE_ERR_CUDA if another
  * context keeps it from launching.  Larger T * k runs the prefill path
@@ -234,8 +254,9 @@ qmoe_status qmoe_fp4_scales_kmajor(const uint8_t *block_scales, int E, int N, in
  *  - Every call, on any stream or host thread, uses the same array, which keeps
  *    the last call's contents: calls that overlap on the GPU race and corrupt
  *    each other's results.  Order them (one stream, or events).
- *  - Nothing in the array needs to start at zero: the routing kernel clears the
- *    per-call counters the later kernels rely on at the start of every call.
+ *  - The array starts at zero, and its header (QMOE_WORKSPACE_HEADER_BYTES)
+ *    stays zero between calls (see QMOE_WORKSPACE_PRIMED), so every call runs
+ *    as a primed one: no per-call reset, programmatic dependent launch.
  */
 #define QMOE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -259,8 +280,9 @@ const char *qmoe_last_error(void);
  * are created by the caller (cudaEventCreate) and must outlive the calls.
  * Pass NULL to switch it off.  Process-wide setting; not thread-safe.
  * Returns the number of kernels one forward call launches for decode shapes
- * (one: the fused routing + FC1 + FC2 + un-permute kernel, after a 12-byte
- * memset of its counters), i.e. how many events after the first are used.
+ * (one: the fused routing + FC1 + FC2 + un-permute kernel, after a memset of
+ * the workspace header unless QMOE_WORKSPACE_PRIMED), i.e. how many events
+ * after the first are used.
  */
 int qmoe_set_stage_events(cudaEvent_t *events, int n_events);
 

@@ -95,3 +95,37 @@ def test_route_and_dequant_validation(qm):
     assert L.qmoe_fp4_dequant(P(264), P(256), None, 1, 64, 64, 0, P(256), None) == 2
     assert L.qmoe_fp4_dequant(P(256), P(256), None, 1, 64, 64, 7, P(256), None) == 3
     assert b"format" in L.qmoe_last_error()
+
+
+def test_binding_constants_match_the_header(qm):
+    """The flag and size constants the binding passes through are the header's."""
+    src = open(os.path.join(ROOT, "include", "qmoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+
+    def value(name):
+        m = re.search(r"\b" + name + r"\s*=\s*(0x[0-9A-Fa-f]+|\d+)", src) or \
+            re.search(r"#define\s+" + name + r"\s+(0x[0-9A-Fa-f]+|\d+)", src)
+        assert m, name
+        return int(m.group(1), 0)
+
+    assert value("QMOE_NVFP4") == qm.NVFP4 and value("QMOE_MXFP4") == qm.MXFP4
+    assert value("QMOE_SCALES_KMAJOR") == qm.SCALES_KMAJOR
+    assert value("QMOE_WORKSPACE_PRIMED") == qm.WORKSPACE_PRIMED
+    assert value("QMOE_WORKSPACE_HEADER_BYTES") == qm.WORKSPACE_HEADER_BYTES
+    assert value("QMOE_GEMV_MAX_ROWS") == qm.GEMV_MAX_ROWS
+    # the flags are distinct bits above the format codes
+    assert qm.SCALES_KMAJOR & qm.WORKSPACE_PRIMED == 0 and min(qm.SCALES_KMAJOR, qm.WORKSPACE_PRIMED) > qm.MXFP4
+
+
+def test_primed_flag_is_a_format_flag_only_for_the_forward_calls(qm):
+    """dequant and scales_kmajor take a plain format: the flag is rejected there."""
+    L = qm.load()
+    dummy = ctypes.c_void_p(256)
+    for fmt in (qm.NVFP4 | qm.WORKSPACE_PRIMED, qm.MXFP4 | qm.WORKSPACE_PRIMED):
+        assert L.qmoe_fp4_dequant(dummy, dummy, None, 1, 64, 64, fmt, dummy, None) == 3
+        assert L.qmoe_fp4_scales_kmajor(dummy, 1, 64, 64, fmt, ctypes.c_void_p(1 << 20), None) == 3
+    # the forward size query accepts it and the size does not depend on it
+    base = qm.forward_workspace_bytes(4, 2048, 512, 256, 8, qm.NVFP4 | qm.SCALES_KMAJOR)
+    assert base == qm.forward_workspace_bytes(4, 2048, 512, 256, 8,
+                                              qm.NVFP4 | qm.SCALES_KMAJOR | qm.WORKSPACE_PRIMED)
+    assert base >= qm.WORKSPACE_HEADER_BYTES
