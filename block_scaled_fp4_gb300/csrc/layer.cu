@@ -222,16 +222,20 @@ __device__ __forceinline__ void store_tile4x4(uint32_t v0, uint32_t v1, uint32_t
 // ---- work geometry ------------------------------------------------------------------
 
 // Work split: the units of FC f, in (expert slot, column tile, k) order, are
-// cut into gridDim.x ranges of about equal cost, cost(unit) = 4 * rows for an
-// expert with `rows` rows (each row is one pass over the unit, decoded on its
-// own); CTA c gets units [bnd[f][c], bnd[f][c + 1]).
-__host__ __device__ __forceinline__ int unit_cost(int rows) { return 4 * rows; }
-// A pass start (one per row of each (expert slot, tile) pair: partial-sum
-// write of the previous pass, activation staging, first copy) costs
-// P.pass_cost in the same units (fitted to per-CTA timings: about 3 units of
-// decode in FC1, 1.5 in FC2); it is charged at the pair's start.
-__host__ __device__ __forceinline__ int pair_cost(const FcPlan &P, int rows) {
-  return rows * P.pass_cost + P.ku * unit_cost(rows);
+// cut into gridDim.x ranges of about equal cost; CTA c gets units
+// [bnd[f][c], bnd[f][c + 1]).  Costs are in 1/64 of one unit decoded for one
+// row.  A CTA spends, on each segment (its units of one pair) of an r-row
+// expert, r * (pass start + 64 * units): every row is one pass over the
+// units.  Every CTA pays at least one segment; the CTA that crosses into a
+// new pair pays one more, so each pair start is charged r * pass_cost.  The
+// per-unit cost of an r-row expert, P.ucost[r - 1] (host table), is what makes
+// a CTA inside such a pair take as long as one inside a one-row pair despite
+// its r pass starts.
+__device__ __forceinline__ int unit_cost(const FcPlan &P, int rows) {
+  return P.ucost[min(rows, kCostRows) - 1];
+}
+__device__ __forceinline__ int pair_cost(const FcPlan &P, int rows) {
+  return rows * P.pass_cost + P.ku * unit_cost(P, rows);
 }
 
 struct FcWork {
@@ -375,8 +379,7 @@ __device__ void build_segments(Shared &S, const LayerArgs &g, const FcPlan &P, i
   if (lane == 0) S.nseg[f] = nseg;
 }
 
-// Cost prefix over the expert slots and the split boundaries of FC f.
-// Prefix: one warp; boundaries: threads [t0, t0 + G].
+// Cost prefix over the expert slots (one warp).
 __device__ void cost_prefix(Shared &S, const FcPlan &P, int f) {
   const int lane = (int)lane_id();
   const int per = (S.na + 31) / 32;
@@ -442,7 +445,8 @@ __device__ void split_bound(Shared &S, const FcPlan &P, int f, int c) {
     if (S.scum[f][mid] <= x) lo = mid; else hi = mid - 1;
   }
   // inside slot lo: pairs of cost pc, each a pass-start charge then ku units
-  const int r = S.slot[lo].z, cu = unit_cost(r), pc = pair_cost(P, r);
+  // of cost cu; the range starts at the first unit that begins at or after x
+  const int r = S.slot[lo].z, cu = unit_cost(P, r), pc = pair_cost(P, r);
   const long long rem = x - S.scum[f][lo];
   const int q = (int)(rem / pc);
   int u;
@@ -968,11 +972,11 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
   }
   // combine the row groups (a fixed butterfly over the lanes of the warp) and
   // write the partial rows
+  for (int m = wpw; m < 32; m <<= 1)
 #pragma unroll
-  for (int r = 0; r < RC; ++r)
+    for (int r = 0; r < RC; ++r)
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      for (int m = wpw; m < 32; m <<= 1) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], m);
+      for (int c = 0; c < 8; ++c) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], m);
   // partial rows of this segment: dst[row * NT + col], row = c0 + r (the
   // offsets are computed by the activation copy warp after its first copies)
   wait_bar(S, g, &S.basesready, 0u);
@@ -1241,10 +1245,6 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
     set_error("no column tiling of N = %d / %d fits the decode kernel", 2 * I, H);
     return QMOE_ERR_UNSUPPORTED;
   }
-  // pass-start charges of the split, in units of a quarter of a unit-pass
-  // (FC1's pass change also waits for its activation rows from memory)
-  L.f[0].pass_cost = 12;
-  L.f[1].pass_cost = 6;
   const size_t G = (size_t)num_sms();
   if (G > (size_t)kMaxCtas) {
     set_error("the decode kernel supports at most %d SMs (this GPU has %zu)", kMaxCtas, G);
@@ -1252,6 +1252,25 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
   }
   const size_t R = (size_t)T * k;
   const size_t na_max = std::min<size_t>((size_t)E, R);
+  // pass-start charge of the split, in 1/64 of a unit decoded for one row
+  // (fitted to per-CTA timings), and the per-unit cost of an r-row expert:
+  // with n1 = R * ct * ku / G one-row units per CTA (in [1, ku]) and
+  // p = pass_cost / 64, a CTA inside an r-row pair matches a one-row CTA's
+  // time (n1 + p) with n_r = (n1 - p * (r - 1)) / r units, so a unit costs
+  // 64 * n1 / n_r, at most twice the decode alone (a pair of many rows is
+  // then cut into short segments, each still paying all its rows' passes)
+  const int pass_start[2] = {192, 96};
+  for (int f = 0; f < 2; ++f) {
+    FcPlan &P = L.f[f];
+    P.pass_cost = pass_start[f];
+    const double n1 = std::max(1.0, std::min((double)P.ku, (double)(R * P.ct * P.ku) / (double)G));
+    const double p = P.pass_cost / 64.0;
+    for (int r = 1; r <= kCostRows; ++r) {
+      const double nr = (n1 - p * (r - 1)) / r;
+      const double c = nr > n1 / (2.0 * r) ? 64.0 * n1 / nr : 128.0 * r;
+      P.ucost[r - 1] = (int)std::min(128.0 * r, std::ceil(c));
+    }
+  }
   int slot = 0, win = 0;
   for (int f = 0; f < 2; ++f) {
     const FcPlan &P = L.f[f];
@@ -1260,10 +1279,10 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
     // segments of one CTA: at most the pairs that exist, and at most two more
     // (the first and the last) than the pairs lying wholly inside its cost
     // range [c * total / G, (c + 1) * total / G], each of which costs at
-    // least pass_cost + 4 ku.  The total is ct * sum over slots of
-    // rows * (pass_cost + 4 ku) <= ct * (pass_cost + 4 ku) R.
-    const size_t pc_min = (size_t)P.pass_cost + 4 * (size_t)P.ku;
-    const size_t total = (size_t)P.ct * pc_min * R;
+    // least pass_cost + 64 ku (one row).  A unit of an r-row expert costs at
+    // most 128 r, so the total is at most ct * R * (pass_cost + 128 ku).
+    const size_t pc_min = (size_t)P.pass_cost + 64 * (size_t)P.ku;
+    const size_t total = (size_t)P.ct * R * ((size_t)P.pass_cost + 128 * (size_t)P.ku);
     const size_t segs = std::min<size_t>(na_max * (size_t)P.ct, 2 + (total / G + 1) / pc_min);
     if (segs > (size_t)kMaxSegs) {
       set_error("too many experts per CTA for the decode kernel (N = %d, K = %d)", P.N, P.K);

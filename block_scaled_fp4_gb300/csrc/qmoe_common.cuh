@@ -128,6 +128,8 @@ struct LayerArgs {
   CUtensorMap tm_s1, tm_s2;  // block scales as 2-D byte arrays (when FcPlan::tma)
 };
 
+constexpr int kCostRows = 64;  // rows of one expert in the decode window (T * k <= 64)
+
 // Geometry of one FC for the decode kernel (host-computed).  Unit = 16*RGS k
 // rows x NT columns; thread (w, rg) owns column word w of k-group rg.
 struct FcPlan {
@@ -142,7 +144,8 @@ struct FcPlan {
   int kn;       // 1: block scales are k-major [E, nblocks, N]; a unit's scale rows ride in its ring slot
   int bpu;      // scale block rows one unit touches (k-major)
   int sc_off;   // offset of those rows in a ring slot
-  int pass_cost;  // split charge of one pass start (see pair_cost)
+  int pass_cost;  // split: charge of a pass start, in 1/64 of a unit decoded for one row
+  int ucost[kCostRows];  // split: cost of one unit of an r-row expert at [r - 1] (same scale)
 };
 struct LayerPlan {
   FcPlan f[2];
