@@ -857,18 +857,22 @@ __device__ bool prestage_fc2(Shared &S, const LayerArgs &g, const LayerPlan &L, 
     total += S.slot[sg.a].z * len;
   }
   if (total * 2 > kXrawBytes) return false;
+  // one flat loop over every element of every pass, so that all their
+  // partial-sum loads are in flight together (segment after segment, a
+  // segment's rows after one another: the passes' order)
   uint16_t *dst = reinterpret_cast<uint16_t *>(xraw);
-  for (int si = 0; si < S.nseg[1]; ++si) {
-    const Seg sg = S.seg[1][si];
-    const int4 sd = S.slot[sg.a];
-    const int k0 = sg.j0 * unit_k, len = min(P.K, sg.j1 * unit_k) - k0;
-    for (int c0 = 0; c0 < sd.z; c0 += kRowsMax) {
-      const int rows = min(kRowsMax, sd.z - c0);
-      for (int i = threadIdx.x; i < rows * len; i += kCons) {
-        const int rr = i / len, kk = i - rr * len;
-        dst[i] = fc2_activation(S, g, L, sg.a, sd.z, c0 + rr, k0 + kk);
+  for (int i = threadIdx.x; i < total; i += kCons) {
+    int base = 0;
+    for (int si = 0; si < S.nseg[1]; ++si) {
+      const Seg sg = S.seg[1][si];
+      const int rows = S.slot[sg.a].z;
+      const int k0 = sg.j0 * unit_k, len = min(P.K, sg.j1 * unit_k) - k0;
+      if (i < base + rows * len) {
+        const int rr = (i - base) / len, kk = i - base - rr * len;
+        dst[i] = fc2_activation(S, g, L, sg.a, rows, rr, k0 + kk);
+        break;
       }
-      dst += rows * len;
+      base += rows * len;
     }
   }
   return true;

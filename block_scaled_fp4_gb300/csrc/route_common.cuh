@@ -108,11 +108,13 @@ __device__ __forceinline__ void route_one_token(const float *__restrict__ logits
   uint64_t top[kMaxTopK];
   warp_topk_keys<N>(key, k, top);
   const float mx = key_logit(top[0]);
-  float s = 0.f;
+  float s = 0.f;  // softmax denominator over all E (not needed when the k weights are renormalised)
+  if (!normalize) {
 #pragma unroll
-  for (int i = 0; i < N; ++i)
-    if (lane + 32 * i < E) s += expf(v[i] - mx);
-  s = warp_sum(s);
+    for (int i = 0; i < N; ++i)
+      if (lane + 32 * i < E) s += expf(v[i] - mx);
+    s = warp_sum(s);
+  }
   // selected experts, in key order
   float sel_sum = 0.f;
   float mine_e = 0.f;
@@ -215,12 +217,14 @@ __device__ inline void rank_rows_small(const int32_t *ids_s, int R, int E, int k
   const int key0 = v0 ? ids_s[i0] * 64 + i0 : kNone, key1 = v1 ? ids_s[i1] * 64 + i1 : kNone;
   const int e0 = key0 >> 6, e1 = key1 >> 6;
   int rank0 = 0, rank1 = 0, lt0 = 0, lt1 = 0, le0 = 0, le1 = 0;
+#pragma unroll 8
   for (int m = 0; m < 32; ++m) {
     const int a = __shfl_sync(0xFFFFFFFFu, key0, m), ea = a >> 6;
     rank0 += a < key0; lt0 += ea < e0; le0 += ea <= e0;
     rank1 += a < key1; lt1 += ea < e1; le1 += ea <= e1;
   }
   if (R > 32) {  // the same in every lane
+#pragma unroll 8
     for (int m = 0; m < 32; ++m) {
       const int a = __shfl_sync(0xFFFFFFFFu, key1, m), ea = a >> 6;
       rank0 += a < key0; lt0 += ea < e0; le0 += ea <= e0;
