@@ -138,7 +138,7 @@ def forward_workspace_bytes(T, H, I, E, k, fmt=NVFP4, with_dequantized=False) ->
 def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: int = 1,
                 alpha: float = 1.0, beta: float = 0.0, limit: float = math.inf,
                 w1_dequant=None, w2_dequant=None, out=None, topk_ids=None, workspace=None,
-                stream=None):
+                stream=None, swiglu_fusion: int = 1):
     """The MoE layer.  x bf16 [T,H]; logits f32 [T,E]; w1 uint8 [E,H,I];
     s1 uint8 [E,2I,H/bs]; g1 f32 [E] or None; w2 uint8 [E,I,H/2];
     s2 uint8 [E,H,I/bs]; g2 f32 [E] or None.  With ``fmt | SCALES_KMAJOR``
@@ -158,15 +158,15 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: 
     nbytes = ctypes.c_size_t(workspace.numel() * workspace.element_size())
     _check(load().qmoe_fp4_moe_forward(_ptr(x), _ptr(logits), _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2),
                                        _ptr(s2), _ptr(g2), _ptr(w1_dequant), _ptr(w2_dequant), fmt, T,
-                                       H, I, E, k, int(normalize), 1, float(alpha), float(beta),
-                                       float(limit), _ptr(out), _ptr(topk_ids), _ptr(workspace),
-                                       ctypes.byref(nbytes), _stream(stream)))
+                                       H, I, E, k, int(normalize), int(swiglu_fusion), float(alpha),
+                                       float(beta), float(limit), _ptr(out), _ptr(topk_ids),
+                                       _ptr(workspace), ctypes.byref(nbytes), _stream(stream)))
     return out
 
 
 def moe_forward_no_alloc(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: int = 1,
                          alpha: float = 1.0, beta: float = 0.0, limit: float = math.inf, out=None,
-                         topk_ids=None, stream=None):
+                         topk_ids=None, stream=None, swiglu_fusion: int = 1):
     """The MoE layer through the entry point that allocates no device memory
     (its scratch is a fixed array inside the library; see include/qmoe.h).
     ``out`` must be given by callers that cannot allocate; when it is None a
@@ -181,8 +181,8 @@ def moe_forward_no_alloc(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, no
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     _check(load().qmoe_fp4_moe_forward_no_alloc(_ptr(x), _ptr(logits), _ptr(w1), _ptr(s1), _ptr(g1),
                                                 _ptr(w2), _ptr(s2), _ptr(g2), fmt, T, H, I, E, k,
-                                                int(normalize), 1, float(alpha), float(beta),
-                                                float(limit), _ptr(out), _ptr(topk_ids),
+                                                int(normalize), int(swiglu_fusion), float(alpha),
+                                                float(beta), float(limit), _ptr(out), _ptr(topk_ids),
                                                 _stream(stream)))
     return out
 

@@ -152,26 +152,18 @@ extern "C" qmoe_status qmoe_fp4_scales_kmajor(const uint8_t *block_scales, int E
 namespace qmoe {
 
 struct DecodeLayout {
-  int32_t *ids, *offsets, *p2e, *e2p, *active, *meta;
-  SlotDesc *slots;
-  float *weights, *p1, *p2;
+  int32_t *meta;
+  float *p1, *p2;
   size_t bytes;
 };
 
-static DecodeLayout decode_layout(void *ws, int T, int E, int k, size_t p1_floats, size_t p2_floats) {
-  const size_t R = (size_t)T * k;
-  const size_t S = (size_t)(E < (int)R ? E : (int)R);
+// The decode kernel routes in shared memory, so its workspace is the header
+// and the FC1 / FC2 partial sums.
+static DecodeLayout decode_layout(void *ws, size_t p1_floats, size_t p2_floats) {
   Carve c(ws);
   DecodeLayout L{};
   // [0] unused, [1] device error flag, [2], [3] grid barriers, [4] CTAs out
   L.meta = c.take<int32_t>(QMOE_WORKSPACE_HEADER_BYTES / sizeof(int32_t));
-  L.ids = c.take<int32_t>(R);
-  L.weights = c.take<float>(R);
-  L.offsets = c.take<int32_t>((size_t)E + 1);
-  L.p2e = c.take<int32_t>(R);
-  L.e2p = c.take<int32_t>(R);
-  L.active = c.take<int32_t>(S);
-  L.slots = c.take<SlotDesc>(S);
   L.p1 = c.take<float>(p1_floats);
   L.p2 = c.take<float>(p2_floats);
   L.bytes = (c.off + 255) & ~(size_t)255;
@@ -220,9 +212,9 @@ static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k,
 static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w, const uint8_t *fc1_s,
                                    const float *fc1_g, const uint8_t *fc2_w, const uint8_t *fc2_s, const float *fc2_g,
                                    const uint16_t *fc1_wd, const uint16_t *fc2_wd, int fmt, bool kmajor, int T, int H,
-                                   int I, int E, int k, int normalize, float alpha, float beta, float limit,
-                                   uint16_t *out, int32_t *topk_ids_out, void *workspace, size_t *workspace_bytes,
-                                   cudaStream_t stream) {
+                                   int I, int E, int k, int normalize, int fusion, float alpha, float beta,
+                                   float limit, uint16_t *out, int32_t *topk_ids_out, void *workspace,
+                                   size_t *workspace_bytes, cudaStream_t stream) {
   QMOE_REQUIRE((long long)T * k <= (1LL << 30), QMOE_ERR_UNSUPPORTED, "T*k too large");
   const int bs = block_size(fmt);
   const bool need_w1 = fc1_wd == nullptr, need_w2 = fc2_wd == nullptr;
@@ -276,7 +268,7 @@ static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const
   }
   PrefillArgs a{};
   a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
-  a.alpha = alpha; a.beta = beta; a.limit = limit;
+  a.alpha = alpha; a.beta = beta; a.limit = limit; a.fusion = fusion;
   a.x = x; a.offsets = L.offsets; a.p2e = L.p2e; a.e2p = L.e2p; a.weights = L.weights;
   a.w1d = w1d; a.w2d = w2d; a.act = L.act; a.y = L.y; a.out = out;
   return cuda_status(launch_prefill(a, stream), "prefill launch");
@@ -302,21 +294,23 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   QMOE_REQUIRE(H >= 64 && I >= 64, QMOE_ERR_INVALID_ARG, "H and I must be >= 64 (got %d, %d)", H, I);
   QMOE_REQUIRE(H % 64 == 0 && I % 64 == 0, QMOE_ERR_UNSUPPORTED, "H and I must be multiples of 64 (got %d, %d)", H,
                I);
-  QMOE_REQUIRE(swiglu_fusion == 1, QMOE_ERR_UNSUPPORTED, "only swiglu_fusion=1 (interleaved) is supported (got %d)",
-               swiglu_fusion);
+  QMOE_REQUIRE(swiglu_fusion >= 0 && swiglu_fusion <= 2, QMOE_ERR_UNSUPPORTED,
+               "swiglu_fusion must be 0, 1 (interleaved) or 2 (concatenated) (got %d)", swiglu_fusion);
+  // 0 is read as 1: the pages' backward-compatibility remap for QMoE
+  const int fusion = swiglu_fusion == 2 ? 2 : 1;
   QMOE_REQUIRE(!std::isnan(alpha) && !std::isnan(beta) && !std::isnan(limit), QMOE_ERR_INVALID_ARG,
                "alpha, beta and limit must not be NaN");
   const long long R = (long long)T * k;
   if (R > QMOE_GEMV_MAX_ROWS)
     return prefill_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, fc1_wd, fc2_wd, base_fmt, kmajor, T, H,
-                           I, E, k, normalize, alpha, beta, limit, out, topk_ids_out, workspace, workspace_bytes,
-                           stream);
+                           I, E, k, normalize, fusion, alpha, beta, limit, out, topk_ids_out, workspace,
+                           workspace_bytes, stream);
   QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
   LayerPlan plan;
   size_t p1_floats = 0, p2_floats = 0;
   st = make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);
   if (st != QMOE_OK) return st;
-  const DecodeLayout need = decode_layout(nullptr, T, E, k, p1_floats, p2_floats);
+  const DecodeLayout need = decode_layout(nullptr, p1_floats, p2_floats);
   if (!workspace) {
     *workspace_bytes = need.bytes;
     return QMOE_OK;
@@ -331,11 +325,11 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   QMOE_REQUIRE((fc1_g == nullptr || ((uintptr_t)fc1_g & 3u) == 0) && (fc2_g == nullptr || ((uintptr_t)fc2_g & 3u) == 0),
                QMOE_ERR_MISALIGNED, "global scales must be 4-byte aligned");
 
-  const DecodeLayout L = decode_layout(workspace, T, E, k, p1_floats, p2_floats);
+  const DecodeLayout L = decode_layout(workspace, p1_floats, p2_floats);
   LayerArgs g{};
   g.fmt = base_fmt;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
-  g.alpha = alpha; g.beta = beta; g.limit = limit;
+  g.alpha = alpha; g.beta = beta; g.limit = limit; g.fusion = fusion;
   g.logits = logits; g.normalize = normalize; g.route_n = route_keys_per_lane(E, k);
   g.ids_out = topk_ids_out;
   g.x = x;

@@ -761,11 +761,39 @@ __device__ __forceinline__ void warp_transpose_window(const uint8_t *wstage, uin
   __syncwarp();
 }
 
+// FC1 output column col of this row (row `row` of slot a): its partial sums
+// summed in segment order.
+__device__ __forceinline__ float fc1_column(const Shared &S, const LayerArgs &g, const FcPlan &P1, int a, int nrows,
+                                            int row, int col) {
+  const int t1 = col / P1.NT, c1 = col - t1 * P1.NT;
+  const int pair = a * P1.ct + t1;
+  const int nc = S.pcnt[0][pair];
+  const size_t stride = (size_t)nrows * P1.NT;
+  const float *src = g.p1 + S.base[0][pair] + (size_t)row * P1.NT + c1;
+  float h = 0.f;
+  for (int c = 0; c < nc; c += 8) {  // up to 8 loads in flight
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = c + u < nc ? __ldcg(src + (c + u) * stride) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (c + u < nc) h += v[u];
+  }
+  return h;
+}
+
 // a[row][k] = bf16(SwiGLU(g1 * h)) for FC2's activations, h = the FC1 partial
-// sums of this row (row c0 + rr of slot a) summed in segment order.
+// sums of this row (row c0 + rr of slot a) summed in segment order.  The gate
+// and linear columns are 2k and 2k + 1 (interleaved, read as one pair), or k
+// and I + k (concatenated).
 __device__ __forceinline__ uint16_t fc2_activation(const Shared &S, const LayerArgs &g, const LayerPlan &L, int a,
                                                    int nrows, int row, int k) {
   const FcPlan &P1 = L.f[0];
+  if (g.fusion == 2) {
+    const float g1 = S.gs[0][a];
+    const float hg = fc1_column(S, g, P1, a, nrows, row, k), hl = fc1_column(S, g, P1, a, nrows, row, g.I + k);
+    return (uint16_t)f32_to_bf16_rne(swiglu(hg * g1, hl * g1, g.alpha, g.beta, g.limit));
+  }
   const int col = 2 * k;
   const int t1 = col / P1.NT, c1 = col - t1 * P1.NT;
   const int pair = a * P1.ct + t1;

@@ -27,6 +27,8 @@ struct GroupedGemm {
   const int32_t *offsets;  // [E + 1] first row of each expert
   int E, N, K;
   int swiglu;              // 1: out_a[p][n / 2] = bf16(SwiGLU(h[n], h[n + 1])); 0: out_y[p][n] = h
+  int concat;              // with swiglu: B holds the gate rows [0, N/2) then the linear rows [N/2, N);
+                           // output column n reads row n / 2 (n even) or N / 2 + n / 2 (n odd)
   uint16_t *out_a;         // [R, N / 2]
   float *out_y;            // [R, N]
   float alpha, beta, limit;
@@ -181,7 +183,9 @@ __global__ void __launch_bounds__(kTcThreads) grouped_gemm_tc_kernel(const __gri
       a_ok |= 1u << q;
     }
     if (n0 + r < p.N) {
-      b_src[q] = p.B + ((size_t)e * p.N + n0 + r) * p.K + cth * 8;
+      const int n = n0 + r;
+      const int brow = p.concat ? ((n & 1) ? p.N / 2 + (n >> 1) : (n >> 1)) : n;
+      b_src[q] = p.B + ((size_t)e * p.N + brow) * p.K + cth * 8;
       b_ok |= 1u << q;
     }
   }
@@ -327,7 +331,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   GroupedGemm g1{};
   g1.A = a.x; g1.perm = a.p2e; g1.ktop = a.k; g1.lda = a.H;
   g1.B = a.w1d; g1.offsets = a.offsets; g1.E = a.E; g1.N = 2 * a.I; g1.K = a.H;
-  g1.swiglu = 1; g1.out_a = a.act; g1.alpha = a.alpha; g1.beta = a.beta; g1.limit = a.limit;
+  g1.swiglu = 1; g1.concat = a.fusion == 2 ? 1 : 0;
+  g1.out_a = a.act; g1.alpha = a.alpha; g1.beta = a.beta; g1.limit = a.limit;
   grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g1.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
       g1, err_flag);
   cudaError_t err = cudaGetLastError();

@@ -84,14 +84,9 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 void set_error(const char *fmt, ...);
 int num_sms();
 
-// Decode routing: one CTA does top-k, softmax and the stable expert ranking for
-// T <= kFusedRouteMaxTokens tokens.
+// Routing of few tokens: one CTA does top-k, softmax and the stable expert
+// ranking for T <= kFusedRouteMaxTokens tokens.
 constexpr int kFusedRouteMaxTokens = 64;
-
-// Decode-path slot descriptor: the s-th expert (ascending id) that received rows.
-struct SlotDesc {
-  int e, row0, nrows, pad;
-};
 
 struct RouteOut {
   int32_t *ids;        // [T*k]
@@ -99,11 +94,6 @@ struct RouteOut {
   int32_t *offsets;    // [E+1]
   int32_t *p2e;        // [T*k]
   int32_t *e2p;        // [T*k]
-  int32_t *active;     // [min(E, T*k)] experts that got rows, ascending; may be null
-  int32_t *meta;       // [4] meta[0] = number of active experts; may be null
-  SlotDesc *slots;     // [min(E, T*k)] slot descriptors; may be null
-  int32_t *zero_words; // words cleared by the route kernel for later kernels; may be null
-  int n_zero_words;
 };
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int normalize, const RouteOut &o,
@@ -115,6 +105,7 @@ int route_keys_per_lane(int E, int k);
 struct LayerArgs {
   int fmt, T, H, I, E, k;
   float alpha, beta, limit;
+  int fusion;              // FC1 gate/linear columns: 1 interleaved (2m, 2m + 1), 2 concatenated (m, I + m)
   const float *logits;     // fp32 [T, E] router logits
   int normalize, route_n;  // routing: renormalise over the k; keys per lane (1, 2, 4, 8)
   int32_t *ids_out;        // [T, k] selected experts, or null
@@ -159,8 +150,8 @@ qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, in
 // so no memset sits between this kernel and the previous one).
 cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, bool pdl, cudaStream_t stream);
 
-// Programmatic dependent launch: let the next kernel in the stream start while
-// this one runs / wait here until the previous kernel's results are visible.
+// Programmatic dependent launch: let the next kernel in the stream be scheduled /
+// wait here until the previous kernel's results are visible.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -174,6 +165,7 @@ cudaError_t launch_transpose_bytes(const uint8_t *in, int E, int rows, int cols,
 struct PrefillArgs {
   int T, H, I, E, k;
   float alpha, beta, limit;
+  int fusion;                // FC1 gate/linear columns: 1 interleaved, 2 concatenated
   const uint16_t *x;         // bf16 [T, H]
   const int32_t *offsets;    // [E + 1]
   const int32_t *p2e, *e2p;  // [T * k] permute maps

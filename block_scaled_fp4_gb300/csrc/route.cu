@@ -30,8 +30,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
 // expert's count is prefixed over warps (segment order = expanded order, so
 // the rank is stable), then over experts.
 __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, int32_t *p2e, int32_t *e2p,
-                           int32_t *active, int32_t *meta, SlotDesc *slots, int32_t *cnt /* smem [W][E] */,
-                           int32_t *tot /* smem [E+1] */) {
+                           int32_t *cnt /* smem [W][E] */, int32_t *tot /* smem [E+1] */) {
   const int W = blockDim.x >> 5, w = (int)(threadIdx.x >> 5), lane = (int)lane_id();
   for (int i = threadIdx.x; i < W * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
@@ -62,37 +61,31 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
     tot[e] = run;
   }
   __syncthreads();
-  // exclusive scan over experts (warp 0), plus the list of experts with rows
+  // exclusive scan over experts (warp 0)
   if (w == 0) {
     const int per = (E + 31) / 32;
-    int sum = 0, nact = 0;
+    int sum = 0;
     for (int q = 0; q < per; ++q) {
       const int e = lane * per + q;
-      if (e < E) { sum += tot[e]; nact += tot[e] > 0; }
+      if (e < E) sum += tot[e];
     }
-    int incl = sum, iact = nact;
+    int incl = sum;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-      const int a = __shfl_up_sync(0xFFFFFFFFu, incl, m), b = __shfl_up_sync(0xFFFFFFFFu, iact, m);
-      if (lane >= m) { incl += a; iact += b; }
+      const int a = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+      if (lane >= m) incl += a;
     }
-    int run = incl - sum, arun = iact - nact;
+    int run = incl - sum;
     for (int q = 0; q < per; ++q) {
       const int e = lane * per + q;
       if (e < E) {
         const int c = tot[e];
         offsets[e] = run;
         tot[e] = run;
-        if (c > 0 && active) active[arun] = e;
-        if (c > 0 && slots) slots[arun] = SlotDesc{e, run, c, 0};
-        arun += c > 0;
         run += c;
       }
     }
-    if (lane == 31) {
-      offsets[E] = run;
-      if (meta) meta[0] = arun;
-    }
+    if (lane == 31) offsets[E] = run;
   }
   __syncthreads();
   for (int i = lo + lane; i < hi; i += 32) {
@@ -104,17 +97,14 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
   }
 }
 
-// Decode routing: one CTA routes T <= 64 tokens (warp per token) and builds the
-// maps and the slot descriptors.  The next kernel may launch as soon as this
-// one starts (it waits for these results before reading them).
+// Routing of up to kFusedRouteMaxTokens tokens in one CTA (warp per token),
+// then the maps.
 template <int N>
 __global__ void __launch_bounds__(256) route_maps_fused_kernel(const float *__restrict__ logits, int T, int E,
                                                               int k, int normalize, RouteOut o) {
   extern __shared__ int32_t smem_i32[];
-  pdl_launch_dependents();
   const int W = blockDim.x >> 5, w = (int)(threadIdx.x >> 5);
   const int R = T * k;
-  for (int i = threadIdx.x; i < o.n_zero_words; i += blockDim.x) o.zero_words[i] = 0;
   if (R <= 64) {
     int32_t *ids_s = smem_i32, *cnt = smem_i32 + 64, *off = cnt + E;
     for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights, ids_s);
@@ -124,15 +114,14 @@ __global__ void __launch_bounds__(256) route_maps_fused_kernel(const float *__re
   }
   for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights);
   __syncthreads();
-  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
+  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, smem_i32, smem_i32 + W * E);
 }
 
 // Prefill routing, second step: one CTA of 1024 threads builds the maps.
 __global__ void __launch_bounds__(1024) maps_kernel(int R, int E, RouteOut o) {
   extern __shared__ int32_t smem_i32[];
   const int W = blockDim.x >> 5;
-  for (int i = threadIdx.x; i < o.n_zero_words; i += blockDim.x) o.zero_words[i] = 0;
-  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, o.active, o.meta, o.slots, smem_i32, smem_i32 + W * E);
+  build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, smem_i32, smem_i32 + W * E);
 }
 
 int route_keys_per_lane(int E, int k) {

@@ -157,36 +157,29 @@ __device__ inline void build_maps_small(const int32_t *ids_s, int R, int E, cons
   __syncwarp();
   if (ok1 && (p1 & lt) == 0u) cnt[e1] += __popc(p1);
   __syncwarp();
-  // exclusive scan of the counts; the list of experts with rows
+  // exclusive scan of the counts
   const int per = (E + 31) / 32;
-  int sum = 0, nact = 0;
+  int sum = 0;
   for (int q = 0; q < per; ++q) {
     const int e = lane * per + q;
-    if (e < E) { sum += cnt[e]; nact += cnt[e] > 0; }
+    if (e < E) sum += cnt[e];
   }
-  int incl = sum, iact = nact;
+  int incl = sum;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
-    const int a = __shfl_up_sync(0xFFFFFFFFu, incl, m), b = __shfl_up_sync(0xFFFFFFFFu, iact, m);
-    if (lane >= m) { incl += a; iact += b; }
+    const int a = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+    if (lane >= m) incl += a;
   }
-  int run = incl - sum, arun = iact - nact;
+  int run = incl - sum;
   for (int q = 0; q < per; ++q) {
     const int e = lane * per + q;
     if (e < E) {
-      const int c = cnt[e];
       o.offsets[e] = run;
       off[e] = run;
-      if (c > 0 && o.active) o.active[arun] = e;
-      if (c > 0 && o.slots) o.slots[arun] = SlotDesc{e, run, c, 0};
-      arun += c > 0;
-      run += c;
+      run += cnt[e];
     }
   }
-  if (lane == 31) {
-    o.offsets[E] = run;
-    if (o.meta) o.meta[0] = arun;
-  }
+  if (lane == 31) o.offsets[E] = run;
   __syncwarp();
   if (ok0) { const int p = off[e0] + r0; o.e2p[i0] = p; o.p2e[p] = i0; }
   if (ok1) { const int p = off[e1] + r1; o.e2p[i1] = p; o.p2e[p] = i1; }

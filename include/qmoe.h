@@ -135,8 +135,7 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   out[t] = bf16( sum_j w[t][j] * FFN_{id[t][j]}(x[t]) ),
  *   FFN_e(x) = Wd2_e * bf16( SwiGLU( Wd1_e * x ) ),
  * with Wd the dequantised weights, fp32 accumulation, the SwiGLU of operator
- * doc §8 on interleaved FC1 columns (2m = gate, 2m + 1 = linear;
- * swiglu_fusion = 1):
+ * doc §8 on the FC1 columns' (gate, linear) pairs:
  *   G = min(gate, limit); L = clamp(linear, -limit, limit);
  *   SwiGLU = G * sigmoid(alpha * G) * (L + beta)
  * (alpha = 1, beta = 0, limit = +inf is SiLU(gate) * linear).
@@ -163,7 +162,12 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *   T, H, I, E, k  sizes: T >= 1; H, I multiples of 64; 1 <= E <= 256;
  *                1 <= k <= min(8, E).
  *   normalize    as in qmoe_route_topk.
- *   swiglu_fusion must be 1 (interleaved gate/linear columns).
+ *   swiglu_fusion  where FC1's 2I columns hold the pairs (operator doc §8):
+ *                1 interleaved, 2m = gate and 2m + 1 = linear; 2
+ *                concatenated, m = gate and I + m = linear (fc1 (gate) and
+ *                fc3 (value) fused offline); 0 is read as 1, the operator's
+ *                backward-compatibility remap for QMoE.  Other values:
+ *                QMOE_ERR_UNSUPPORTED.
  *   alpha, beta, limit  SwiGLU parameters (limit may be +inf).
  *   out          bf16 [T, H] result.
  *   topk_ids_out int32 [T, k] selected experts, or NULL.

@@ -72,10 +72,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_expert_fc2.restype = i
             L.oracle_expert_fc2.argtypes = [P, i, P, P, P, i, i, i, P]
             L.oracle_expert_ffn.restype = i
-            L.oracle_expert_ffn.argtypes = [P, i, P, P, P, P, P, P, i, i, i, d, d, d, P]
+            L.oracle_expert_ffn.argtypes = [P, i, P, P, P, P, P, P, i, i, i, d, d, d, i, P]
             L.oracle_moe_forward.restype = i
             L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, i,
-                                             d, d, d, P, i, P, i]
+                                             d, d, d, i, P, i, P, i]
             _lib = L
     return _lib
 
@@ -189,24 +189,25 @@ def expert_fc2(a, e, w2, s2, g2, fmt) -> np.ndarray:
 
 
 def expert_ffn(x_row, e, w1, s1, g1, w2, s2, g2, fmt, alpha=1.0, beta=0.0,
-               limit=float("inf")) -> np.ndarray:
+               limit=float("inf"), fusion=1) -> np.ndarray:
     x_row = _c(x_row, np.uint16)
     w1, s1, g1 = _c(w1, np.uint8), _c(s1, np.uint8), _c(g1, np.float32)
     w2, s2, g2 = _c(w2, np.uint8), _c(s2, np.uint8), _c(g2, np.float32)
     H, I = w1.shape[1], w1.shape[2]
     y = np.empty(H, np.float64)
     _check(lib().oracle_expert_ffn(_ptr(x_row), e, _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2),
-                                   _ptr(s2), _ptr(g2), fmt, H, I, alpha, beta, limit,
+                                   _ptr(s2), _ptr(g2), fmt, H, I, alpha, beta, limit, fusion,
                                    _ptr(y)), "expert_ffn")
     return y
 
 
 def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt, k, normalize=1, alpha=1.0,
-                beta=0.0, limit=float("inf"), tokens=None, nthreads=None) -> np.ndarray:
+                beta=0.0, limit=float("inf"), tokens=None, nthreads=None, fusion=1) -> np.ndarray:
     """The whole layer.  x bf16 bits [T,H], logits f32 [T,E], fc1 packed
     [E,H,I] + scales [E,2I,H/bs] + global [E]/None, fc2 packed [E,I,H/2] +
-    scales [E,H,I/bs] + global [E]/None.  Returns bf16 bits [len(tokens),H]
-    (all T tokens when ``tokens`` is None)."""
+    scales [E,H,I/bs] + global [E]/None.  ``fusion`` is swiglu_fusion: FC1's
+    gate/linear columns interleaved (1, and 0 read as 1) or concatenated (2).
+    Returns bf16 bits [len(tokens),H] (all T tokens when ``tokens`` is None)."""
     x, logits = _c(x, np.uint16), _c(logits, np.float32)
     w1, s1, g1 = _c(w1, np.uint8), _c(s1, np.uint8), _c(g1, np.float32)
     w2, s2, g2 = _c(w2, np.uint8), _c(s2, np.uint8), _c(g2, np.float32)
@@ -218,6 +219,6 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt, k, normalize=1, alpha=1.
     nth = nthreads if nthreads else (os.cpu_count() or 1)
     _check(lib().oracle_moe_forward(_ptr(x), _ptr(logits), _ptr(w1), _ptr(s1), _ptr(g1),
                                     _ptr(w2), _ptr(s2), _ptr(g2), fmt, T, H, I, E, k,
-                                    normalize, alpha, beta, limit, _ptr(tok), ntok,
+                                    normalize, alpha, beta, limit, fusion, _ptr(tok), ntok,
                                     _ptr(out), nth), "moe_forward")
     return out

@@ -35,7 +35,11 @@
  *  - routing weights: softmax over all E experts, then (normalize != 0) divided
  *    by their sum over the k selected experts;
  *  - expanded index i = t*k + j; rows of one expert keep ascending i;
- *  - FC1 columns 2m (gate) and 2m+1 (linear) are interleaved (swiglu_fusion=1);
+ *  - FC1 columns: swiglu_fusion=1 interleaves them, 2m = gate and 2m+1 =
+ *    linear; swiglu_fusion=2 concatenates them, m = gate and I+m = linear
+ *    (the fc1 (gate) / fc3 (value) concatenation of the SwiGLU fusion
+ *    section); swiglu_fusion=0 is read as 1, the pages' backward-compatibility
+ *    remap for QMoE;
  *  - the FC1 activation a is rounded to bf16, y and the weighted sum stay wide,
  *    the layer output is rounded to bf16.
  */
@@ -281,21 +285,26 @@ int oracle_expert_fc2(const double *a, int e, const uint8_t *w2, const uint8_t *
     return ORACLE_OK;
 }
 
-/* y = FFN_e(x): FC1, SwiGLU on the interleaved (gate, linear) pairs with the
- * result rounded to bf16, then FC2. */
+/* y = FFN_e(x): FC1, SwiGLU on the (gate, linear) pairs of the FC1 columns
+ * (interleaved for swiglu_fusion 0 and 1, concatenated for 2) with the result
+ * rounded to bf16, then FC2. */
 int oracle_expert_ffn(const uint16_t *x_row, int e,
                       const uint8_t *w1, const uint8_t *s1, const float *g1,
                       const uint8_t *w2, const uint8_t *s2, const float *g2,
                       int fmt, int H, int I, double alpha, double beta, double limit,
-                      double *y) {
+                      int fusion, double *y) {
     int m;
-    double *h = (double *)malloc(sizeof(double) * 2 * (size_t)I);
-    double *a = (double *)malloc(sizeof(double) * (size_t)I);
+    double *h, *a;
+    if (fusion < 0 || fusion > 2) return ORACLE_BAD_ARG;
+    h = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+    a = (double *)malloc(sizeof(double) * (size_t)I);
     if (!h || !a) { free(h); free(a); return ORACLE_BAD_ARG; }
     oracle_expert_fc1(x_row, e, w1, s1, g1, fmt, H, I, h);
-    for (m = 0; m < I; ++m)
-        a[m] = oracle_bf16_to_double(
-            oracle_bf16_rne(oracle_swiglu(h[2 * m], h[2 * m + 1], alpha, beta, limit)));
+    for (m = 0; m < I; ++m) {
+        const double gate = fusion == 2 ? h[m] : h[2 * m];
+        const double lin = fusion == 2 ? h[I + m] : h[2 * m + 1];
+        a[m] = oracle_bf16_to_double(oracle_bf16_rne(oracle_swiglu(gate, lin, alpha, beta, limit)));
+    }
     oracle_expert_fc2(a, e, w2, s2, g2, fmt, H, I, y);
     free(h);
     free(a);
@@ -312,13 +321,14 @@ int oracle_moe_forward(const uint16_t *x, const float *logits,
                        const uint8_t *w1, const uint8_t *s1, const float *g1,
                        const uint8_t *w2, const uint8_t *s2, const float *g2,
                        int fmt, int T, int H, int I, int E, int k, int normalize,
-                       double alpha, double beta, double limit,
+                       double alpha, double beta, double limit, int fusion,
                        const int32_t *tokens, int ntok, uint16_t *out, int nthreads) {
     int r, npairs, pidx, status = ORACLE_OK;
     int32_t *ids;
     double *wts, *y;
     if (!x || !logits || !w1 || !s1 || !w2 || !s2 || !out) return ORACLE_BAD_ARG;
     if (fmt != ORACLE_NVFP4 && fmt != ORACLE_MXFP4) return ORACLE_BAD_ARG;
+    if (fusion < 0 || fusion > 2) return ORACLE_BAD_ARG;
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORACLE_BAD_ARG;
     if (H % block_size(fmt) || I % block_size(fmt) || (H & 1)) return ORACLE_BAD_ARG;
     if (!tokens) ntok = T;
@@ -336,7 +346,7 @@ int oracle_moe_forward(const uint16_t *x, const float *logits,
         int rr = pidx / k, j = pidx % k;
         int t = tokens ? tokens[rr] : rr;
         oracle_expert_ffn(x + (size_t)t * H, ids[t * k + j], w1, s1, g1, w2, s2, g2,
-                          fmt, H, I, alpha, beta, limit, y + (size_t)pidx * H);
+                          fmt, H, I, alpha, beta, limit, fusion, y + (size_t)pidx * H);
     }
     for (r = 0; r < ntok; ++r) {
         int t = tokens ? tokens[r] : r, j, hh;

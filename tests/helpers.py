@@ -39,3 +39,22 @@ def row_rel_l2(got_bits, ref_bits):
 
 # The layer output bar: row-L2-normalised relative error with fp32 accumulation.
 OUTPUT_RTOL = 1e-2
+
+
+def concatenated_fc1(w1, s1, kmajor=False):
+    """FC1 weights and block scales with interleaved gate/linear columns
+    (2m, 2m + 1) rewritten in the concatenated order (m, I + m) of
+    swiglu_fusion = 2: column c of the result is column 2c (c < I) or
+    2(c - I) + 1 of the input.  w1 packed [E, H, I] (low nibble = even
+    column), s1 [E, 2I, H/bs] ([E, H/bs, 2I] when kmajor)."""
+    w1 = np.asarray(w1, np.uint8)
+    E, H, half = w1.shape
+    codes = np.empty((E, H, 2 * half), np.uint8)
+    codes[..., 0::2] = w1 & 0xF
+    codes[..., 1::2] = w1 >> 4
+    perm = np.concatenate([np.arange(0, 2 * half, 2), np.arange(1, 2 * half, 2)])
+    c2 = codes[..., perm]
+    w1c = (c2[..., 0::2] | (c2[..., 1::2] << 4)).astype(np.uint8)
+    s1 = np.asarray(s1, np.uint8)
+    s1c = s1[:, :, perm] if kmajor else s1[:, perm, :]
+    return np.ascontiguousarray(w1c), np.ascontiguousarray(s1c)

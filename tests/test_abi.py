@@ -70,7 +70,10 @@ def test_forward_validation(qm):
     assert _fwd(L, T=0)[0] == 1
     assert _fwd(L, logits=None)[0] == 1
     assert _fwd(L, H=2000)[0] == 3                                # H % 64
-    assert _fwd(L, fusion=2)[0] == 3                              # concatenated SwiGLU
+    assert _fwd(L, fusion=3)[0] == 3                              # no such SwiGLU layout
+    assert _fwd(L, fusion=-1)[0] == 3
+    assert _fwd(L, fusion=2) == (0, need)                         # concatenated: same workspace
+    assert _fwd(L, fusion=0) == (0, need)                         # read as interleaved
     assert _fwd(L, fmt=2)[0] == 3
     assert _fwd(L, alpha=float("nan"))[0] == 1
     ws = ctypes.c_void_p(1 << 20)

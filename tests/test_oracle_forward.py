@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import synthetic as syn
+from helpers import concatenated_fc1
 
 NV, MX = 0, 1
 
@@ -22,7 +23,7 @@ def _bf16_round(a):
     return torch.from_numpy(np.asarray(a, np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def _dense_layer(oracle, L, wl):
+def _dense_layer(oracle, L, wl, fusion=1):
     x = torch.from_numpy(_f(L["x"]))
     W1 = torch.from_numpy(_f(oracle.dequant(L["w1"], L["s1"], L["g1"], wl.fmt)))  # [E,2I,H]
     W2 = torch.from_numpy(_f(oracle.dequant(L["w2"], L["s2"], L["g2"], wl.fmt)))  # [E,H,I]
@@ -39,7 +40,10 @@ def _dense_layer(oracle, L, wl):
             p = [v / s for v in p]
         for j, e in enumerate(order):
             h = W1[e] @ x[t]
-            gate, lin = h[0::2].numpy(), h[1::2].numpy()
+            if fusion == 2:
+                gate, lin = h[: wl.I].numpy(), h[wl.I:].numpy()
+            else:
+                gate, lin = h[0::2].numpy(), h[1::2].numpy()
             act = np.array([oracle.swiglu(a, b, wl.alpha, wl.beta, wl.limit)
                             for a, b in zip(gate, lin)])
             a = torch.from_numpy(_bf16_round(act))
@@ -117,3 +121,61 @@ def test_output_is_weighted_sum_of_expert_outputs(oracle):
     out = oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"],
                              L["s2"], L["g2"], MX, 3)
     assert np.array_equal(out[0], np.array([oracle.bf16_rne(v) for v in acc], np.uint16))
+
+
+# ---- swiglu_fusion: concatenated (2) and the remapped 0 ---------------------------
+
+@pytest.mark.parametrize("wl", CASES[:4], ids=lambda w: w.name)
+def test_concatenated_swiglu_matches_dense_brute_force(oracle, wl):
+    """swiglu_fusion = 2 pairs column m (gate) with column I + m (linear)."""
+    L = syn.layer(wl, seed=21)
+    w1c, s1c = concatenated_fc1(L["w1"], L["s1"])
+    Lc = dict(L, w1=w1c, s1=s1c)
+    ref = _dense_layer(oracle, Lc, wl, fusion=2)
+    got = _f(oracle.moe_forward(Lc["x"], Lc["logits"], Lc["w1"], Lc["s1"], Lc["g1"], Lc["w2"], Lc["s2"],
+                                Lc["g2"], wl.fmt, wl.k, wl.normalize, wl.alpha, wl.beta, wl.limit,
+                                fusion=2))
+    np.testing.assert_allclose(got, ref, rtol=2 ** -7, atol=1e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_concatenated_layout_is_a_column_permutation(oracle, wl):
+    """The same weights, columns rewritten from interleaved to concatenated
+    order, give the identical layer (every FC1 dot product is the same)."""
+    L = syn.layer(wl, seed=22)
+    args = (L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], wl.fmt, wl.k,
+            wl.normalize, wl.alpha, wl.beta, wl.limit)
+    w1c, s1c = concatenated_fc1(L["w1"], L["s1"])
+    interleaved = oracle.moe_forward(*args)
+    concatenated = oracle.moe_forward(L["x"], L["logits"], w1c, s1c, *args[4:], fusion=2)
+    assert np.array_equal(interleaved, concatenated)
+    # read the other way round, the layouts differ (the pin is not vacuous)
+    assert not np.array_equal(interleaved, oracle.moe_forward(*args, fusion=2))
+
+
+def test_fusion_zero_reads_as_interleaved(oracle):
+    wl = CASES[0]
+    L = syn.layer(wl, seed=23)
+    args = (L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], wl.fmt, wl.k)
+    assert np.array_equal(oracle.moe_forward(*args, fusion=0), oracle.moe_forward(*args, fusion=1))
+    with pytest.raises(Exception):
+        oracle.moe_forward(*args, fusion=3)
+
+
+def test_concatenated_fc1_helper_moves_columns():
+    """The test helper itself: one nonzero code per column lands where the
+    concatenated order puts it, and the scales move with it."""
+    E, H, I = 1, 2, 4
+    w1 = np.zeros((E, H, I), np.uint8)
+    s1 = np.zeros((E, 2 * I, 1), np.uint8)
+    for n in range(2 * I):
+        k = n % H
+        w1[0, k, n // 2] |= np.uint8((n + 1) << (4 * (n % 2)))
+        s1[0, n, 0] = n + 100
+    w1c, s1c = concatenated_fc1(w1, s1)
+    for c in range(2 * I):
+        src = 2 * c if c < I else 2 * (c - I) + 1
+        assert s1c[0, c, 0] == src + 100
+        for k in range(H):
+            code = (int(w1c[0, k, c // 2]) >> (4 * (c % 2))) & 0xF
+            assert code == ((src + 1) if src % H == k else 0)
