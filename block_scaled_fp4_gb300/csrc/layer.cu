@@ -914,11 +914,12 @@ template <int FMT, int RC, int KN>
 __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const LayerPlan &L, const PassCtx &C,
                                          unsigned char *ring, uint8_t *win, const uint8_t *stage, __half *xw,
                                          unsigned char *xraw, uint32_t &it, uint32_t &wn, uint32_t &xn,
-                                         int &pre_off) {
+                                         int &pre_off, uint32_t &slot, uint32_t &phase) {
   const FcPlan &P = L.f[C.f];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int wpw = 32 / P.RGS;
-  const int rg = lane / wpw, wl = lane - rg * wpw;
+  // RGS is a power of two: the lane geometry by shifts, no division
+  const int lg_rgs = __ffs(P.RGS) - 1, wpw = 32 >> lg_rgs, lg_wpw = 5 - lg_rgs;
+  const int rg = lane >> lg_wpw, wl = lane & (wpw - 1);
   const int w = warp * wpw + wl;
   const bool active = w < P.NW;
   const int row_bytes = P.NT / 2;
@@ -932,12 +933,12 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
 #pragma unroll
   for (int r = 0; r < RC; ++r) sh[r] = 0;
   const int unit_k = 16 * P.RGS;
-  const int xw_units = kXsK / unit_k;
+  const int xw_units = kXsK / 16 >> lg_rgs;  // kXsK / unit_k
   int cur_wid = -1;
   uint32_t ws = 0;
-  // ring position of the pass's first unit; advanced without division
+  // ring position (slot, phase) of the pass's first unit: carried from pass
+  // to pass by the caller and advanced without division
   const uint32_t ring_n = (uint32_t)L.ring;
-  uint32_t slot = it % ring_n, phase = (it / ring_n) & 1u;
   // k-major scales: this lane's 8 scale bytes sit at a fixed offset in every slot
   const int sc_lane = P.sc_off + ((rg * 16) / BS) * P.NT + 8 * w;
   for (int xj = C.j0; xj < C.j1; xj += xw_units) {
@@ -1082,6 +1083,7 @@ template <int FMT, int KN>
 __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const LayerPlan &L, unsigned char *ring,
                                       uint8_t *win, const uint8_t *stage, __half *xs, unsigned char *xraw) {
   uint32_t it = 0, wn = 0, xn = 0;
+  uint32_t slot = 0, phase = 0;  // ring position of unit `it` (k-major path)
   __half *xw = xs + (size_t)(threadIdx.x >> 5) * (kXwBytes / 2);  // this warp's activation window
   int pre_off = 0;
   for (int f = 0; f < 2; ++f) {
@@ -1106,7 +1108,7 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const Layer
       for (int c0 = 0; c0 < C.sd.z; c0 += kRowsMax) {
         C.c0 = c0;
         C.rows = min(kRowsMax, C.sd.z - c0);
-        run_pass<FMT, kRowsMax, KN>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off);
+        run_pass<FMT, kRowsMax, KN>(S, g, L, C, ring, win, stage, xw, xraw, it, wn, xn, pre_off, slot, phase);
       }
     }
   }
