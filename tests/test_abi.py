@@ -132,3 +132,19 @@ def test_primed_flag_is_a_format_flag_only_for_the_forward_calls(qm):
     assert base == qm.forward_workspace_bytes(4, 2048, 512, 256, 8,
                                               qm.NVFP4 | qm.SCALES_KMAJOR | qm.WORKSPACE_PRIMED)
     assert base >= qm.WORKSPACE_HEADER_BYTES
+
+
+def test_plan_accepts_every_supported_decode_shape(qm):
+    """The decode plan (column tiling, ring, work-split bounds) exists for every
+    shape inside the documented gate: H and I multiples of 64 up to 16384,
+    1 <= k <= min(8, E), E <= 256, T * k <= 64, both formats and scale layouts
+    (a size query: host logic only, nothing is launched)."""
+    shapes = [(1, 8, 2), (4, 256, 8), (8, 256, 8), (64, 8, 1), (64, 64, 1), (16, 32, 4), (32, 2, 2),
+              (1, 1, 1), (21, 3, 3)]
+    dims = (64, 128, 192, 320, 1024, 2048, 2880, 4096, 7168, 16384)
+    for fmt in (qm.NVFP4, qm.MXFP4, qm.NVFP4 | qm.SCALES_KMAJOR, qm.MXFP4 | qm.SCALES_KMAJOR):
+        for H in dims:
+            for I in dims:
+                for T, E, k in shapes:
+                    assert T * k <= qm.GEMV_MAX_ROWS
+                    assert qm.forward_workspace_bytes(T, H, I, E, k, fmt) > 0, (fmt, H, I, T, E, k)
