@@ -9,8 +9,9 @@
 // instead of to every weight, fp32 accumulation for bf16 activations, and a
 // 64-expanded-row window.  Design here (sm_103a, one CTA per SM):
 //  * every CTA routes the (at most 64) expanded rows itself with the routing
-//    kernel's warp top-k and ranking code, so all CTAs hold identical maps
-//    and no separate launch sits between the call and the weight stream;
+//    kernel's warp top-k and a one-warp stable ranking, so all CTAs hold
+//    identical maps and no separate launch sits between the call and the
+//    weight stream;
 //  * work unit = 16*RGS k rows x NT columns of one active expert's weights
 //    (about 32 KB).  The units of all active experts are laid end to end
 //    (expert slot, column tile, k) and split over the CTAs by cost

@@ -2,14 +2,13 @@
 //
 // "[CUDA] Cut the MoE routing prologue/epilogue cost for small-batch decode"
 // (PR #31156) describes the design idea kept here: one token row per warp held
-// entirely in registers, each lane bitonic-sorts its own keys, then the warp
-// runs a butterfly of bitonic top-N merges where the merge rule
-// C[i] = max(A[i], B[N-1-i]) is symmetric, so one shuffle per key leaves both
-// partners with the same result (no shared memory, no barrier); and expert
-// ranking with warp ballots/matches instead of per-thread radix counters.
-// Ties are broken by a packed stable key: fp32 logit (order-preserving bits,
-// -0.0 folded onto +0.0) in the high word, (0xFFFF - expert) in the low word,
-// so a larger key means a larger logit, then a lower expert index.
+// entirely in registers (no shared memory, no block sort), and expert ranking
+// with warp matches instead of per-thread radix counters.  The warp top-k
+// (route_common.cuh) sorts each lane's keys and takes the k largest with k
+// rounds of a warp maximum.  Ties are broken by a packed stable key: fp32
+// logit (order-preserving bits, -0.0 folded onto +0.0) in the high word,
+// (0xFFFF - expert) in the low word, so a larger key means a larger logit,
+// then a lower expert index.
 #include "route_common.cuh"
 
 namespace qmoe {
