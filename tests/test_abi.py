@@ -6,6 +6,7 @@ import math
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -148,3 +149,25 @@ def test_plan_accepts_every_supported_decode_shape(qm):
                 for T, E, k in shapes:
                     assert T * k <= qm.GEMV_MAX_ROWS
                     assert qm.forward_workspace_bytes(T, H, I, E, k, fmt) > 0, (fmt, H, I, T, E, k)
+
+
+def test_binding_has_no_cpu_fallback(qm):
+    """The Python binding refuses host tensors instead of computing anything
+    on the CPU, for every compute entry point."""
+    import torch
+    import synthetic as syn
+    wl = syn.small("cpu", T=2, E=4, k=2, H=64, I=64)
+    L = syn.layer(wl, seed=1)
+    t = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v))) for k, v in L.items()}
+    x = t["x"].view(torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qm.moe_forward(x, t["logits"], t["w1"], t["s1"], t["g1"], t["w2"], t["s2"], t["g2"], wl.fmt, wl.k)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qm.moe_forward_no_alloc(x, t["logits"], t["w1"], t["s1"], t["g1"], t["w2"], t["s2"], t["g2"],
+                                wl.fmt, wl.k)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qm.route_topk(t["logits"], wl.k)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qm.dequant(t["w1"], t["s1"], t["g1"], wl.fmt)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qm.scales_kmajor(t["s1"], wl.fmt)
