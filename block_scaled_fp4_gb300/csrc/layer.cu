@@ -30,8 +30,8 @@
 //    k-group rg (16 rows) of a unit, decodes with the hardware
 //    cvt.rn.f16x2.e2m1x2 and multiplies with fma.rn.f32.f16 (fp16 operands,
 //    exact product, fp32 accumulator); the 16-row partial is multiplied once
-//    by its block scale (NVFP4 scales used as E4M3 * 2^-120, bits moved into
-//    fp32 position, exact; the 2^120 applied at the end);
+//    by its block scale (NVFP4: the E4M3 value from the hardware conversion
+//    cvt.rn.f16x2.e4m3x2, exact; MXFP4: 2^(b-127) by bit placement);
 //  * activations are staged in fp16 after an exact power-of-two rescale per
 //    row (largest |x| in [2^14, 2^15)), so every finite bf16 activation is
 //    exact in fp16; the rescale is undone on the fp32 partial;
@@ -155,8 +155,10 @@ __device__ __forceinline__ int ld_acquire(const int32_t *p) {
 
 // ---- scales and activation helpers -----------------------------------------------
 
-// Raw block scale as fp32.  NVFP4: E4M3 value * 2^-120 (exact); MXFP4: 2^(b-127).
-// `special` is set for codes that need the exact slow path (NaN; E8M0 0 / 255).
+// Raw block scale as fp32 (MXFP4 block scales; NVFP4 ones go through the
+// hardware E4M3 conversion).  NVFP4: E4M3 value * 2^-120 (exact); MXFP4:
+// 2^(b-127).  `special` is set for codes that need the exact slow path (NaN;
+// E8M0 0 / 255).
 template <int FMT>
 __device__ __forceinline__ float raw_scale(uint32_t b, bool &special) {
   if (FMT == QMOE_NVFP4) {
@@ -310,6 +312,7 @@ __device__ __forceinline__ int busy_ctas(const Shared &S, int f, int c0, int c1)
 }
 
 __device__ __forceinline__ bool wait_bar(Shared &S, const LayerArgs &g, uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;  // the usual case: no abort-flag read
   const uint32_t limit = *(volatile int *)&S.abort ? 64u : kWaitLimit;
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -670,9 +673,28 @@ __device__ __forceinline__ void fma16(const uint32_t (&p)[4], const uint32_t (&q
       : "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3]), "r"(x2));
 }
 
-// The 8 block scales of a thread's column word.
+// Two E4M3 bytes (low 16 bits) -> f16x2, exact (every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(r) : "r"(two));
+  return r;
+}
+
+// The 8 block scales of a thread's column word.  NVFP4: the E4M3 values
+// themselves (hardware conversion, NaN codes give NaN); MXFP4: 2^(b-127).
 template <int FMT>
 __device__ __forceinline__ void block_scales8(uint2 sv, float (&sc)[8]) {
+  if constexpr (FMT == QMOE_NVFP4) {
+    const uint32_t h[4] = {e4m3x2_to_f16x2(sv.x & 0xFFFFu), e4m3x2_to_f16x2(sv.x >> 16),
+                           e4m3x2_to_f16x2(sv.y & 0xFFFFu), e4m3x2_to_f16x2(sv.y >> 16)};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 v = *reinterpret_cast<const __half2 *>(&h[q]);
+      sc[2 * q] = __low2float(v);
+      sc[2 * q + 1] = __high2float(v);
+    }
+    return;
+  }
   bool special = false;
 #pragma unroll
   for (int c = 0; c < 8; ++c) sc[c] = raw_scale<FMT>(((c < 4 ? sv.x : sv.y) >> (8 * (c & 3))) & 0xFFu, special);
@@ -1016,16 +1038,15 @@ __device__ __forceinline__ void run_pass(Shared &S, const LayerArgs &g, const La
   wait_bar(S, g, &S.basesready, 0u);
   float *dst = (C.f == 0 ? g.p1 : g.p2) + S.seg[C.f][C.si].dst;
   if (active && rg == 0) {
-    const float fold = FMT == QMOE_NVFP4 ? 0x1p120f : 1.0f;
 #pragma unroll
     for (int r = 0; r < RC; ++r) {
       if (r < C.rows) {
-        // fold first: sum * 2^120 is near the rescaled row's magnitude, so
-        // undoing the 2^-shift afterwards cannot underflow
+        // the sum is near the rescaled row's magnitude (the block scales
+        // enter at their own value), so undoing the 2^-shift cannot underflow
         const float un = pow2f(sh[r]);
         float4 *d = reinterpret_cast<float4 *>(dst + (size_t)(C.c0 + r) * P.NT + 8 * w);
-        d[0] = make_float4(acc[r][0] * fold * un, acc[r][1] * fold * un, acc[r][2] * fold * un, acc[r][3] * fold * un);
-        d[1] = make_float4(acc[r][4] * fold * un, acc[r][5] * fold * un, acc[r][6] * fold * un, acc[r][7] * fold * un);
+        d[0] = make_float4(acc[r][0] * un, acc[r][1] * un, acc[r][2] * un, acc[r][3] * un);
+        d[1] = make_float4(acc[r][4] * un, acc[r][5] * un, acc[r][6] * un, acc[r][7] * un);
       }
     }
   }
