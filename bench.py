@@ -153,34 +153,40 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
-def make_layers(n_layers: int, seed: int, device):
-    """Seeded synthetic layers of the decode workload, generated on the GPU
-    (weights) and with the shared host generator (activations, logits)."""
+def make_layers(n_layers: int, seed: int, device, workload: str = WORKLOAD):
+    """Seeded synthetic layers of a decode workload, generated on the GPU
+    (weights, with the workload's distributions) and with the shared host
+    generator (activations, logits)."""
     import numpy as np
     import torch
     import synthetic as syn
-    wl = syn.WORKLOADS[WORKLOAD]
+    wl = syn.WORKLOADS[workload]
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     layers = []
     E, H, I = wl.E, wl.H, wl.I
+    bs = 16 if wl.fmt == 0 else 32
 
-    def e4m3_codes(shape):
-        idx = torch.randint(0, 32, shape, generator=gen, device=device, dtype=torch.int32)
-        return (((idx // 8) + 5) << 3 | (idx % 8)).to(torch.uint8)
+    def scales(shape):
+        if wl.fmt == 0:  # E4M3 codes with value in [0.25, 4): exponent field 5..8, any mantissa
+            idx = torch.randint(0, 32, shape, generator=gen, device=device, dtype=torch.int32)
+            return (((idx // 8) + 5) << 3 | (idx % 8)).to(torch.uint8)
+        return torch.randint(120, 135, shape, generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
 
     def gscale():
+        if wl.fmt != 0:
+            return None
         u = torch.randint(0, 5, (E,), generator=gen, device=device, dtype=torch.int32)
         return torch.ldexp(torch.ones(E, device=device), -u.float()).float()
 
     for li in range(n_layers):
         rng = syn.rng_for(seed, 100 + li)
         x = torch.from_numpy(syn.activations(rng, wl.T, H).view(np.int16)).to(device).view(torch.bfloat16)
-        lg = torch.from_numpy(syn.logits(rng, wl.T, E, wl.logit_std)).to(device)
+        lg = torch.from_numpy(syn.logits(rng, wl.T, E, wl.logit_std, wl.ties, wl.k)).to(device)
         w1 = torch.randint(0, 256, (E, H, I), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
         w2 = torch.randint(0, 256, (E, I, H // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
-        layers.append(dict(x=x, logits=lg, w1=w1, s1=e4m3_codes((E, 2 * I, H // 16)), g1=gscale(),
-                           w2=w2, s2=e4m3_codes((E, H, I // 16)), g2=gscale()))
+        layers.append(dict(x=x, logits=lg, w1=w1, s1=scales((E, 2 * I, H // bs)), g1=gscale(),
+                           w2=w2, s2=scales((E, H, I // bs)), g2=gscale()))
     return wl, layers
 
 
@@ -370,7 +376,11 @@ def run_gpu(args):
             "clocks": clocks.summary(t_host0, t_host1),
             "cpu_baseline": cpu,
             "dequant": bench_dequant(device, peak) if not args.no_dequant else None,
+            "dequant_fc2": (bench_dequant(device, peak, K=1536, N=2048, what="prefill FC2 weights")
+                            if not args.no_dequant else None),
             "prefill": bench_prefill(device, peak) if not args.no_prefill else None,
+            "routing": bench_routing(device) if not args.no_configs else None,
+            "configs": bench_configs(args, device, peak) if not args.no_configs else None,
         }
     if world > 1:
         import torch.distributed as dist
@@ -378,16 +388,157 @@ def run_gpu(args):
     return res
 
 
-# ---------------------------------------------------------------- prefill dequant
+# ---------------------------------------------------------------- other decode configs
 
-def bench_dequant(device, peak: float, reps: int = 10) -> dict:
-    """The prefill FP4 -> bf16 dequantisation on the NVFP4 prefill shape's FC1
-    weights (E=128, K=2048, N=3072): 384 MiB codes + 48 MiB scales read,
-    1.5 GiB bf16 written per launch (far above L2).  Event-timed on the
-    launching stream, after warm-up."""
+DECODE_CONFIGS = {
+    # workload: (distinct layers per replay, why that many)
+    "tiny_nvfp4_decode": (40, "0.44 MB of weights per layer: L2-resident whatever the rotation (launch-bound)"),
+    "mxfp4_decode": (8, "8 distinct layers, 3.4 GB of weights per replay (> L2)"),
+    "nvfp4_verify_edge": (4, "4 distinct layers, 13.8 GB of weights per replay (> L2)"),
+}
+
+
+def bench_decode(device, workload: str, n_layers: int, steps: int, peak: float, kmajor: bool = True,
+                 cpu_tokens=None) -> dict:
+    """One decode workload: n_layers distinct layers replayed as one CUDA graph
+    (primed workspace), microseconds per layer, the algorithmic bytes of the
+    experts the seeded routing activates, and the fraction of the measured HBM
+    bandwidth; plus the oracle's host-core time on a bounded sample."""
     import torch
     import block_scaled_fp4_gb300 as q
-    E, K, N = 128, 2048, 3072
+    wl, layers = make_layers(n_layers, seed=4321, device=device, workload=workload)
+    fmt = wl.fmt
+    if kmajor:
+        for L in layers:
+            L["s1"] = q.scales_kmajor(L["s1"], wl.fmt)
+            L["s2"] = q.scales_kmajor(L["s2"], wl.fmt)
+        fmt |= q.SCALES_KMAJOR
+    fmt |= q.WORKSPACE_PRIMED
+    ws = torch.zeros(q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, fmt), dtype=torch.uint8,
+                     device=device)
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
+    ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=device) for _ in layers]
+    stream = torch.cuda.Stream(device=device)
+
+    def step():
+        for i, L in enumerate(layers):
+            q.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], fmt, wl.k,
+                          wl.normalize, wl.alpha, wl.beta, wl.limit, out=outs[i], topk_ids=ids[i], workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    q.check_device_error(ws)
+    us = e0.elapsed_time(e1) * 1e3 / (steps * len(layers))
+    fc1_b, fc2_b = per_expert_bytes(wl)
+    act = [len(set(i.cpu().numpy().reshape(-1).tolist())) for i in ids]
+    alg = sum(a * (fc1_b + fc2_b) + 2 * wl.T * wl.H * 2 for a in act) / len(act)
+    gbs = alg / (us * 1e-6) / 1e9
+    res = {"workload": f"{workload}: T={wl.T} E={wl.E} k={wl.k} H={wl.H} I={wl.I} "
+                       f"{'NVFP4' if wl.fmt == 0 else 'MXFP4'} SwiGLU",
+           "us_per_layer": round(us, 3), "alg_bytes_per_layer": int(alg),
+           "mean_active_experts": sum(act) / len(act), "achieved_gbs": round(gbs, 1), "peak": peak,
+           "frac": round(gbs / peak, 4), "layers_per_replay": len(layers), "replays": steps,
+           "scale_layout": "k-major" if kmajor else "[E, N, K/bs] as stored"}
+    del layers, ws, graph
+    torch.cuda.empty_cache()
+    if cpu_tokens is not None:
+        res["cpu_oracle"] = cpu_oracle_sample(workload, cpu_tokens)
+    return res
+
+
+def cpu_oracle_sample(workload: str, tokens) -> dict:
+    """The fp64 oracle on the host cores for `tokens` of one layer, scaled to
+    microseconds per whole layer (time x T / tokens)."""
+    import numpy as np
+    import oracle
+    import synthetic as syn
+    wl = syn.WORKLOADS[workload]
+    oracle.build()
+    cores = os.cpu_count() or 1
+    L = syn.layer(wl, seed=0)
+    tok = np.asarray(tokens, np.int32)
+    t0 = time.perf_counter()
+    oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], wl.fmt, wl.k,
+                       wl.normalize, wl.alpha, wl.beta, wl.limit, tokens=tok, nthreads=cores)
+    sec = time.perf_counter() - t0
+    return {"value": round(sec * 1e6 * wl.T / len(tok), 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(tok)} of {wl.T} tokens of one layer, scaled to the whole layer"}
+
+
+def bench_routing(device, reps: int = 200) -> dict:
+    """qmoe_route_topk alone on the MTP decode shape (4 tokens, 256 experts,
+    top-8): 40 calls on distinct logits replayed as one CUDA graph."""
+    import torch
+    import block_scaled_fp4_gb300 as q
+    import synthetic as syn
+    wl = syn.WORKLOADS[WORKLOAD]
+    lg = [torch.from_numpy(syn.logits(syn.rng_for(7, i), wl.T, wl.E, wl.logit_std)).to(device) for i in range(40)]
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for x in lg:
+            q.route_topk(x, wl.k, wl.normalize, stream=stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for x in lg:
+            q.route_topk(x, wl.k, wl.normalize, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = max(1, reps // 40)
+        for _ in range(n):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (n * len(lg))
+    return {"kernel": "route_maps_fused_kernel (top-k softmax + permute maps, one launch)",
+            "workload": f"T={wl.T} E={wl.E} k={wl.k}", "us_per_call": round(us, 3), "bound": "latency",
+            "calls": n * len(lg)}
+
+
+def bench_configs(args, device, peak: float) -> dict:
+    """Every other decode workload, and the MTP decode workload with its block
+    scales in the stored [E, N, K/bs] layout."""
+    out = {}
+    cpu = not args.no_cpu_baseline
+    samples = {"tiny_nvfp4_decode": [0], "mxfp4_decode": [0], "nvfp4_verify_edge": [0]}
+    for name, (n_layers, why) in DECODE_CONFIGS.items():
+        r = bench_decode(device, name, n_layers, max(5, args.steps // 4), peak,
+                         cpu_tokens=samples[name] if cpu else None)
+        r["l2"] = why
+        out[name] = r
+    r = bench_decode(device, WORKLOAD, LAYERS, max(5, args.steps // 4), peak, kmajor=False)
+    r["l2"] = "40 distinct layers, 17.3 GB of weights per replay (> L2)"
+    out[WORKLOAD + " (page-layout scales)"] = r
+    return out
+
+
+# ---------------------------------------------------------------- prefill dequant
+
+def bench_dequant(device, peak: float, reps: int = 10, E: int = 128, K: int = 2048, N: int = 3072,
+                  what: str = "prefill FC1 weights") -> dict:
+    """The prefill FP4 -> bf16 dequantisation on one FC of the NVFP4 prefill
+    shape (FC1: E=128, K=2048, N=3072, 384 MiB codes + 48 MiB scales read,
+    1.5 GiB bf16 written; FC2: K=1536, N=2048), far above L2 per launch.
+    Event-timed on the launching stream, after warm-up."""
+    import torch
+    import block_scaled_fp4_gb300 as q
     gen = torch.Generator(device=device)
     gen.manual_seed(77)
     packed = torch.randint(0, 256, (E, K, N // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
@@ -412,7 +563,7 @@ def bench_dequant(device, peak: float, reps: int = 10) -> dict:
     gbs = alg / (med * 1e-6) / 1e9
     del packed, scales, out
     return {"kernel": "dequant_kernel<NVFP4> (FP4 -> bf16, [E,K,N/2] -> [E,N,K])",
-            "workload": f"E={E} K={K} N={N} NVFP4 (prefill FC1 weights)", "us": round(med, 2),
+            "workload": f"E={E} K={K} N={N} NVFP4 ({what})", "us": round(med, 2),
             "us_p10_p90": [round(us[max(0, len(us) // 10)], 2), round(us[min(len(us) - 1, 9 * len(us) // 10)], 2)],
             "bound": "hbm", "alg_bytes": alg, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(gbs / peak, 4), "launches": reps}
@@ -566,6 +717,8 @@ def main(argv=None):
                     help="reset the workspace header before every call (no programmatic dependent launch)")
     ap.add_argument("--no-dequant", action="store_true", help="skip the prefill dequant measurement")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill forward measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other decode workloads, the page-layout line and the routing line")
     ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],
                     help="block-scale layout the layer reads (default: k-major, prepared once at load)")
     args = ap.parse_args(argv)

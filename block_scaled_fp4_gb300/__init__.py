@@ -27,11 +27,13 @@ BLOCK = {NVFP4: 16, MXFP4: 32}
 GEMV_MAX_ROWS = 64
 
 STATUS = {0: "QMOE_OK", 1: "QMOE_ERR_INVALID_ARG", 2: "QMOE_ERR_MISALIGNED",
-          3: "QMOE_ERR_UNSUPPORTED", 4: "QMOE_ERR_WORKSPACE", 5: "QMOE_ERR_CUDA"}
+          3: "QMOE_ERR_UNSUPPORTED", 4: "QMOE_ERR_WORKSPACE", 5: "QMOE_ERR_CUDA",
+          6: "QMOE_ERR_DEVICE"}
 
 # Every symbol include/qmoe.h declares.
 EXPORTS = ("qmoe_route_topk", "qmoe_fp4_moe_forward", "qmoe_fp4_dequant", "qmoe_last_error",
-           "qmoe_set_stage_events", "qmoe_fp4_moe_forward_no_alloc", "qmoe_fp4_scales_kmajor")
+           "qmoe_set_stage_events", "qmoe_fp4_moe_forward_no_alloc", "qmoe_fp4_scales_kmajor",
+           "qmoe_check_device_error", "qmoe_binary_version")
 
 
 class QMoEError(RuntimeError):
@@ -72,6 +74,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             L.qmoe_last_error.argtypes = []
             L.qmoe_set_stage_events.restype = i
             L.qmoe_set_stage_events.argtypes = [P, i]
+            L.qmoe_check_device_error.restype = i
+            L.qmoe_check_device_error.argtypes = [P, P]
+            L.qmoe_binary_version.restype = i
+            L.qmoe_binary_version.argtypes = []
             L.qmoe_fp4_moe_forward_no_alloc.restype = i
             L.qmoe_fp4_moe_forward_no_alloc.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
                                                         f, f, f, P, P, P]
@@ -217,6 +223,21 @@ def scales_kmajor(scales, fmt: int, out=None, stream=None):
     return out
 
 
+def check_device_error(workspace=None, stream=None) -> None:
+    """Read and clear the device error flag of a forward workspace (``None``:
+    the no-alloc entry point's static scratch on the current device).  Raises
+    QMoEError (QMOE_ERR_DEVICE) when a bounded wait inside a kernel gave up
+    since the last check.  Synchronises the stream."""
+    _cuda(workspace, "workspace")
+    _check(load().qmoe_check_device_error(_ptr(workspace), _stream(stream)))
+
+
+def binary_version() -> int:
+    """Compute capability the library's decode kernel was built for, as the
+    runtime reports it on the current device (103 for sm_103a)."""
+    return int(load().qmoe_binary_version())
+
+
 def set_stage_events(events) -> int:
     """Record ``events[i]`` (torch.cuda.Event) around the forward's kernels;
     ``None`` switches it off.  Returns the number of kernels per decode call."""
@@ -234,4 +255,5 @@ _stage_keepalive = None
 
 __all__ = ["NVFP4", "MXFP4", "BLOCK", "GEMV_MAX_ROWS", "QMoEError", "build", "load", "library_path",
            "route_topk", "moe_forward", "moe_forward_no_alloc", "forward_workspace_bytes", "dequant",
-           "scales_kmajor", "SCALES_KMAJOR", "set_stage_events", "EXPORTS"]
+           "scales_kmajor", "SCALES_KMAJOR", "set_stage_events", "check_device_error", "binary_version",
+           "EXPORTS"]

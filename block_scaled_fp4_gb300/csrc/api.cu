@@ -1,6 +1,7 @@
 // The C ABI declared in include/qmoe.h: host-side validation, workspace
 // layout and kernel launches.  Every check runs before the first launch; an
 // invalid call launches nothing.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -19,16 +20,22 @@ void set_error(const char *fmt, ...) {
   va_end(ap);
 }
 
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
 int num_sms() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
-  if (cache[dev] == 0) {
-    int n = 0;
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 132;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 132;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 static cudaEvent_t *g_stage_events = nullptr;
@@ -178,6 +185,7 @@ namespace qmoe {
 // caller passes them), page-layout scales reconstituted from k-major ones
 // (only then), FC1 activations and FC2 rows in permuted order.
 struct PrefillLayout {
+  int32_t *meta;  // the header: word 1 is the device error flag (the counters are never written here)
   int32_t *ids, *offsets, *p2e, *e2p;
   float *weights, *y;
   uint16_t *w1d, *w2d, *act;
@@ -190,7 +198,7 @@ static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k,
   const size_t R = (size_t)T * k;
   Carve c(ws);
   PrefillLayout L{};
-  c.take<uint8_t>(QMOE_WORKSPACE_HEADER_BYTES);  // the decode kernel's header: never written here
+  L.meta = c.take<int32_t>(QMOE_WORKSPACE_HEADER_BYTES / sizeof(int32_t));
   L.ids = c.take<int32_t>(R);
   L.weights = c.take<float>(R);
   L.offsets = c.take<int32_t>((size_t)E + 1);
@@ -271,10 +279,33 @@ static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const
   a.alpha = alpha; a.beta = beta; a.limit = limit; a.fusion = fusion;
   a.x = x; a.offsets = L.offsets; a.p2e = L.p2e; a.e2p = L.e2p; a.weights = L.weights;
   a.w1d = w1d; a.w2d = w2d; a.act = L.act; a.y = L.y; a.out = out;
+  a.err_flag = L.meta + 1;
   return cuda_status(launch_prefill(a, stream), "prefill launch");
 }
 
 }  // namespace qmoe
+
+extern "C" qmoe_status qmoe_check_device_error(void *workspace, cudaStream_t stream) {
+  g_err[0] = 0;
+  void *ws = workspace;
+  if (!ws) {  // the static scratch of the no-alloc entry point on this device
+    const qmoe_status st = no_alloc_scratch(&ws);
+    if (st != QMOE_OK) return st;
+  }
+  QMOE_REQUIRE(aligned16(ws), QMOE_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  int32_t *flag_dev = static_cast<int32_t *>(ws) + 1;  // header word 1
+  int32_t flag = 0;
+  cudaError_t err = cudaMemcpyAsync(&flag, flag_dev, sizeof flag, cudaMemcpyDeviceToHost, stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return cuda_status(err, "reading the device error flag");
+  if (flag == 0) return QMOE_OK;
+  err = cudaMemsetAsync(flag_dev, 0, sizeof flag, stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return cuda_status(err, "clearing the device error flag");
+  set_error("a bounded wait inside a kernel gave up (device error flag %d): the outputs of the calls on this "
+            "workspace since the last check are not to be trusted", (int)flag);
+  return QMOE_ERR_DEVICE;
+}
 
 extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w,
                                             const uint8_t *fc1_s, const float *fc1_g, const uint8_t *fc2_w,

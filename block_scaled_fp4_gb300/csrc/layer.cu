@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "route_common.cuh"
 
@@ -509,15 +510,20 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   const int lane = (int)lane_id();
   const uint64_t pol = l2_evict_first_policy();
+  // a wait by lane 0, its outcome in every lane: false once a bounded wait gave
+  // up, after which this warp issues no further copy
+  auto wait_all_lanes = [&](uint64_t *bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(S, g, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+  };
+  // issue index of the last copy into each ring slot / window slot (drained before exit)
+  uint32_t last_it[kRingMax] = {~0u, ~0u, ~0u, ~0u}, last_wn[2] = {~0u, ~0u};
   // With [E, N, K/bs] scales the weight stream starts once the first scale
   // window (a tensor copy, in the same bulk-copy queue) is on its way: small
   // copies issued behind a GPU-wide burst of bulk copies wait for all of it.
   // With k-major scales every small copy goes through cp.async and the
   // weight stream starts at once.
-  if (ROLE == 0 && !L.f[0].kn) {
-    if (lane == 0) wait_bar(S, g, &S.smallfirst, 0u);
-    __syncwarp();
-  }
   bool first_done = ROLE == 0;
   // ROLE 1, once its first copies are issued: the global scales (needed after
   // the first grid barrier) and the partial-sum offsets (needed at the end of
@@ -544,6 +550,9 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
     first_done = true;
   };
   uint32_t it = 0, wn = 0, xn = 0;
+  if (ROLE == 0 && !L.f[0].kn) {
+    if (!wait_all_lanes(&S.smallfirst, 0u)) goto drain;
+  }
   for (int f = 0; f < 2; ++f) {
     const FcPlan &P = L.f[f];
     const uint8_t *wbase = f == 0 ? g.w1 : g.w2;
@@ -563,10 +572,7 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
             // FC1: the activation rows of this k window, ahead of its weights
             const int k0 = j * unit_k, len = min(P.K, min(sg.j1, j + xw_units) * unit_k) - k0;
             const int s = (int)(xn & 1u);
-            if (xn >= 2u) {
-              if (lane == 0) wait_bar(S, g, &S.xempty[s], ((xn >> 1) + 1u) & 1u);
-              __syncwarp();
-            }
+            if (xn >= 2u && !wait_all_lanes(&S.xempty[s], ((xn >> 1) + 1u) & 1u)) goto drain;
             // 16-byte pieces, all 32 lanes; each lane arrives once its own have landed
             const int cpr = len / 8;  // pieces per row
             for (int i = lane; i < rows_p * cpr; i += 32) {
@@ -581,10 +587,8 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
           const int wid = unit_window<FMT>(P, j);
           if (ROLE == 1 && P.tma && wid != cur) {
             const int s = (int)(wn & 1u);
-            if (wn >= 2u) {
-              if (lane == 0) wait_bar(S, g, &S.wempty[s], ((wn >> 1) + 1u) & 1u);
-              __syncwarp();
-            }
+            if (wn >= 2u && !wait_all_lanes(&S.wempty[s], ((wn >> 1) + 1u) & 1u)) goto drain;
+            last_wn[s] = wn;
             uint8_t *dst = stage + (size_t)s * L.win_bytes;
             // the barrier counts 32 arrivals (one per lane, as for the cp.async windows)
             if (lane == 0) mbar_expect_tx(&S.wfull[s], (uint32_t)(P.NT * kTmaWB));
@@ -601,10 +605,8 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
           }
           const uint32_t ring_n = (uint32_t)L.ring;
           const int s = (int)(it % ring_n);
-          if (it >= ring_n) {
-            if (lane == 0) wait_bar(S, g, &S.empty[s], ((it / ring_n) + 1u) & 1u);
-            __syncwarp();
-          }
+          if (it >= ring_n && !wait_all_lanes(&S.empty[s], ((it / ring_n) + 1u) & 1u)) goto drain;
+          last_it[s] = it;
           unsigned char *dst = ring + (size_t)s * L.slot_bytes;
           const int r0 = j * 16 * P.RGS, rows = unit_rows(P, j);
           // the slot was only read by the consumers (generic loads) before they
@@ -641,7 +643,25 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const Layer
       }
     }
   }
+drain:
   if (!first_done) after_first();
+  // No CTA may exit while its own copies are still landing in its shared
+  // memory: wait (bounded, even after an abort) for the last copy issued into
+  // every slot.  In a normal run the consumers have seen all of them already.
+  if (ROLE == 1) asm volatile("cp.async.wait_all;" ::: "memory");
+  if (lane == 0) {
+    const uint32_t ring_n = (uint32_t)L.ring;
+    for (int s = 0; s < (ROLE == 0 ? L.ring : 2); ++s) {
+      const uint32_t last = ROLE == 0 ? last_it[s] : last_wn[s];
+      if (last == ~0u) continue;
+      uint64_t *bar = ROLE == 0 ? &S.full[s] : &S.wfull[s];
+      const uint32_t parity = ROLE == 0 ? (last / ring_n) & 1u : (last >> 1) & 1u;
+      uint32_t i = 0;
+      while (!mbar_try_wait(bar, parity) && ++i < kWaitLimit) {
+      }
+    }
+  }
+  __syncwarp();
 }
 
 // ---- consumers -------------------------------------------------------------------------
@@ -1410,17 +1430,20 @@ static cudaError_t encode_scale_map(CUtensorMap *m, const uint8_t *scales, int E
 
 template <int FMT>
 static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, bool pdl, cudaStream_t stream) {
-  static int smem_set = 0, smem_ok = 0;
+  // kernel attributes are per device: the opt-in size set and the size checked for residency
+  static std::atomic<int> smem_set[kMaxDevices], smem_ok[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
   auto kfn = moe_layer_kernel<FMT>;
-  if (L.smem > smem_set) {
+  if (L.smem > smem_set[dev].load(std::memory_order_acquire)) {
     cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                            cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
     if (err != cudaSuccess) return err;
-    smem_set = L.smem;
+    smem_set[dev].store(L.smem, std::memory_order_release);
   }
-  if (L.smem != smem_ok) {  // one CTA per SM must fit, or the cooperative launch is refused
+  if (L.smem != smem_ok[dev].load(std::memory_order_acquire)) {  // one CTA per SM must fit, or the cooperative launch is refused
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kLayerThreads, L.smem);
     if (err != cudaSuccess) return err;
@@ -1431,7 +1454,7 @@ static cudaError_t launch_layer_fmt(const LayerArgs &a, const LayerPlan &L, bool
                 fa.numRegs, kLayerThreads, (size_t)fa.sharedSizeBytes, L.smem);
       return cudaErrorCooperativeLaunchTooLarge;
     }
-    smem_ok = L.smem;
+    smem_ok[dev].store(L.smem, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms());
@@ -1462,3 +1485,9 @@ cudaError_t launch_layer(LayerArgs &a, const LayerPlan &L, int E, bool pdl, cuda
 }
 
 }  // namespace qmoe
+
+extern "C" int qmoe_binary_version(void) {
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, qmoe::moe_layer_kernel<QMOE_NVFP4>) != cudaSuccess) return -1;
+  return fa.binaryVersion;
+}

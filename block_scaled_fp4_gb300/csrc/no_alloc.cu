@@ -24,21 +24,24 @@ constexpr size_t kStaticScratchBytes = QMOE_NO_ALLOC_SCRATCH_BYTES;
 // device below.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+void *g_scratch_addr[qmoe::kMaxDevices] = {nullptr};
+
+}  // namespace
+
+namespace qmoe {
 
 // Device address of the scratch array on the current device (looked up on the
 // first call for that device).
-qmoe_status scratch_address(void **addr) {
+qmoe_status no_alloc_scratch(void **addr) {
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) {
     qmoe::set_error("no-alloc forward: cudaGetDevice failed: %s", cudaGetErrorString(err));
     return QMOE_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    qmoe::set_error("no-alloc forward: device %d outside the supported range 0..%d", dev, kMaxDevices - 1);
+  if (dev < 0 || dev >= qmoe::kMaxDevices) {
+    qmoe::set_error("no-alloc forward: device %d outside the supported range 0..%d", dev, qmoe::kMaxDevices - 1);
     return QMOE_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
@@ -56,7 +59,7 @@ qmoe_status scratch_address(void **addr) {
   return QMOE_OK;
 }
 
-}  // namespace
+}  // namespace qmoe
 
 extern "C" qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const float *logits, const uint8_t *fc1_w,
                                                      const uint8_t *fc1_s, const float *fc1_g,
@@ -78,7 +81,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const fl
     return QMOE_ERR_WORKSPACE;
   }
   void *scratch = nullptr;
-  st = scratch_address(&scratch);
+  st = qmoe::no_alloc_scratch(&scratch);
   if (st != QMOE_OK) return st;
   size_t have = kStaticScratchBytes;
   // The array is zero when the module loads and its header stays zero between

@@ -14,6 +14,8 @@
 // activations) and its epilogue applies SwiGLU to the adjacent (gate,
 // linear) columns of a row, writing a = bf16(SwiGLU) [R, I]; GEMM2 writes
 // y (fp32) [R, H].
+#include <atomic>
+
 #include "qmoe_common.cuh"
 
 namespace qmoe {
@@ -311,20 +313,17 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const float *__restrict_
   }
 }
 
-__device__ int32_t g_prefill_error;  // set by a tcgen05 GEMM CTA whose wait gave up
-
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
-  static bool smem_set = false;
-  static int32_t *err_flag = nullptr;
-  if (!smem_set) {
+  // the shared-memory opt-in is a per-device attribute of the kernel
+  static std::atomic<int> smem_set[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (err != cudaSuccess) return err;
-    void *ptr = nullptr;
-    err = cudaGetSymbolAddress(&ptr, g_prefill_error);
-    if (err != cudaSuccess) return err;
-    err_flag = static_cast<int32_t *>(ptr);
-    smem_set = true;
+    smem_set[dev].store(1, std::memory_order_release);
   }
+  int32_t *err_flag = a.err_flag;
   const int R = a.T * a.k;
   const int na_max = a.E < R ? a.E : R;
   const unsigned mtiles = (unsigned)((R + kTcBM - 1) / kTcBM + na_max);  // >= the sum over experts of ceil(rows / kTcBM)

@@ -83,6 +83,13 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 void set_error(const char *fmt, ...);
 int num_sms();
+// Per-device host caches (kernel attributes, symbol addresses) hold this many devices.
+constexpr int kMaxDevices = 64;
+// The current device, or -1 when there is none or it is outside [0, kMaxDevices).
+int current_device();
+// Device address of the no-alloc entry point's static scratch on the current
+// device (looked up once per device).
+qmoe_status no_alloc_scratch(void **addr);
 
 // Routing of few tokens: one CTA does top-k, softmax and the stable expert
 // ranking for T <= kFusedRouteMaxTokens tokens.
@@ -175,6 +182,7 @@ struct PrefillArgs {
   uint16_t *act;             // bf16 [T * k, I] FC1 activations, permuted order
   float *y;                  // fp32 [T * k, H] FC2 rows, permuted order
   uint16_t *out;             // bf16 [T, H]
+  int32_t *err_flag;         // the workspace's device error flag (header word 1)
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
 

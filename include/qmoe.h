@@ -61,7 +61,8 @@ typedef enum {
     QMOE_ERR_MISALIGNED = 2,   /* a tensor pointer is not 16-byte aligned */
     QMOE_ERR_UNSUPPORTED = 3,  /* shape outside what the kernels cover */
     QMOE_ERR_WORKSPACE = 4,    /* *workspace_bytes smaller than required */
-    QMOE_ERR_CUDA = 5          /* a CUDA call or kernel launch failed */
+    QMOE_ERR_CUDA = 5,         /* a CUDA call or kernel launch failed */
+    QMOE_ERR_DEVICE = 6        /* a bounded wait inside a kernel gave up (qmoe_check_device_error) */
 } qmoe_status;
 
 typedef enum {
@@ -84,9 +85,10 @@ typedef enum {
      * kernel of the stream is still finishing elsewhere, and waits until that
      * kernel's results are visible before it touches global memory.  Back-to-
      * back layers then pay no memset node and no full launch gap.  Header
-     * word 1 (int32) is the decode kernel's error flag, set to 1 when a
-     * bounded wait inside the kernel gave up (its results are then not to be
-     * trusted); with the flag it stays set until the caller clears it. */
+     * word 1 (int32) is the device error flag (see qmoe_check_device_error):
+     * any kernel of a forward call sets it to 1 when one of its bounded waits
+     * gave up.  Only that word can become nonzero; it stays set until
+     * qmoe_check_device_error reads and clears it. */
     QMOE_WORKSPACE_PRIMED = 0x200
 } qmoe_fp4_format;
 
@@ -258,9 +260,12 @@ qmoe_status qmoe_fp4_scales_kmajor(const uint8_t *block_scales, int E, int N, in
  *  - Every call, on any stream or host thread, uses the same array, which keeps
  *    the last call's contents: calls that overlap on the GPU race and corrupt
  *    each other's results.  Order them (one stream, or events).
- *  - The array starts at zero, and its header (QMOE_WORKSPACE_HEADER_BYTES)
- *    stays zero between calls (see QMOE_WORKSPACE_PRIMED), so every call runs
- *    as a primed one: no per-call reset, programmatic dependent launch.
+ *  - The array starts at zero.  The counters in its header
+ *    (QMOE_WORKSPACE_HEADER_BYTES) are back at zero whenever a call returns
+ *    (see QMOE_WORKSPACE_PRIMED), so every call runs as a primed one: no
+ *    per-call reset, programmatic dependent launch.  The header's error flag
+ *    is the one exception: qmoe_check_device_error(NULL, stream) reads and
+ *    clears it.
  */
 #define QMOE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -273,6 +278,33 @@ qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const float *logits
                                           float alpha, float beta, float limit,
                                           uint16_t *out, int32_t *topk_ids_out,
                                           cudaStream_t stream);
+
+/*
+ * qmoe_check_device_error -- read and clear the device error flag of a
+ * forward workspace.  Every wait inside the library's kernels is bounded (a
+ * kernel never hangs the GPU): a wait that gives up sets word 1 of the
+ * workspace header to 1 and the kernel returns early, so the outputs of that
+ * call (and of later calls on the same workspace until the flag is cleared)
+ * are not to be trusted.  The flag is never set by a call that ran normally.
+ *
+ *   workspace  the workspace passed to qmoe_fp4_moe_forward, or NULL for the
+ *              static scratch of qmoe_fp4_moe_forward_no_alloc on the
+ *              current device.
+ *   stream     the stream of the calls to check.
+ * Synchronises `stream`, reads the flag (a 4-byte device-to-host copy) and,
+ * when it is set, resets it to 0 (a 4-byte memset on `stream`, then a
+ * synchronisation) and returns QMOE_ERR_DEVICE; otherwise returns QMOE_OK.
+ * A call without QMOE_WORKSPACE_PRIMED resets the flag with the rest of the
+ * header before it launches, so check before the next such call on the same
+ * workspace.  Allocates nothing.
+ */
+qmoe_status qmoe_check_device_error(void *workspace, cudaStream_t stream);
+
+/* Diagnostics: the binary version (compute capability x 10 + minor, 103 for
+ * sm_103a) of the decode kernel as the CUDA runtime reports it on the current
+ * device (cudaFuncGetAttributes), or -1 when the query fails (no device, or
+ * no image for it). */
+int qmoe_binary_version(void);
 
 /* One-line description of the last failed call on this host thread ("" if none). */
 const char *qmoe_last_error(void);

@@ -38,13 +38,32 @@ def test_library_exports_every_declared_symbol(qm):
     assert declared == set(qm.EXPORTS)
 
 
-def test_built_for_sm103a(qm):
+def test_built_for_sm103a_only(qm):
+    """The build compiles one image, for sm_103a (the runtime check of the
+    image a GB300 loads is test_gpu_errors.test_kernels_run_the_sm103a_image)."""
+    import importlib
+    b = importlib.import_module("block_scaled_fp4_gb300.build")
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+# The validation tests below pass placeholder pointers, which the host checks
+# must reject before any launch.  They run in a child process that sees no GPU,
+# so a validation regression can never launch a kernel on those pointers.
+def _in_child_without_gpu(body: str) -> None:
     import subprocess
-    out = subprocess.run(["cuobjdump", "--list-elf", qm.library_path()], capture_output=True,
-                         text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    assert "sm_103a" in out.stdout
+    import sys
+    import textwrap
+    code = textwrap.dedent("""
+        import ctypes, math, os, sys
+        sys.path.insert(0, %r)
+        sys.path.insert(0, %r)
+        import block_scaled_fp4_gb300 as qm
+        L = qm.load()
+        import test_abi as T
+    """) % (ROOT, os.path.join(ROOT, "tests")) + textwrap.dedent(body)
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="-1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
 
 
 def _fwd(L, **kw):
@@ -61,8 +80,7 @@ def _fwd(L, **kw):
     return rc, nb.value
 
 
-def test_forward_validation(qm):
-    L = qm.load()
+def check_forward_validation(L):
     rc, need = _fwd(L)
     assert rc == 0 and need > 0                                   # size query
     assert _fwd(L, k=9)[0] == 1                                   # k > 8
@@ -84,8 +102,11 @@ def test_forward_validation(qm):
     assert b"workspace" in L.qmoe_last_error() or True
 
 
-def test_route_and_dequant_validation(qm):
-    L = qm.load()
+def test_forward_validation(qm):
+    _in_child_without_gpu("T.check_forward_validation(L)")
+
+
+def check_route_and_dequant_validation(L):
     P = ctypes.c_void_p
     nb = ctypes.c_size_t(99)
     assert L.qmoe_route_topk(P(256), 4, 256, 8, 1, None, None, None, None, None, None,
@@ -99,6 +120,10 @@ def test_route_and_dequant_validation(qm):
     assert L.qmoe_fp4_dequant(P(264), P(256), None, 1, 64, 64, 0, P(256), None) == 2
     assert L.qmoe_fp4_dequant(P(256), P(256), None, 1, 64, 64, 7, P(256), None) == 3
     assert b"format" in L.qmoe_last_error()
+
+
+def test_route_and_dequant_validation(qm):
+    _in_child_without_gpu("T.check_route_and_dequant_validation(L)")
 
 
 def test_binding_constants_match_the_header(qm):
@@ -121,9 +146,8 @@ def test_binding_constants_match_the_header(qm):
     assert qm.SCALES_KMAJOR & qm.WORKSPACE_PRIMED == 0 and min(qm.SCALES_KMAJOR, qm.WORKSPACE_PRIMED) > qm.MXFP4
 
 
-def test_primed_flag_is_a_format_flag_only_for_the_forward_calls(qm):
+def check_primed_flag(qm, L):
     """dequant and scales_kmajor take a plain format: the flag is rejected there."""
-    L = qm.load()
     dummy = ctypes.c_void_p(256)
     for fmt in (qm.NVFP4 | qm.WORKSPACE_PRIMED, qm.MXFP4 | qm.WORKSPACE_PRIMED):
         assert L.qmoe_fp4_dequant(dummy, dummy, None, 1, 64, 64, fmt, dummy, None) == 3
@@ -133,6 +157,10 @@ def test_primed_flag_is_a_format_flag_only_for_the_forward_calls(qm):
     assert base == qm.forward_workspace_bytes(4, 2048, 512, 256, 8,
                                               qm.NVFP4 | qm.SCALES_KMAJOR | qm.WORKSPACE_PRIMED)
     assert base >= qm.WORKSPACE_HEADER_BYTES
+
+
+def test_primed_flag_is_a_format_flag_only_for_the_forward_calls(qm):
+    _in_child_without_gpu("T.check_primed_flag(qm, L)")
 
 
 def test_plan_accepts_every_supported_decode_shape(qm):
@@ -171,3 +199,24 @@ def test_binding_has_no_cpu_fallback(qm):
         qm.dequant(t["w1"], t["s1"], t["g1"], wl.fmt)
     with pytest.raises(ValueError, match="CUDA tensor"):
         qm.scales_kmajor(t["s1"], wl.fmt)
+
+
+def test_no_alloc_rejects_sizes_beyond_its_scratch(qm):
+    """A shape whose scratch need exceeds the no-alloc entry point's fixed array
+    is refused with a clear error before anything is launched (in a child that
+    sees no GPU; the size check needs none)."""
+    import re
+    hdr = open(os.path.join(ROOT, "include", "qmoe.h")).read()
+    m = re.search(r"#define QMOE_NO_ALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", hdr)
+    scratch = int(m.group(1)) << int(m.group(2))
+    need = qm.forward_workspace_bytes(64, 8192, 4096, 64, 1, qm.NVFP4)
+    assert need > scratch
+    _in_child_without_gpu("""
+        P = ctypes.c_void_p
+        bad = P(0x1001)
+        rc = L.qmoe_fp4_moe_forward_no_alloc(bad, P(256), bad, bad, None, bad, bad, None, 0, 64, 8192, 4096,
+                                             64, 1, 1, 1, ctypes.c_float(1.0), ctypes.c_float(0.0),
+                                             ctypes.c_float(math.inf), bad, None, None)
+        assert rc == 4, rc
+        assert b"static scratch" in L.qmoe_last_error()
+    """)

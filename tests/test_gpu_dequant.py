@@ -65,21 +65,17 @@ def test_dequant_mxfp4_with_global_scale(qgpu, oracle):
     _same(_run(qgpu, w, s, g, MX), oracle.dequant(w, s, g, MX))
 
 
-def test_dequant_prefill_size_sampled(qgpu, oracle):
-    """The prefill workload's FC1 dequant at full size ([128,2048,1536] ->
-    [128,3072,2048]) in the launch configuration the benchmark uses, checked
-    on sampled elements the oracle computes one by one, plus whole rows."""
+@pytest.mark.parametrize("fc", ["fc1", "fc2"])
+def test_dequant_prefill_size_whole_tensor(qgpu, oracle, fc):
+    """The prefill workload's dequantisations at full size, in the launch
+    configuration the benchmark uses, compared with the oracle bit for bit over
+    the whole tensor: FC1 [128, 2048, 1536] -> [128, 3072, 2048] and FC2
+    [128, 1536, 1024] -> [128, 2048, 1536]."""
     wl = syn.WORKLOADS["nvfp4_prefill"]
-    rng = syn.rng_for(0, 7)
-    w, s, g = syn.expert_weights(rng, NV, wl.E, wl.H, 2 * wl.I)
+    K, N = (wl.H, 2 * wl.I) if fc == "fc1" else (wl.I, wl.H)
+    rng = syn.rng_for(0, 7 if fc == "fc1" else 8)
+    w, s, g = syn.expert_weights(rng, NV, wl.E, K, N)
     got = _run(qgpu, w, s, g, NV)
-    E, N, K = got.shape
-    samp = np.random.default_rng(1)
-    for _ in range(3000):
-        e, n, k = int(samp.integers(E)), int(samp.integers(N)), int(samp.integers(K))
-        ref = oracle.bf16_rne(oracle.dequant_element(w, s, g, NV, e, n, k))
-        assert got[e, n, k] == ref, (e, n, k)
-    for e, n in [(0, 0), (E - 1, N - 1), (63, 1537)]:
-        sub = oracle.dequant(w[e:e + 1], s[e:e + 1], g[e:e + 1], NV)[0]
-        _same(got[e, n], sub[n])
-        _same(got[e, :, 0], sub[:, 0])
+    assert got.shape == (wl.E, N, K)
+    ref = oracle.dequant(w, s, g, NV)
+    _same(got, ref)

@@ -46,8 +46,9 @@ def test_forward_decode_workloads(qgpu, oracle, name):
 
 
 @pytest.mark.parametrize("seed", [1, 2])
-def test_forward_mtp_decode_more_seeds(qgpu, oracle, seed):
-    _check(qgpu, oracle, syn.WORKLOADS["nvfp4_mtp_decode"], seed=seed)
+@pytest.mark.parametrize("name", DECODE[1:])
+def test_forward_decode_workloads_more_seeds(qgpu, oracle, name, seed):
+    _check(qgpu, oracle, syn.WORKLOADS[name], seed=seed)
 
 
 EDGE = [
