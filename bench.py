@@ -228,6 +228,8 @@ def run_gpu(args):
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
     ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=device) for _ in layers]
     stream = torch.cuda.Stream(device=device)
+    # inputs and the workspace were written on the current stream: order them first
+    stream.wait_stream(torch.cuda.current_stream())
 
     def step(lst=layers):
         for i, L in enumerate(lst):
@@ -419,6 +421,8 @@ def bench_decode(device, workload: str, n_layers: int, steps: int, peak: float, 
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
     ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=device) for _ in layers]
     stream = torch.cuda.Stream(device=device)
+    # inputs and the workspace were written on the current stream: order them first
+    stream.wait_stream(torch.cuda.current_stream())
 
     def step():
         for i, L in enumerate(layers):
@@ -488,6 +492,8 @@ def bench_routing(device, reps: int = 200) -> dict:
     wl = syn.WORKLOADS[WORKLOAD]
     lg = [torch.from_numpy(syn.logits(syn.rng_for(7, i), wl.T, wl.E, wl.logit_std)).to(device) for i in range(40)]
     stream = torch.cuda.Stream(device=device)
+    # inputs and the workspace were written on the current stream: order them first
+    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for x in lg:
             q.route_topk(x, wl.k, wl.normalize, stream=stream)
@@ -548,6 +554,8 @@ def bench_dequant(device, peak: float, reps: int = 10, E: int = 128, K: int = 20
                     -torch.randint(0, 5, (E,), generator=gen, device=device).float()).float()
     out = torch.empty((E, N, K), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.Stream(device=device)
+    # inputs and the workspace were written on the current stream: order them first
+    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for _ in range(3):
             q.dequant(packed, scales, g, q.NVFP4, out=out, stream=stream)
@@ -605,6 +613,8 @@ def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
     w1d, w2d = q.dequant(w1, s1, g1, q.NVFP4), q.dequant(w2, s2, g2, q.NVFP4)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.Stream(device=device)
+    # inputs and the workspace were written on the current stream: order them first
+    stream.wait_stream(torch.cuda.current_stream())
     ws_full = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4), dtype=torch.uint8, device=device)
     ws_gemm = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4, True), dtype=torch.uint8, device=device)
 

@@ -318,7 +318,8 @@ __device__ __forceinline__ bool wait_bar(Shared &S, const LayerArgs &g, uint64_t
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   *(volatile int *)&S.abort = 1;
-  atomicExch(g.meta + 1, 1);
+  // the flag keeps the first failure: 100 + the barrier's index in the shared block
+  atomicCAS(g.meta + 1, 0, 100 + (int)(bar - reinterpret_cast<uint64_t *>(&S)));
   return false;
 }
 
@@ -331,7 +332,7 @@ __device__ void grid_barrier(Shared &S, const LayerArgs &g, int32_t *ctr) {
     for (uint32_t i = 0; ld_acquire(ctr) < (int)gridDim.x; ++i) {
       if (i >= limit) {
         *(volatile int *)&S.abort = 1;
-        atomicExch(g.meta + 1, 1);
+        atomicCAS(g.meta + 1, 0, 200 + (int)(ctr - g.meta));  // 202, 203: the grid barriers
         break;
       }
       __nanosleep(64);
@@ -364,7 +365,7 @@ __device__ void build_segments(Shared &S, const LayerArgs &g, const FcPlan &P, i
   if (n > kMaxSegs) {  // the host bounds this; report rather than drop work
     if (lane == 0) {
       *(volatile int *)&S.abort = 1;
-      atomicExch(g.meta + 1, 1);
+      atomicCAS(g.meta + 1, 0, 300);  // more segments than the kernel holds
     }
   }
   const int nseg = min(n, kMaxSegs);
@@ -1168,8 +1169,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   // Launched with programmatic dependent launch, the kernel may start while
   // the previous kernel of the stream still runs: nothing in global memory
   // (inputs, workspace) is touched before that kernel's results are visible.
-  // The next kernel may then be scheduled at once: it cannot become resident
-  // on an SM before this kernel's CTA there has exited.
+  // The next kernel may then be scheduled at once: it is launched only once
+  // every CTA of this grid has passed this point (so all are resident), and
+  // it cannot become resident on an SM before this kernel's CTA there exits.
   pdl_wait();
   pdl_launch_dependents();
   if (tid == 0) {

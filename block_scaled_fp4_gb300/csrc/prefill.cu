@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kTcThreads) grouped_gemm_tc_kernel(const __gri
       // stage ns was read by the MMAs of k step kt - 1: wait for them
       if (kt >= 1 && !s_abort && !tc_mbar_wait(&mma_done[ns], (uint32_t)((kt - 1) / kTcStages) & 1u)) {
         s_abort = 1;
-        atomicExch(err_flag, 1);
+        atomicCAS(err_flag, 0, 400);
       }
       load_stage(ns, nk * kTcBK);
     }
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads) grouped_gemm_tc_kernel(const __gri
   cp_async_wait<0>();
   if (!s_abort && !tc_mbar_wait(&mma_done[(KT - 1) % kTcStages], (uint32_t)((KT - 1) / kTcStages) & 1u)) {
     s_abort = 1;
-    atomicExch(err_flag, 1);
+    atomicCAS(err_flag, 0, 400);
   }
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 

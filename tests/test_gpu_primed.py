@@ -89,6 +89,8 @@ def test_primed_chain_in_cuda_graph(qgpu):
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda") for wl, _ in layers]
     s = torch.cuda.Stream()
+    # inputs and the workspace were written on the current stream: order them first
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         for (wl, d), o in zip(layers, outs):  # warm-up, outside the capture
             _call(qgpu, d, wl, wl.fmt | qgpu.WORKSPACE_PRIMED, ws, o)
@@ -126,3 +128,54 @@ def test_default_call_resets_a_dirty_header(qgpu):
     torch.cuda.synchronize()
     assert not _header(dirty).any()
     assert np.array_equal(bf16_tensor_bits(a), bf16_tensor_bits(b))
+
+
+@pytest.mark.parametrize("name,kmajor", [("nvfp4_mtp_decode", True), ("mxfp4_decode", False),
+                                         ("nvfp4_verify_edge", False), ("tiny_nvfp4_decode", True)])
+def test_primed_long_chain_keeps_the_flag_clear(qgpu, name, kmajor):
+    """Many primed calls of one workload back to back (eagerly and replayed
+    from a CUDA graph): every launch is chained to the previous one by
+    programmatic dependent launch, and no bounded wait may give up (the
+    device error flag stays clear) while the results equal the default
+    calls' bit for bit."""
+    import importlib
+    bench = importlib.import_module("bench")
+    dev = torch.device("cuda", 0)
+    wl, layers = bench.make_layers(4, 99, dev, name)
+    fmt = wl.fmt
+    if kmajor:
+        for L in layers:
+            L["s1"], L["s2"] = qgpu.scales_kmajor(L["s1"], wl.fmt), qgpu.scales_kmajor(L["s2"], wl.fmt)
+        fmt |= qgpu.SCALES_KMAJOR
+    need = qgpu.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, fmt)
+    refs = []
+    for L in layers:
+        o = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+        _call(qgpu, L, wl, fmt, torch.empty(need, dtype=torch.uint8, device=dev), o)
+        refs.append(bf16_tensor_bits(o))
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev) for _ in layers]
+    stream = torch.cuda.Stream()
+    # inputs and the workspace were written on the current stream: order them first
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def chain():
+        for _ in range(6):
+            for L, o in zip(layers, outs):
+                _call(qgpu, L, wl, fmt | qgpu.WORKSPACE_PRIMED, ws, o)
+
+    with torch.cuda.stream(stream):
+        chain()
+    torch.cuda.synchronize()
+    qgpu.check_device_error(ws, stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        chain()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    qgpu.check_device_error(ws, stream)
+    assert not _header(ws).any(), _header(ws)
+    for o, r in zip(outs, refs):
+        assert np.array_equal(bf16_tensor_bits(o), r)
