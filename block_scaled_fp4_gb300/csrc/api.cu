@@ -337,9 +337,13 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
                            I, E, k, normalize, fusion, alpha, beta, limit, out, topk_ids_out, workspace,
                            workspace_bytes, stream);
   QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
+  // k-major block scales: moe_decode_kernel (decode.cu); scales as stored
+  // ([E, N, K/bs]): moe_layer_kernel (layer.cu)
   LayerPlan plan;
+  DkPlan dplan;
   size_t p1_floats = 0, p2_floats = 0;
-  st = make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);
+  st = kmajor ? make_dk_plan(base_fmt, T, H, I, E, k, dplan, p1_floats, p2_floats)
+              : make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);
   if (st != QMOE_OK) return st;
   const DecodeLayout need = decode_layout(nullptr, p1_floats, p2_floats);
   if (!workspace) {
@@ -377,7 +381,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
     err = cudaMemsetAsync(L.meta, 0, QMOE_WORKSPACE_HEADER_BYTES, stream);
     if (err != cudaSuccess) return cuda_status(err, "counter reset");
   }
-  err = launch_layer(g, plan, E, primed, stream);
+  err = kmajor ? launch_dk(g, dplan, primed, stream) : launch_layer(g, plan, E, primed, stream);
   if (err == cudaErrorCooperativeLaunchTooLarge && g_err[0]) return QMOE_ERR_CUDA;  // message already set
   if (err != cudaSuccess) return cuda_status(err, "layer launch");
   stage_event(1, stream);

@@ -124,6 +124,7 @@ struct LayerArgs {
   float *p1, *p2;          // fp32 partial sums of FC1 / FC2 (split-K segments)
   uint16_t *out;           // [T, H] bf16
   CUtensorMap tm_s1, tm_s2;  // block scales as 2-D byte arrays (when FcPlan::tma)
+  CUtensorMap tm_w1, tm_w2;  // packed weights as 2-D word arrays [E*K rows][N/8 words] (k-major decode, DkFc::ct > 1)
 };
 
 constexpr int kCostRows = 64;  // rows of one expert in the decode window (T * k <= 64)
@@ -151,6 +152,29 @@ struct LayerPlan {
   int slot_bytes, win_bytes;
   int sw_off, st_off, xs_off, xr_off, smem;
 };
+// Geometry of one FC for the k-major decode kernel (host-computed): unit =
+// UK = 16 * RGS k rows x NT columns; consumer thread (w, rg) owns column word
+// w (8 columns) of k-group rg of every unit.
+struct DkFc {
+  int K, N, NT, ct, NW, RGS, lg_rgs, UK;
+  int ku;         // units per (expert, column tile)
+  int nkg;        // K / 16
+  int nblocks;    // K / block size
+  int bpu;        // scale block rows one unit touches
+  int row_bytes;  // NT / 2
+  int rg_stride;  // bytes between row groups in a ring slot
+  int sc_off;     // offset of the unit's scale rows in its slot
+  int cap;        // partial rows one CTA's region holds
+};
+struct DkPlan {
+  DkFc f[2];
+  int slot_bytes, win_off, pre_off, smem;  // dynamic shared memory: the ring at 0, windows, FC2 activations
+  int u0, u1, pass;                        // split costs: unit = chunks * u0 + rows * u1; row-chunk start = pass
+};
+qmoe_status make_dk_plan(int fmt, int T, int H, int I, int E, int k, DkPlan &P, size_t &p1_floats,
+                         size_t &p2_floats);
+cudaError_t launch_dk(const LayerArgs &a, const DkPlan &P, bool pdl, cudaStream_t stream);
+
 qmoe_status make_layer_plan(int fmt, bool kmajor, int T, int H, int I, int E, int k, LayerPlan &L,
                             size_t &p1_floats, size_t &p2_floats);
 // pdl: launch with programmatic dependent launch (the header is already zero,
