@@ -22,6 +22,10 @@ SCALES_KMAJOR = 0x100  # OR'd into fmt of the forward calls: block scales are [E
 # bytes are zero (zeroed once by the caller; the library keeps them zero), so
 # decode calls skip their header reset and chain by programmatic dependent launch
 WORKSPACE_PRIMED = 0x200
+# OR'd with SCALES_KMAJOR into fmt of moe_forward: decode calls run on the
+# multi-row kernel whatever their size (without it, short weight streams run on
+# the one-row-per-pass kernel)
+DECODE_MULTIROW = 0x400
 WORKSPACE_HEADER_BYTES = 64
 BLOCK = {NVFP4: 16, MXFP4: 32}
 GEMV_MAX_ROWS = 64
@@ -255,5 +259,5 @@ _stage_keepalive = None
 
 __all__ = ["NVFP4", "MXFP4", "BLOCK", "GEMV_MAX_ROWS", "QMoEError", "build", "load", "library_path",
            "route_topk", "moe_forward", "moe_forward_no_alloc", "forward_workspace_bytes", "dequant",
-           "scales_kmajor", "SCALES_KMAJOR", "set_stage_events", "check_device_error", "binary_version",
+           "scales_kmajor", "SCALES_KMAJOR", "DECODE_MULTIROW", "set_stage_events", "check_device_error", "binary_version",
            "EXPORTS"]

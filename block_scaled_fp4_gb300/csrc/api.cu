@@ -320,7 +320,10 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   QMOE_REQUIRE(workspace_bytes, QMOE_ERR_INVALID_ARG, "workspace_bytes is NULL");
   const bool kmajor = (fmt & QMOE_SCALES_KMAJOR) != 0;
   const bool primed = (fmt & QMOE_WORKSPACE_PRIMED) != 0;
-  const int base_fmt = (int)fmt & ~(int)(QMOE_SCALES_KMAJOR | QMOE_WORKSPACE_PRIMED);
+  const bool multirow = (fmt & QMOE_DECODE_MULTIROW) != 0;
+  const int base_fmt = (int)fmt & ~(int)(QMOE_SCALES_KMAJOR | QMOE_WORKSPACE_PRIMED | QMOE_DECODE_MULTIROW);
+  QMOE_REQUIRE(!multirow || kmajor, QMOE_ERR_UNSUPPORTED,
+               "QMOE_DECODE_MULTIROW needs k-major block scales (QMOE_SCALES_KMAJOR)");
   QMOE_REQUIRE(base_fmt == QMOE_NVFP4 || base_fmt == QMOE_MXFP4, QMOE_ERR_UNSUPPORTED, "unknown format %d", (int)fmt);
   QMOE_REQUIRE(H >= 64 && I >= 64, QMOE_ERR_INVALID_ARG, "H and I must be >= 64 (got %d, %d)", H, I);
   QMOE_REQUIRE(H % 64 == 0 && I % 64 == 0, QMOE_ERR_UNSUPPORTED, "H and I must be multiples of 64 (got %d, %d)", H,
@@ -337,14 +340,25 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
                            I, E, k, normalize, fusion, alpha, beta, limit, out, topk_ids_out, workspace,
                            workspace_bytes, stream);
   QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
-  // k-major block scales: moe_decode_kernel (decode.cu); scales as stored
-  // ([E, N, K/bs]): moe_layer_kernel (layer.cu)
+  // Scales as stored ([E, N, K/bs]): moe_layer_kernel (layer.cu).  k-major
+  // scales: moe_decode_kernel (decode.cu, every row of an expert in one pass)
+  // unless one SM's share of the FC1 stream is short (under 16 units, all
+  // rows counted once), where moe_layer_kernel's earlier stream start wins;
+  // QMOE_DECODE_MULTIROW forces decode.cu.
   LayerPlan plan;
   DkPlan dplan;
   size_t p1_floats = 0, p2_floats = 0;
-  st = kmajor ? make_dk_plan(base_fmt, T, H, I, E, k, dplan, p1_floats, p2_floats)
-              : make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);
-  if (st != QMOE_OK) return st;
+  bool use_dk = false;
+  if (kmajor) {
+    st = make_dk_plan(base_fmt, T, H, I, E, k, dplan, p1_floats, p2_floats);
+    if (st != QMOE_OK) return st;
+    const double units_per_sm = (double)R * dplan.f[0].ct * dplan.f[0].ku / (double)num_sms();
+    use_dk = multirow || units_per_sm >= 16.0;
+  }
+  if (!use_dk) {
+    st = make_layer_plan(base_fmt, kmajor, T, H, I, E, k, plan, p1_floats, p2_floats);
+    if (st != QMOE_OK) return st;
+  }
   const DecodeLayout need = decode_layout(nullptr, p1_floats, p2_floats);
   if (!workspace) {
     *workspace_bytes = need.bytes;
@@ -381,7 +395,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
     err = cudaMemsetAsync(L.meta, 0, QMOE_WORKSPACE_HEADER_BYTES, stream);
     if (err != cudaSuccess) return cuda_status(err, "counter reset");
   }
-  err = kmajor ? launch_dk(g, dplan, primed, stream) : launch_layer(g, plan, E, primed, stream);
+  err = use_dk ? launch_dk(g, dplan, primed, stream) : launch_layer(g, plan, E, primed, stream);
   if (err == cudaErrorCooperativeLaunchTooLarge && g_err[0]) return QMOE_ERR_CUDA;  // message already set
   if (err != cudaSuccess) return cuda_status(err, "layer launch");
   stage_event(1, stream);

@@ -55,12 +55,12 @@ constexpr int kConsWarps = kCons / 32;
 constexpr int kThreads = kCons + 64;       // + the copy warp + the activation warp
 constexpr int kWarpP = kConsWarps;         // weight copies
 constexpr int kWarpH = kConsWarps + 1;     // activation windows
-constexpr int kRing = 4;                   // weight ring slots (32 KB units)
+constexpr int kRing = 5;                   // weight ring slots (32 KB units)
 constexpr int kMaxRC = 2;                  // rows decoded together (more rows: chunks of two)
-constexpr int kWinElems = 4096;            // fp16 activations per window buffer (rows x window length)
-constexpr int kPreElems = 12288;           // bf16 FC2 activations computed per group
+constexpr int kWinElems = 2048;            // fp16 activations per window buffer (rows x window length)
+constexpr int kPreElems = 4096;            // bf16 FC2 activations computed per group
 constexpr int kMaxSlots = 64;
-constexpr int kMaxPairs = 1024;            // (slot, tile) pairs whose CTA range is tabulated
+constexpr int kMaxPairs = 512;             // (slot, tile) pairs whose CTA range is tabulated
 constexpr int kHoldPairs = 128;            // pairs whose holders' partial-row bases are tabulated
 constexpr int kMaxCtas = 256;
 constexpr int kSmemOptin = 232448;
@@ -71,6 +71,7 @@ struct Shared {
   uint64_t full[kRing], empty[kRing];  // weight ring
   uint64_t xfull[2], xempty[2];        // activation windows
   uint64_t pre_ready;                  // an FC2 activation group is in place (every consumer thread arrives)
+  uint64_t tables_ready;               // the cross-CTA lookup tables are in place (every lane of the activation warp)
   int4 slot[kMaxSlots];                // {expert, first permuted row, rows, 0}, ascending expert
   int row_tok[kMaxSlots], row2slot[kMaxSlots];
   int r_ids[kMaxSlots], r_e2p[kMaxSlots], r_p2e[kMaxSlots];
@@ -93,9 +94,9 @@ struct Shared {
 __device__ __forceinline__ int nchunks(int rows) { return (rows + kMaxRC - 1) / kMaxRC; }
 // cost of one unit of an r-row expert and of a whole (expert, tile) pair, in
 // the plan's units (a 32 KB unit decoded for one row is u0 + u1)
-__device__ __forceinline__ int unit_cost(const DkPlan &P, int rows) { return nchunks(rows) * P.u0 + rows * P.u1; }
+__device__ __forceinline__ int unit_cost(const DkFc &F, int rows) { return nchunks(rows) * F.u0 + rows * F.u1; }
 __device__ __forceinline__ int pair_cost(const DkPlan &P, const DkFc &F, int rows) {
-  return nchunks(rows) * P.pass + F.ku * unit_cost(P, rows);
+  return nchunks(rows) * P.pass + F.ku * unit_cost(F, rows);
 }
 // partial rows of all pairs before pair p = (slot a, tile t)
 __device__ __forceinline__ int wpair(const Shared &S, const DkFc &F, int p) {
@@ -116,7 +117,7 @@ __device__ int split_bound(const Shared &S, const DkPlan &P, int f, int c, int G
     const int mid = (lo + hi + 1) >> 1;
     if (S.scum[f][mid] <= x) lo = mid; else hi = mid - 1;
   }
-  const int r = S.slot[lo].z, cu = unit_cost(P, r), pc = pair_cost(P, F, r);
+  const int r = S.slot[lo].z, cu = unit_cost(F, r), pc = pair_cost(P, F, r);
   const long long rem = x - S.scum[f][lo];
   const int q = (int)(rem / pc);
   int u;
@@ -309,7 +310,7 @@ __device__ __noinline__ void producer(Shared &S, const LayerArgs &g, const DkPla
       const uint8_t *wexp = wbase + (size_t)e * F.K * (F.N / 2) + (size_t)c.t * F.row_bytes;
       const uint8_t *sexp = sbase + (size_t)e * F.nblocks * F.N + (size_t)c.t * F.NT;
       for (int j = c.wj0; j < c.wj1; ++j, ++it) {
-        const int s = (int)(it & (kRing - 1));
+        const int s = (int)(it % kRing);
         if (it >= (uint32_t)kRing) {
           int ok = 1;
           if (lane == 0) ok = wait_bar(S, g, &S.empty[s], ((it / kRing) + 1u) & 1u) ? 1 : 0;
@@ -388,12 +389,53 @@ __device__ __forceinline__ void stage_window(Shared &S, const LayerArgs &g, cons
   }
 }
 
+// Lookup tables of the cross-CTA sums (needed once the FC1 partials are
+// complete), by the activation warp once its FC1 windows are staged (off the
+// consumers' path): every CTA's partial-row offset, the CTA range of every
+// (slot, tile) pair, the holders' partial-row bases of the tabulated pairs
+// and the slots' global scales.  The consumers wait for them (tables_ready)
+// after the first grid barrier.
+__device__ __noinline__ void build_tables(Shared &S, const LayerArgs &g, const DkPlan &P) {
+  const int lane = (int)lane_id(), G = (int)gridDim.x, na = S.na;
+  const int np0 = min(na * P.f[0].ct, kMaxPairs), np1 = min(na * P.f[1].ct, kMaxPairs);
+  for (int i = lane; i < 2 * G + np0 + np1 + na; i += 32) {
+    if (i < 2 * G) {
+      const int f = i >= G ? 1 : 0, c = i - f * G;
+      S.offp[f][c] = offp_of(S, P.f[f], f, c);
+    } else if (i < 2 * G + np0 + np1) {
+      const int f = i >= 2 * G + np0 ? 1 : 0, p = i - 2 * G - (f ? np0 : 0);
+      const DkFc &F = P.f[f];
+      const int cf = cta_of(S.bnd[f], p * F.ku), cl = cta_of(S.bnd[f], p * F.ku + F.ku - 1);
+      S.pr[f][p] = (uint32_t)cf | ((uint32_t)cl << 16);
+      if (p < kHoldPairs) {
+        const int wp = wpair(S, F, p);
+        for (int u = 0; u < 8; ++u) {
+          const int o = cf + u <= cl ? offp_of(S, F, f, cf + u) : -1;
+          S.hold[f][p][u] = o >= 0 ? o + wp : -1;
+        }
+        if (cl - cf >= 8) S.hold[f][p][7] = -2;  // more than 8 holders: not tabulated
+      }
+    } else {
+      const int a = i - 2 * G - np0 - np1;
+      S.gs[0][a] = g.g1 ? __ldg(g.g1 + S.slot[a].x) : 1.0f;
+      S.gs[1][a] = g.g2 ? __ldg(g.g2 + S.slot[a].x) : 1.0f;
+    }
+  }
+  mbar_arrive(&S.tables_ready);  // every lane, after its own stores
+}
+
+__device__ __noinline__ void warm_code(Shared &S, const LayerArgs &g, const DkPlan &P, uint16_t *pre);
+
 __device__ __noinline__ void activations(Shared &S, const LayerArgs &g, const DkPlan &P, __half *wins,
                                          const uint16_t *pre) {
   const int lane = (int)lane_id();
   uint32_t wn = 0, gidx = 0;
   int gused = -1;
   for (int f = 0; f < 2; ++f) {
+    if (f == 1) {  // every FC1 window is staged
+      build_tables(S, g, P);
+      warm_code(S, g, P, const_cast<uint16_t *>(pre));
+    }
     Cur c;
     for (cur_begin(c, S, P, f); c.valid; cur_next(c, S, P), ++wn) {
       const uint16_t *src = nullptr;
@@ -591,25 +633,34 @@ __device__ __forceinline__ uint16_t fc2_activation(const Shared &S, const LayerA
 // The FC2 activations of the group of windows starting at c, into `pre`
 // (window after window, rows of klen values), by every consumer thread; each
 // thread then arrives on pre_ready.
-__device__ __noinline__ void prestage_group(Shared &S, const LayerArgs &g, const DkPlan &P, const Cur c0,
-                                            uint16_t *pre) {
+__device__ __forceinline__ void prestage_body(Shared &S, const LayerArgs &g, const DkPlan &P, const Cur c0,
+                                              uint16_t *pre, bool dry = false) {
   Cur q = c0;
   int base = 0;
   bool first = true;
-  int i = (int)threadIdx.x;  // this thread's next element of the group
+  int i = dry ? (int)lane_id() : (int)threadIdx.x;  // this thread's next element of the group
   while (q.valid) {
     const int sz = q.rc * q.klen;
     if (!first && base + sz > kPreElems) break;  // the group rule of group_step
 #pragma unroll 1
     for (; i < base + sz; i += kCons) {
       const int loc = i - base, rr = loc / q.klen;
-      pre[i] = fc2_activation(S, g, P, q.a, q.c0 + rr, q.k0 + loc - rr * q.klen);
+      const uint16_t v = fc2_activation(S, g, P, q.a, q.c0 + rr, q.k0 + loc - rr * q.klen);
+      if (dry) return;  // a dry run (see warm_code) stops after one element
+      pre[i] = v;
     }
     base += sz;
     first = false;
     cur_next(q, S, P);
   }
-  mbar_arrive(&S.pre_ready);
+  if (!dry) mbar_arrive(&S.pre_ready);
+}
+// out of line for the groups after the first (inside the chunk loop, rare);
+// the first group is computed inline at the start of FC2, where few registers
+// are live (no call, no saved registers)
+__device__ __noinline__ void prestage_group(Shared &S, const LayerArgs &g, const DkPlan &P, const Cur c0,
+                                            uint16_t *pre) {
+  prestage_body(S, g, P, c0, pre);
 }
 
 // All windows of one row chunk of a segment (c on its first window; on return
@@ -702,12 +753,13 @@ __device__ __forceinline__ void run_chunk(Shared &S, const LayerArgs &g, const D
 // out[t][n] = bf16(sum_j w[t][j] * g2 * y_j[n]) once every FC2 partial is
 // written: 8 lanes per column pair, lane j gathers expert j's FC2 partials;
 // the lanes are summed by a fixed butterfly.
-__device__ __noinline__ void finalize(Shared &S, const LayerArgs &g, const DkPlan &P) {
+__device__ __noinline__ void finalize(Shared &S, const LayerArgs &g, const DkPlan &P, bool dry = false) {
   const DkFc &F = P.f[1];
   const int half = g.H / 2;
   const int items = g.T * half * 8;
   const int items_pad = (items + 31) & ~31;
-  for (int idx = (int)blockIdx.x * kCons + (int)threadIdx.x; idx < items_pad; idx += (int)gridDim.x * kCons) {
+  const int i0 = dry ? (int)lane_id() : (int)blockIdx.x * kCons + (int)threadIdx.x;
+  for (int idx = i0; idx < items_pad; idx += (int)gridDim.x * kCons) {
     const int grp = idx >> 3, j = idx & 7;
     const bool ok = grp < g.T * half && j < g.k;
     float y0 = 0.f, y1 = 0.f;
@@ -729,42 +781,23 @@ __device__ __noinline__ void finalize(Shared &S, const LayerArgs &g, const DkPla
       y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, m);
       y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, m);
     }
+    if (dry) return;  // a dry run (see warm_code) stops after one item
     if (ok && j == 0)
       reinterpret_cast<uint32_t *>(g.out + (size_t)t * g.H)[n / 2] = f32_to_bf16_rne(y0) | (f32_to_bf16_rne(y1) << 16);
   }
 }
 
-// Lookup tables of the cross-CTA sums (needed once the FC1 partials are
-// complete), by every consumer thread of the CTA before the first grid
-// barrier: every CTA's partial-row offset, the CTA range of every (slot, tile)
-// pair, the holders' partial-row bases of the tabulated pairs and the slots'
-// global scales.  The grid barrier's CTA barriers publish them.
-__device__ __noinline__ void build_tables(Shared &S, const LayerArgs &g, const DkPlan &P) {
-  const int tid = threadIdx.x, G = (int)gridDim.x, na = S.na;
-  const int np0 = min(na * P.f[0].ct, kMaxPairs), np1 = min(na * P.f[1].ct, kMaxPairs);
-  for (int i = tid; i < 2 * G + np0 + np1 + na; i += kCons) {
-    if (i < 2 * G) {
-      const int f = i >= G ? 1 : 0, c = i - f * G;
-      S.offp[f][c] = offp_of(S, P.f[f], f, c);
-    } else if (i < 2 * G + np0 + np1) {
-      const int f = i >= 2 * G + np0 ? 1 : 0, p = i - 2 * G - (f ? np0 : 0);
-      const DkFc &F = P.f[f];
-      const int cf = cta_of(S.bnd[f], p * F.ku), cl = cta_of(S.bnd[f], p * F.ku + F.ku - 1);
-      S.pr[f][p] = (uint32_t)cf | ((uint32_t)cl << 16);
-      if (p < kHoldPairs) {
-        const int wp = wpair(S, F, p);
-        for (int u = 0; u < 8; ++u) {
-          const int o = cf + u <= cl ? offp_of(S, F, f, cf + u) : -1;
-          S.hold[f][p][u] = o >= 0 ? o + wp : -1;
-        }
-        if (cl - cf >= 8) S.hold[f][p][7] = -2;  // more than 8 holders: not tabulated
-      }
-    } else {
-      const int a = i - 2 * G - np0 - np1;
-      S.gs[0][a] = g.g1 ? __ldg(g.g1 + S.slot[a].x) : 1.0f;
-      S.gs[1][a] = g.g2 ? __ldg(g.g2 + S.slot[a].x) : 1.0f;
-    }
-  }
+// The code that runs right after the grid barriers (the FC2 activations and
+// the weighted un-permute) runs once per launch, so its first execution pays
+// for every instruction fetch.  The activation warp, idle during FC1, runs it
+// once without side effects (one element each, nothing stored, no barrier
+// arrival: the FC1 partials it reads are still being written and the result
+// is dropped), which brings that code into the SM's instruction cache.
+__device__ __noinline__ void warm_code(Shared &S, const LayerArgs &g, const DkPlan &P, uint16_t *pre) {
+  Cur c;
+  cur_begin(c, S, P, 1);
+  if (c.valid) prestage_body(S, g, P, c, pre, true);
+  finalize(S, g, P, true);
 }
 
 template <int FMT>
@@ -781,13 +814,13 @@ __device__ __noinline__ void consumer(Shared &S, const LayerArgs &g, const DkPla
   bool first_group_done = false;
   for (int f = 0; f < 2; ++f) {
     if (f == 1) {
-      build_tables(S, g, P);
-      grid_barrier(S, g, g.meta + 2);  // every FC1 partial is written (and the tables are in place)
+      grid_barrier(S, g, g.meta + 2);  // every FC1 partial is written
+      wait_bar(S, g, &S.tables_ready, 0u);
     }
     Cur c;
     cur_begin(c, S, P, f);
     if (f == 1 && c.valid) {  // the first FC2 activation group, while few registers are live
-      prestage_group(S, g, P, c, pre);
+      prestage_body(S, g, P, c, pre);
       first_group_done = true;
     }
     while (c.valid) {
@@ -818,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
       mbar_init(&S.xempty[i], kConsWarps);
     }
     mbar_init(&S.pre_ready, kCons);
+    mbar_init(&S.tables_ready, 32);
     mbar_fence_init();
     S.abort = 0;
   }
@@ -984,9 +1018,13 @@ qmoe_status make_dk_plan(int fmt, int T, int H, int I, int E, int k, DkPlan &P, 
   // and the per-row multiply-adds), a row chunk's start = pass.  With few
   // units per CTA the weight stream's latency, not the decode, sets a CTA's
   // time, and a unit costs nearly the same whatever its rows.
+  // FC2's weights are mostly in shared memory before its decode starts, so
+  // its units always cost by their rows.
   const double n1 = (double)(T * k) * P.f[0].ct * P.f[0].ku / (double)num_sms();
-  P.u0 = n1 < 16.0 ? 56 : 24;
-  P.u1 = n1 < 16.0 ? 8 : 40;
+  P.f[0].u0 = n1 < 16.0 ? 56 : 24;
+  P.f[0].u1 = n1 < 16.0 ? 8 : 40;
+  P.f[1].u0 = 24;
+  P.f[1].u1 = 40;
   P.pass = 48;
   // Partial rows: a fixed region of cap rows per CTA.  A CTA's range spans at
   // most two pairs that it shares with others (at most rows_max rows each)
@@ -997,8 +1035,8 @@ qmoe_status make_dk_plan(int fmt, int T, int H, int I, int E, int k, DkPlan &P, 
   const size_t R = (size_t)T * k, rows_max = std::min<size_t>((size_t)T, R);
   for (int f = 0; f < 2; ++f) {
     DkFc &F = P.f[f];
-    const double pc1 = (double)P.pass + (double)F.ku * (P.u0 + P.u1);
-    const double inner = std::ceil((double)F.ct * (double)R * pc1 / ((double)G * F.ku * P.u1)) + 1.0;
+    const double pc1 = (double)P.pass + (double)F.ku * (F.u0 + F.u1);
+    const double inner = std::ceil((double)F.ct * (double)R * pc1 / ((double)G * F.ku * F.u1)) + 1.0;
     F.cap = (int)std::min<double>((double)R * F.ct, 2.0 * (double)rows_max + inner);
   }
   p1_floats = G * (size_t)P.f[0].cap * P.f[0].NT;

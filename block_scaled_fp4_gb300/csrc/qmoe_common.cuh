@@ -165,11 +165,12 @@ struct DkFc {
   int rg_stride;  // bytes between row groups in a ring slot
   int sc_off;     // offset of the unit's scale rows in its slot
   int cap;        // partial rows one CTA's region holds
+  int u0, u1;     // split cost of a unit of an r-row expert: chunks * u0 + r * u1
 };
 struct DkPlan {
   DkFc f[2];
   int slot_bytes, win_off, pre_off, smem;  // dynamic shared memory: the ring at 0, windows, FC2 activations
-  int u0, u1, pass;                        // split costs: unit = chunks * u0 + rows * u1; row-chunk start = pass
+  int pass;                                // split cost of a row chunk's start
 };
 qmoe_status make_dk_plan(int fmt, int T, int H, int I, int E, int k, DkPlan &P, size_t &p1_floats,
                          size_t &p2_floats);

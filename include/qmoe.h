@@ -89,7 +89,18 @@ typedef enum {
      * any kernel of a forward call sets it to 1 when one of its bounded waits
      * gave up.  Only that word can become nonzero; it stays set until
      * qmoe_check_device_error reads and clears it. */
-    QMOE_WORKSPACE_PRIMED = 0x200
+    QMOE_WORKSPACE_PRIMED = 0x200,
+    /* Flag, OR'd with QMOE_SCALES_KMAJOR into the format of
+     * qmoe_fp4_moe_forward: a decode call (T * k <= QMOE_GEMV_MAX_ROWS) runs
+     * on the multi-row decode kernel whatever its size.  Without the flag the
+     * kernel is chosen by the length of the weight stream: when one SM's share
+     * of FC1 is under 16 units of 32 KB (e.g. 4 tokens, 256 experts, top-8,
+     * hidden 2048, intermediate 512) the one-row-per-pass kernel runs, whose
+     * stream starts sooner; longer streams run on the multi-row kernel, which
+     * decodes every row of an expert in one pass over its weights and copies
+     * column tiles as 2-D tensor copies.  Both give the layer within the same
+     * tolerance; the flag exists so that either can be run on any shape. */
+    QMOE_DECODE_MULTIROW = 0x400
 } qmoe_fp4_format;
 
 /* Bytes at the start of every forward workspace reserved for the decode

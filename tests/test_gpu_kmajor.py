@@ -1,6 +1,7 @@
 """k-major block scales on the GPU: the conversion is bit-exact against the
 oracle, and the layer on k-major scales matches the oracle (row-L2 relative
-error <= 1e-2) on every decode workload and on edge cases."""
+error <= 1e-2) on every decode workload and on edge cases, with the decode
+kernel chosen by the shape and with the multi-row kernel forced."""
 import numpy as np
 import pytest
 import torch
@@ -30,14 +31,15 @@ def test_scales_kmajor_full_size(qgpu, oracle):
     assert np.array_equal(got.cpu().numpy(), oracle.scales_kmajor(L["s1"]))
 
 
-def _check_kmajor(qgpu, oracle, wl, seed):
+def _check_kmajor(qgpu, oracle, wl, seed, multirow=False):
     L = syn.layer(wl, seed)
     d = to_dev(L)
     s1 = qgpu.scales_kmajor(d["s1"], wl.fmt)
     s2 = qgpu.scales_kmajor(d["s2"], wl.fmt)
     ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
     out = qgpu.moe_forward(d["x"], d["logits"], d["w1"], s1, d["g1"], d["w2"], s2, d["g2"],
-                           wl.fmt | qgpu.SCALES_KMAJOR, wl.k, wl.normalize, wl.alpha, wl.beta, wl.limit,
+                           wl.fmt | qgpu.SCALES_KMAJOR | (qgpu.DECODE_MULTIROW if multirow else 0), wl.k,
+                           wl.normalize, wl.alpha, wl.beta, wl.limit,
                            topk_ids=ids)
     torch.cuda.synchronize()
     ref = oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"],
@@ -47,9 +49,18 @@ def _check_kmajor(qgpu, oracle, wl, seed):
     assert err <= OUTPUT_RTOL, (wl.name, err, elem)
 
 
-@pytest.mark.parametrize("name", ["tiny_nvfp4_decode", "nvfp4_mtp_decode", "mxfp4_decode", "nvfp4_verify_edge"])
+DECODE = ["tiny_nvfp4_decode", "nvfp4_mtp_decode", "mxfp4_decode", "nvfp4_verify_edge"]
+
+
+@pytest.mark.parametrize("name", DECODE)
 def test_forward_kmajor_decode_workloads(qgpu, oracle, name):
     _check_kmajor(qgpu, oracle, syn.WORKLOADS[name], seed=0)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("name", DECODE)
+def test_forward_kmajor_multirow_workloads(qgpu, oracle, name, seed):
+    _check_kmajor(qgpu, oracle, syn.WORKLOADS[name], seed=seed, multirow=True)
 
 
 EDGE = [
@@ -63,13 +74,17 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("multirow", [False, True])
 @pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
-def test_forward_kmajor_edge_cases(qgpu, oracle, wl):
-    _check_kmajor(qgpu, oracle, wl, seed=13)
+def test_forward_kmajor_edge_cases(qgpu, oracle, wl, multirow):
+    _check_kmajor(qgpu, oracle, wl, seed=13, multirow=multirow)
 
 
 def test_kmajor_api_errors(qgpu):
     s = torch.zeros((2, 64, 4), dtype=torch.uint8, device="cuda")
+    with pytest.raises(qgpu.QMoEError) as ei:   # the multi-row kernel takes k-major scales only
+        qgpu.forward_workspace_bytes(4, 256, 128, 8, 2, qgpu.NVFP4 | qgpu.DECODE_MULTIROW)
+    assert ei.value.status == 3
     with pytest.raises(qgpu.QMoEError) as ei:   # dequant takes the page layout only
         qgpu.dequant(torch.zeros((2, 64, 32), dtype=torch.uint8, device="cuda"), s, None,
                      qgpu.NVFP4 | qgpu.SCALES_KMAJOR)
