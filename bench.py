@@ -37,9 +37,9 @@ WORKLOAD = "nvfp4_mtp_decode"
 # DRAM bytes (read + write) of one moe_layer_kernel launch on this workload,
 # from one ncu capture of the current kernel; None whenever the kernel changes
 # and has not been captured again.
-LAYER_TRAFFIC_BYTES = None
-LAYER_TRAFFIC_SOURCE = ("not captured for the current kernel (the build before its pass-prologue change: "
-                        "55,197,696 B per launch, 55.029 MB read + 0.169 MB written)")
+LAYER_TRAFFIC_BYTES = 55054336 + 395264
+LAYER_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one moe_layer_kernel launch of the "
+                        "current build (python bench.py --profile-case nvfp4_mtp_decode --layers 3; first layer)")
 LAYERS = 40
 METRIC = "us per MoE layer (NVFP4 MTP decode, T=4 E=256 top-8 H=2048 I=512)"
 UNIT = "us/layer"
@@ -392,6 +392,25 @@ def run_gpu(args):
 
 # ---------------------------------------------------------------- other decode configs
 
+# Which decode kernel each workload runs on with k-major scales (the library
+# picks by the length of one SM's FC1 stream: short streams run the
+# one-row-per-pass kernel, longer ones the multi-row kernel).
+DECODE_KERNEL = {
+    "tiny_nvfp4_decode": "moe_layer_kernel (one row per pass)",
+    "nvfp4_mtp_decode": "moe_layer_kernel (one row per pass)",
+    "mxfp4_decode": "moe_decode_kernel (multi-row)",
+    "nvfp4_verify_edge": "moe_decode_kernel (multi-row)",
+}
+# DRAM bytes (read + write) of one launch of each workload's kernel, from ncu
+# captures of the current kernels (per launch; the captured layer's active
+# experts differ from the bench's mean, so compare with that layer's bytes);
+# None where no capture of the current kernel exists.
+DECODE_TRAFFIC = {
+    "nvfp4_mtp_decode": {"bytes": 55054336 + 395264, "source": "ncu, first layer of --profile-case, --layers 3"},
+    "nvfp4_verify_edge": {"bytes": 750515200 + 10542336, "source": "ncu, first layer of --profile-case, --layers 3"},
+    "mxfp4_decode": {"bytes": 276891648 + 9066496, "source": "ncu, first layer of --profile-case, --layers 3"},
+}
+
 DECODE_CONFIGS = {
     # workload: (distinct layers per replay, why that many)
     "tiny_nvfp4_decode": (40, "0.44 MB of weights per layer: L2-resident whatever the rotation (launch-bound)"),
@@ -453,6 +472,8 @@ def bench_decode(device, workload: str, n_layers: int, steps: int, peak: float, 
     gbs = alg / (us * 1e-6) / 1e9
     res = {"workload": f"{workload}: T={wl.T} E={wl.E} k={wl.k} H={wl.H} I={wl.I} "
                        f"{'NVFP4' if wl.fmt == 0 else 'MXFP4'} SwiGLU",
+           "kernel": DECODE_KERNEL[workload] if kmajor else "moe_layer_kernel (scales as stored)",
+           "traffic": DECODE_TRAFFIC.get(workload) if kmajor else None,
            "us_per_layer": round(us, 3), "alg_bytes_per_layer": int(alg),
            "mean_active_experts": sum(act) / len(act), "achieved_gbs": round(gbs, 1), "peak": peak,
            "frac": round(gbs / peak, 4), "layers_per_replay": len(layers), "replays": steps,
@@ -713,6 +734,31 @@ def run_reference(args):
             "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case(workload: str, n_layers: int) -> None:
+    """A small case for ncu captures: n_layers distinct layers of one decode
+    workload (k-major scales, primed workspace), each run twice, eagerly."""
+    import torch
+    import block_scaled_fp4_gb300 as q
+    device = torch.device("cuda", torch.cuda.current_device())
+    q.build()
+    q.load()
+    wl, layers = make_layers(n_layers, seed=4321, device=device, workload=workload)
+    for L in layers:
+        L["s1"] = q.scales_kmajor(L["s1"], wl.fmt)
+        L["s2"] = q.scales_kmajor(L["s2"], wl.fmt)
+    fmt = wl.fmt | q.SCALES_KMAJOR | q.WORKSPACE_PRIMED
+    ws = torch.zeros(q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, fmt), dtype=torch.uint8,
+                     device=device)
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
+    for _ in range(2):
+        for i, L in enumerate(layers):
+            q.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"], L["g2"], fmt, wl.k,
+                          wl.normalize, wl.alpha, wl.beta, wl.limit, out=outs[i], workspace=ws)
+    torch.cuda.synchronize()
+    q.check_device_error(ws)
+    print(f"profile case {workload}: {n_layers} layers x 2, ok")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -731,7 +777,13 @@ def main(argv=None):
                     help="skip the other decode workloads, the page-layout line and the routing line")
     ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],
                     help="block-scale layout the layer reads (default: k-major, prepared once at load)")
+    ap.add_argument("--profile-case", default=None, choices=sorted(DECODE_KERNEL),
+                    help="profiler helper: run --layers layers of one decode workload twice, eagerly, and exit "
+                         "(no timing, no JSON line)")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        profile_case(args.profile_case, args.layers)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
