@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_scales_kmajor.argtypes = [P, i, i, i, P]
             L.oracle_route.restype = i
             L.oracle_route.argtypes = [P, i, i, i, i, P, P, P, P, P]
+            L.oracle_route_mixed.restype = i
+            L.oracle_route_mixed.argtypes = [P, P, i, i, i, i, P, P, P, P, P]
             L.oracle_expert_fc1.restype = i
             L.oracle_expert_fc1.argtypes = [P, i, P, P, P, i, i, i, P]
             L.oracle_expert_fc2.restype = i
@@ -74,7 +76,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_expert_ffn.restype = i
             L.oracle_expert_ffn.argtypes = [P, i, P, P, P, P, P, P, i, i, i, d, d, d, i, P]
             L.oracle_moe_forward.restype = i
-            L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, i,
+            L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, i,
                                              d, d, d, i, P, i, P, i]
             _lib = L
     return _lib
@@ -153,8 +155,13 @@ def scales_kmajor(scales) -> np.ndarray:
 
 # ---- routing -----------------------------------------------------------------
 
-def route(logits, k: int, normalize: int = 1) -> dict:
+def route(logits, k: int, normalize: int = 1, router_weights=None) -> dict:
+    """Top-k routing and the permute maps.  With ``router_weights`` [T, E]
+    (operator input 14) the logits only select and the mixing weights are
+    ``router_weights[t][id]`` gathered at the selected experts (renormalised
+    over the k when ``normalize``)."""
     logits = _c(logits, np.float32)
+    rw = None if router_weights is None else _c(router_weights, np.float32)
     T, E = logits.shape
     R = T * k
     ids = np.empty(R, np.int32)
@@ -162,8 +169,8 @@ def route(logits, k: int, normalize: int = 1) -> dict:
     off = np.empty(E + 1, np.int32)
     p2e = np.empty(max(R, 1), np.int32)
     e2p = np.empty(max(R, 1), np.int32)
-    _check(lib().oracle_route(_ptr(logits), T, E, k, normalize, _ptr(ids), _ptr(w),
-                              _ptr(off), _ptr(p2e), _ptr(e2p)), "route")
+    _check(lib().oracle_route_mixed(_ptr(logits), _ptr(rw), T, E, k, normalize, _ptr(ids), _ptr(w),
+                                    _ptr(off), _ptr(p2e), _ptr(e2p)), "route")
     return dict(ids=ids.reshape(T, k), weights=w.reshape(T, k), offsets=off,
                 perm_to_expanded=p2e[:R], expanded_to_perm=e2p[:R])
 
@@ -202,13 +209,16 @@ def expert_ffn(x_row, e, w1, s1, g1, w2, s2, g2, fmt, alpha=1.0, beta=0.0,
 
 
 def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt, k, normalize=1, alpha=1.0,
-                beta=0.0, limit=float("inf"), tokens=None, nthreads=None, fusion=1) -> np.ndarray:
+                beta=0.0, limit=float("inf"), tokens=None, nthreads=None, fusion=1,
+                router_weights=None) -> np.ndarray:
     """The whole layer.  x bf16 bits [T,H], logits f32 [T,E], fc1 packed
     [E,H,I] + scales [E,2I,H/bs] + global [E]/None, fc2 packed [E,I,H/2] +
     scales [E,H,I/bs] + global [E]/None.  ``fusion`` is swiglu_fusion: FC1's
     gate/linear columns interleaved (1, and 0 read as 1) or concatenated (2).
+    ``router_weights`` [T, E] or None: the mixing weights (see ``route``).
     Returns bf16 bits [len(tokens),H] (all T tokens when ``tokens`` is None)."""
     x, logits = _c(x, np.uint16), _c(logits, np.float32)
+    rw = None if router_weights is None else _c(router_weights, np.float32)
     w1, s1, g1 = _c(w1, np.uint8), _c(s1, np.uint8), _c(g1, np.float32)
     w2, s2, g2 = _c(w2, np.uint8), _c(s2, np.uint8), _c(g2, np.float32)
     T, H = x.shape
@@ -217,7 +227,7 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt, k, normalize=1, alpha=1.
     ntok = T if tok is None else len(tok)
     out = np.empty((ntok, H), np.uint16)
     nth = nthreads if nthreads else (os.cpu_count() or 1)
-    _check(lib().oracle_moe_forward(_ptr(x), _ptr(logits), _ptr(w1), _ptr(s1), _ptr(g1),
+    _check(lib().oracle_moe_forward(_ptr(x), _ptr(logits), _ptr(rw), _ptr(w1), _ptr(s1), _ptr(g1),
                                     _ptr(w2), _ptr(s2), _ptr(g2), fmt, T, H, I, E, k,
                                     normalize, alpha, beta, limit, fusion, _ptr(tok), ntok,
                                     _ptr(out), nth), "moe_forward")

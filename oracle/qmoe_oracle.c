@@ -34,6 +34,10 @@
  *    made on the fp32 logits (softmax is monotone); -0.0 == +0.0;
  *  - routing weights: softmax over all E experts, then (normalize != 0) divided
  *    by their sum over the k selected experts;
+ *  - with router_weights (input 14 of the operator schema, §2.3: "DeepSeek-
+ *    style routing", router_probs selects, router_weights gives the mixing
+ *    weights gathered at the selected experts): weight j = router_weights[t][id_j]
+ *    as given, then the same renormalisation over the k when normalize != 0;
  *  - expanded index i = t*k + j; rows of one expert keep ascending i;
  *  - FC1 columns: swiglu_fusion=1 interleaves them, 2m = gate and 2m+1 =
  *    linear; swiglu_fusion=2 concatenates them, m = gate and I+m = linear
@@ -187,14 +191,15 @@ static int key_cmp(const void *pa, const void *pb) {
 /* Top-k softmax routing and the permute-by-expert maps.
  *   ids[T*k], weights[T*k]: per token, the k experts in selection order and
  *       their routing weights (softmax over all E, renormalised over the k if
- *       normalize != 0);
+ *       normalize != 0); with router_weights [T, E] (may be NULL) the weights
+ *       are router_weights[t][ids[t*k+j]] instead, renormalised the same way;
  *   offsets[E+1]: first permuted row of each expert, offsets[E] = T*k;
  *   expanded_to_perm[T*k]: permuted row of expanded index i = t*k + j;
  *   perm_to_expanded[T*k]: its inverse.
  * Any of the map outputs may be NULL. */
-int oracle_route(const float *logits, int T, int E, int k, int normalize,
-                 int32_t *ids, double *weights, int32_t *offsets,
-                 int32_t *perm_to_expanded, int32_t *expanded_to_perm) {
+int oracle_route_mixed(const float *logits, const float *router_weights, int T, int E, int k, int normalize,
+                       int32_t *ids, double *weights, int32_t *offsets,
+                       int32_t *perm_to_expanded, int32_t *expanded_to_perm) {
     int t, j, e, i, R = T * k;
     key_t_ *keys;
     int32_t *count, *seen;
@@ -210,7 +215,9 @@ int oracle_route(const float *logits, int T, int E, int k, int normalize,
         for (e = 0; e < E; ++e) den += exp((double)row[e] - mx);
         for (j = 0; j < k; ++j) {
             ids[t * k + j] = keys[j].idx;
-            if (weights) weights[t * k + j] = exp((double)row[keys[j].idx] - mx) / den;
+            if (weights)
+                weights[t * k + j] = router_weights ? (double)router_weights[(size_t)t * E + keys[j].idx]
+                                                    : exp((double)row[keys[j].idx] - mx) / den;
         }
         if (weights && normalize) {
             for (j = 0; j < k; ++j) sel += weights[t * k + j];
@@ -240,6 +247,13 @@ int oracle_route(const float *logits, int T, int E, int k, int normalize,
     free(count);
     free(seen);
     return ORACLE_OK;
+}
+
+int oracle_route(const float *logits, int T, int E, int k, int normalize,
+                 int32_t *ids, double *weights, int32_t *offsets,
+                 int32_t *perm_to_expanded, int32_t *expanded_to_perm) {
+    return oracle_route_mixed(logits, NULL, T, E, k, normalize, ids, weights, offsets, perm_to_expanded,
+                              expanded_to_perm);
 }
 
 /* ---- activation ---------------------------------------------------------- */
@@ -315,9 +329,10 @@ int oracle_expert_ffn(const uint16_t *x_row, int e,
 
 /* The whole layer for the tokens listed in `tokens` (NULL: all T tokens, in
  * order): out[r][h] = bf16( sum_j w[t][j] * FFN_{id[t][j]}(x[t])[h] ) for the
- * r-th listed token t.  Routing uses the full logits row of each token.
+ * r-th listed token t.  Routing uses the full logits row of each token; the
+ * mixing weights come from router_weights when it is not NULL.
  * `nthreads` > 0 caps the OpenMP threads used over the (token, j) pairs. */
-int oracle_moe_forward(const uint16_t *x, const float *logits,
+int oracle_moe_forward(const uint16_t *x, const float *logits, const float *router_weights,
                        const uint8_t *w1, const uint8_t *s1, const float *g1,
                        const uint8_t *w2, const uint8_t *s2, const float *g2,
                        int fmt, int T, int H, int I, int E, int k, int normalize,
@@ -340,7 +355,7 @@ int oracle_moe_forward(const uint16_t *x, const float *logits,
     npairs = ntok * k;
     y = (double *)malloc(sizeof(double) * (size_t)npairs * H + 1);
     if (!ids || !wts || !y) { free(ids); free(wts); free(y); return ORACLE_BAD_ARG; }
-    oracle_route(logits, T, E, k, normalize, ids, wts, NULL, NULL, NULL);
+    oracle_route_mixed(logits, router_weights, T, E, k, normalize, ids, wts, NULL, NULL, NULL);
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
     for (pidx = 0; pidx < npairs; ++pidx) {
         int rr = pidx / k, j = pidx % k;

@@ -23,7 +23,7 @@ def _bf16_round(a):
     return torch.from_numpy(np.asarray(a, np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def _dense_layer(oracle, L, wl, fusion=1):
+def _dense_layer(oracle, L, wl, fusion=1, router_weights=None):
     x = torch.from_numpy(_f(L["x"]))
     W1 = torch.from_numpy(_f(oracle.dequant(L["w1"], L["s1"], L["g1"], wl.fmt)))  # [E,2I,H]
     W2 = torch.from_numpy(_f(oracle.dequant(L["w2"], L["s2"], L["g2"], wl.fmt)))  # [E,H,I]
@@ -35,6 +35,8 @@ def _dense_layer(oracle, L, wl, fusion=1):
         mx = max(row)
         den = math.fsum(math.exp(v - mx) for v in row)
         p = [math.exp(row[e] - mx) / den for e in order]
+        if router_weights is not None:  # selection by the logits, mixing by router_weights
+            p = [float(router_weights[t][e]) for e in order]
         if wl.normalize:
             s = math.fsum(p)
             p = [v / s for v in p]
@@ -179,3 +181,40 @@ def test_concatenated_fc1_helper_moves_columns():
         for k in range(H):
             code = (int(w1c[0, k, c // 2]) >> (4 * (c % 2))) & 0xF
             assert code == ((src + 1) if src % H == k else 0)
+
+
+# ---- router_weights (operator input 14): the logits select, router_weights mix ----
+
+@pytest.mark.parametrize("wl", CASES[:3], ids=lambda w: w.name)
+def test_router_weights_layer_matches_dense_brute_force(oracle, wl):
+    L = syn.layer(wl, seed=5)
+    rw = np.random.default_rng(11).uniform(0.05, 2.0, (wl.T, wl.E)).astype(np.float32)
+    got = _f(oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"],
+                                L["s2"], L["g2"], wl.fmt, wl.k, wl.normalize, wl.alpha,
+                                wl.beta, wl.limit, router_weights=rw))
+    ref = _dense_layer(oracle, L, wl, router_weights=rw)
+    ref_bf = _bf16_round(ref)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
+    assert np.all(np.abs(got - ref_bf) <= ulp + 1e-300)
+    # and the mixing weights matter: the default path gives another layer
+    base = _f(oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"],
+                                 L["s2"], L["g2"], wl.fmt, wl.k, wl.normalize, wl.alpha,
+                                 wl.beta, wl.limit))
+    assert not np.array_equal(base, got)
+
+
+def test_router_weights_one_hot_is_one_expert(oracle):
+    """router_weights 1 at each token's first selected expert and 0 elsewhere
+    (no renormalisation): the layer is that one expert's FFN, exactly."""
+    wl = syn.small("rw1", T=2, E=5, k=3, H=32, I=32, fmt=MX, normalize=0)
+    L = syn.layer(wl, seed=9)
+    ids = oracle.route(L["logits"], wl.k, 0)["ids"]
+    rw = np.zeros((wl.T, wl.E), np.float32)
+    for t in range(wl.T):
+        rw[t, ids[t, 0]] = 1.0
+    out = oracle.moe_forward(L["x"], L["logits"], L["w1"], L["s1"], L["g1"], L["w2"], L["s2"],
+                             L["g2"], MX, wl.k, 0, router_weights=rw)
+    for t in range(wl.T):
+        y = oracle.expert_ffn(L["x"][t], int(ids[t, 0]), L["w1"], L["s1"], L["g1"], L["w2"],
+                              L["s2"], L["g2"], MX)
+        assert np.array_equal(out[t], np.array([oracle.bf16_rne(v) for v in y], np.uint16))

@@ -91,3 +91,42 @@ def test_maps_are_stable_rank_by_expert(oracle, T, E, k):
     inv = np.empty_like(r["perm_to_expanded"])
     inv[r["perm_to_expanded"]] = np.arange(T * k)
     assert np.array_equal(r["expanded_to_perm"], inv)
+
+
+# ---- router_weights (operator input 14) -------------------------------------------
+
+@pytest.mark.parametrize("normalize", [0, 1])
+def test_router_weights_gathered_at_the_selection(oracle, normalize):
+    """The logits alone select (same ids as without router_weights); the weights
+    are router_weights at the selected experts, renormalised over the k when
+    asked (brute force with Python's sort and math.fsum)."""
+    rng = np.random.default_rng(21)
+    logits = rng.standard_normal((5, 33)).astype(np.float32)
+    rw = rng.uniform(0.01, 3.0, (5, 33)).astype(np.float32)
+    r = oracle.route(logits, 8, normalize, router_weights=rw)
+    ids, _ = _brute(logits, 8, normalize)
+    assert np.array_equal(r["ids"], ids)
+    assert np.array_equal(r["ids"], oracle.route(logits, 8, normalize)["ids"])
+    for t in range(5):
+        p = [float(rw[t][e]) for e in ids[t]]
+        if normalize:
+            s = math.fsum(p)
+            p = [v / s for v in p]
+        assert np.allclose(r["weights"][t], p, rtol=1e-15, atol=0)
+
+
+def test_router_weights_special_cases(oracle):
+    rng = np.random.default_rng(22)
+    logits = rng.standard_normal((3, 16)).astype(np.float32)
+    const = np.full((3, 16), 0.375, np.float32)
+    assert np.all(oracle.route(logits, 4, 1, router_weights=const)["weights"] == 0.25)  # 1/k exactly
+    assert np.all(oracle.route(logits, 4, 0, router_weights=const)["weights"] == 0.375)
+    # the softmax of the logits as router_weights gives the default weights
+    # (up to the fp32 rounding of the supplied probabilities)
+    l64 = logits.astype(np.float64)
+    prob = np.exp(l64 - l64.max(1, keepdims=True))
+    prob = (prob / prob.sum(1, keepdims=True)).astype(np.float32)
+    for normalize in (0, 1):
+        a = oracle.route(logits, 4, normalize, router_weights=prob)["weights"]
+        b = oracle.route(logits, 4, normalize)["weights"]
+        assert np.allclose(a, b, rtol=2e-7, atol=0)
