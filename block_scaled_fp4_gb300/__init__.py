@@ -66,9 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
             L = ctypes.CDLL(p)
             P, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_size_t)
             L.qmoe_route_topk.restype = i
-            L.qmoe_route_topk.argtypes = [P, i, i, i, i, P, P, P, P, P, P, sz, P]
+            L.qmoe_route_topk.argtypes = [P, P, i, i, i, i, P, P, P, P, P, P, sz, P]
             L.qmoe_fp4_moe_forward.restype = i
-            L.qmoe_fp4_moe_forward.argtypes = [P, P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
+            L.qmoe_fp4_moe_forward.argtypes = [P, P, P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
                                                f, f, f, P, P, P, sz, P]
             L.qmoe_fp4_dequant.restype = i
             L.qmoe_fp4_dequant.argtypes = [P, P, P, i, i, i, i, P, P]
@@ -113,12 +113,15 @@ def _cuda(t, name):
     return t
 
 
-def route_topk(logits, k: int, normalize: int = 1, stream=None):
+def route_topk(logits, k: int, normalize: int = 1, stream=None, router_weights=None):
     """Top-k softmax routing + permute-by-expert maps.  Returns a dict of
     CUDA tensors: ids [T,k] int32, weights [T,k] f32, offsets [E+1],
-    perm_to_expanded [T*k], expanded_to_perm [T*k]."""
+    perm_to_expanded [T*k], expanded_to_perm [T*k].  ``router_weights``
+    f32 [T,E] (optional): the mixing weights, gathered at the experts the
+    logits select."""
     import torch
     _cuda(logits, "logits")
+    _cuda(router_weights, "router_weights")
     T, E = logits.shape
     dev = logits.device
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -127,7 +130,7 @@ def route_topk(logits, k: int, normalize: int = 1, stream=None):
     p2e = torch.empty(T * k, dtype=torch.int32, device=dev)
     e2p = torch.empty(T * k, dtype=torch.int32, device=dev)
     nbytes = ctypes.c_size_t(0)
-    _check(load().qmoe_route_topk(_ptr(logits), T, E, k, int(normalize), _ptr(ids), _ptr(w),
+    _check(load().qmoe_route_topk(_ptr(logits), _ptr(router_weights), T, E, k, int(normalize), _ptr(ids), _ptr(w),
                                   _ptr(off), _ptr(p2e), _ptr(e2p), None, ctypes.byref(nbytes),
                                   _stream(stream)))
     return dict(ids=ids, weights=w, offsets=off, perm_to_expanded=p2e, expanded_to_perm=e2p)
@@ -137,7 +140,7 @@ def forward_workspace_bytes(T, H, I, E, k, fmt=NVFP4, with_dequantized=False) ->
     """Workspace bytes ``moe_forward`` needs for these sizes."""
     nbytes = ctypes.c_size_t(0)
     dummy = ctypes.c_void_p(16)
-    _check(load().qmoe_fp4_moe_forward(None, dummy, None, None, None, None, None, None,
+    _check(load().qmoe_fp4_moe_forward(None, dummy, None, None, None, None, None, None, None,
                                        dummy if with_dequantized else None,
                                        dummy if with_dequantized else None, fmt, T, H, I, E, k, 1, 1,
                                        1.0, 0.0, math.inf, None, None, None, ctypes.byref(nbytes),
@@ -148,15 +151,17 @@ def forward_workspace_bytes(T, H, I, E, k, fmt=NVFP4, with_dequantized=False) ->
 def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: int = 1,
                 alpha: float = 1.0, beta: float = 0.0, limit: float = math.inf,
                 w1_dequant=None, w2_dequant=None, out=None, topk_ids=None, workspace=None,
-                stream=None, swiglu_fusion: int = 1):
+                stream=None, swiglu_fusion: int = 1, router_weights=None):
     """The MoE layer.  x bf16 [T,H]; logits f32 [T,E]; w1 uint8 [E,H,I];
     s1 uint8 [E,2I,H/bs]; g1 f32 [E] or None; w2 uint8 [E,I,H/2];
     s2 uint8 [E,H,I/bs]; g2 f32 [E] or None.  With ``fmt | SCALES_KMAJOR``
     s1 is [E,H/bs,2I] and s2 [E,I/bs,H] (see ``scales_kmajor``).
-    Returns out bf16 [T,H]."""
+    ``router_weights`` f32 [T,E] (optional): the mixing weights, gathered at
+    the experts the logits select.  Returns out bf16 [T,H]."""
     import torch
     for t, n in ((x, "x"), (logits, "logits"), (w1, "w1"), (s1, "s1"), (g1, "g1"), (w2, "w2"),
-                 (s2, "s2"), (g2, "g2"), (w1_dequant, "w1_dequant"), (w2_dequant, "w2_dequant")):
+                 (s2, "s2"), (g2, "g2"), (w1_dequant, "w1_dequant"), (w2_dequant, "w2_dequant"),
+                 (router_weights, "router_weights")):
         _cuda(t, n)
     T, H = x.shape
     E, _, I = w1.shape
@@ -166,7 +171,8 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: 
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     nbytes = ctypes.c_size_t(workspace.numel() * workspace.element_size())
-    _check(load().qmoe_fp4_moe_forward(_ptr(x), _ptr(logits), _ptr(w1), _ptr(s1), _ptr(g1), _ptr(w2),
+    _check(load().qmoe_fp4_moe_forward(_ptr(x), _ptr(logits), _ptr(router_weights), _ptr(w1), _ptr(s1),
+                                       _ptr(g1), _ptr(w2),
                                        _ptr(s2), _ptr(g2), _ptr(w1_dequant), _ptr(w2_dequant), fmt, T,
                                        H, I, E, k, int(normalize), int(swiglu_fusion), float(alpha),
                                        float(beta), float(limit), _ptr(out), _ptr(topk_ids),

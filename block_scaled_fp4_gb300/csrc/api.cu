@@ -99,7 +99,8 @@ extern "C" int qmoe_set_stage_events(cudaEvent_t *events, int n_events) {
   return 1;
 }
 
-extern "C" qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normalize, int32_t *topk_ids,
+extern "C" qmoe_status qmoe_route_topk(const float *logits, const float *router_weights, int T, int E, int k,
+                                       int normalize, int32_t *topk_ids,
                                        float *topk_weights, int32_t *expert_offsets, int32_t *perm_to_expanded,
                                        int32_t *expanded_to_perm, void *workspace, size_t *workspace_bytes,
                                        cudaStream_t stream) {
@@ -112,7 +113,9 @@ extern "C" qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k,
   if (!topk_ids && !topk_weights && !expert_offsets && !perm_to_expanded && !expanded_to_perm) return QMOE_OK;
   QMOE_REQUIRE(topk_ids && topk_weights && expert_offsets && perm_to_expanded && expanded_to_perm,
                QMOE_ERR_INVALID_ARG, "an output pointer is NULL");
+  QMOE_REQUIRE(((uintptr_t)router_weights & 3u) == 0, QMOE_ERR_MISALIGNED, "router_weights must be 4-byte aligned");
   RouteOut o{};
+  o.mix = router_weights;
   o.ids = topk_ids;
   o.weights = topk_weights;
   o.offsets = expert_offsets;
@@ -217,7 +220,8 @@ static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k,
 // T * k > QMOE_GEMV_MAX_ROWS: route, dequantise (unless given), grouped GEMMs,
 // weighted un-permute.  Arguments already checked by the caller: routing
 // sizes, format, H and I, swiglu_fusion, alpha / beta / limit.
-static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w, const uint8_t *fc1_s,
+static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const float *mix, const uint8_t *fc1_w,
+                                   const uint8_t *fc1_s,
                                    const float *fc1_g, const uint8_t *fc2_w, const uint8_t *fc2_s, const float *fc2_g,
                                    const uint16_t *fc1_wd, const uint16_t *fc2_wd, int fmt, bool kmajor, int T, int H,
                                    int I, int E, int k, int normalize, int fusion, float alpha, float beta,
@@ -244,6 +248,7 @@ static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const
                QMOE_ERR_MISALIGNED, "global scales must be 4-byte aligned");
   const PrefillLayout L = prefill_layout(workspace, T, H, I, E, k, bs, need_w1, need_w2, kmajor);
   RouteOut ro{};
+  ro.mix = mix;
   ro.ids = topk_ids_out ? topk_ids_out : L.ids;
   ro.weights = L.weights;
   ro.offsets = L.offsets;
@@ -307,7 +312,8 @@ extern "C" qmoe_status qmoe_check_device_error(void *workspace, cudaStream_t str
   return QMOE_ERR_DEVICE;
 }
 
-extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const uint8_t *fc1_w,
+extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const float *router_weights,
+                                            const uint8_t *fc1_w,
                                             const uint8_t *fc1_s, const float *fc1_g, const uint8_t *fc2_w,
                                             const uint8_t *fc2_s, const float *fc2_g, const uint16_t *fc1_wd,
                                             const uint16_t *fc2_wd, qmoe_fp4_format fmt, int T, int H, int I, int E,
@@ -318,6 +324,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   qmoe_status st = check_route_args(logits, T, E, k);
   if (st != QMOE_OK) return st;
   QMOE_REQUIRE(workspace_bytes, QMOE_ERR_INVALID_ARG, "workspace_bytes is NULL");
+  QMOE_REQUIRE(((uintptr_t)router_weights & 3u) == 0, QMOE_ERR_MISALIGNED, "router_weights must be 4-byte aligned");
   const bool kmajor = (fmt & QMOE_SCALES_KMAJOR) != 0;
   const bool primed = (fmt & QMOE_WORKSPACE_PRIMED) != 0;
   const bool multirow = (fmt & QMOE_DECODE_MULTIROW) != 0;
@@ -336,7 +343,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
                "alpha, beta and limit must not be NaN");
   const long long R = (long long)T * k;
   if (R > QMOE_GEMV_MAX_ROWS)
-    return prefill_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, fc1_wd, fc2_wd, base_fmt, kmajor, T, H,
+    return prefill_forward(x, logits, router_weights, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, fc1_wd, fc2_wd, base_fmt, kmajor, T, H,
                            I, E, k, normalize, fusion, alpha, beta, limit, out, topk_ids_out, workspace,
                            workspace_bytes, stream);
   QMOE_REQUIRE(H <= 16384 && I <= 16384, QMOE_ERR_UNSUPPORTED, "decode path needs H, I <= 16384");
@@ -379,7 +386,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logi
   g.fmt = base_fmt;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k;
   g.alpha = alpha; g.beta = beta; g.limit = limit; g.fusion = fusion;
-  g.logits = logits; g.normalize = normalize; g.route_n = route_keys_per_lane(E, k);
+  g.logits = logits; g.mix = router_weights; g.normalize = normalize; g.route_n = route_keys_per_lane(E, k);
   g.ids_out = topk_ids_out;
   g.x = x;
   g.w1 = fc1_w; g.s1 = fc1_s; g.g1 = fc1_g;

@@ -865,10 +865,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
   // experts in every CTA): warp w routes tokens w, w + 18, ...
   const int R = g.T * g.k;
   for (int t = warp; t < g.T; t += kThreads / 32) {
-    if (g.route_n == 1) route_one_token<1>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
-    else if (g.route_n == 2) route_one_token<2>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
-    else if (g.route_n == 4) route_one_token<4>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
-    else route_one_token<8>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    if (g.route_n == 1) route_one_token<1>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else if (g.route_n == 2) route_one_token<2>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else if (g.route_n == 4) route_one_token<4>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else route_one_token<8>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
   }
   __syncthreads();
   {

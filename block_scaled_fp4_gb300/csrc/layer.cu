@@ -1017,10 +1017,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const __gri
   // cost prefix of both FCs over those slots.
   const int R = g.T * g.k;
   for (int t = warp; t < g.T; t += kLayerThreads / 32) {
-    if (g.route_n == 1) route_one_token<1>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
-    else if (g.route_n == 2) route_one_token<2>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
-    else if (g.route_n == 4) route_one_token<4>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
-    else route_one_token<8>(g.logits, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    if (g.route_n == 1) route_one_token<1>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else if (g.route_n == 2) route_one_token<2>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else if (g.route_n == 4) route_one_token<4>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
+    else route_one_token<8>(g.logits, g.mix, t, g.E, g.k, g.normalize, S.r_ids, S.r_w);
   }
   __syncthreads();
   if (warp == 0) {

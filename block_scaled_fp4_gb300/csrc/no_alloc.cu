@@ -70,7 +70,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const fl
                                                      int32_t *topk_ids_out, cudaStream_t stream) {
   // How much scratch this call needs (validates the sizes, launches nothing).
   size_t need = 0;
-  qmoe_status st = qmoe_fp4_moe_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, nullptr, nullptr, fmt,
+  qmoe_status st = qmoe_fp4_moe_forward(x, logits, nullptr, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, nullptr, nullptr, fmt,
                                         T, H, I, E, k, normalize, swiglu_fusion, alpha, beta, limit, out,
                                         topk_ids_out, nullptr, &need, stream);
   if (st != QMOE_OK) return st;
@@ -87,7 +87,7 @@ extern "C" qmoe_status qmoe_fp4_moe_forward_no_alloc(const uint16_t *x, const fl
   // The array is zero when the module loads and its header stays zero between
   // calls (decode kernels leave it so; the prefill path never writes it).
   const qmoe_fp4_format primed = (qmoe_fp4_format)((int)fmt | (int)QMOE_WORKSPACE_PRIMED);
-  return qmoe_fp4_moe_forward(x, logits, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, nullptr, nullptr, primed, T, H,
+  return qmoe_fp4_moe_forward(x, logits, nullptr, fc1_w, fc1_s, fc1_g, fc2_w, fc2_s, fc2_g, nullptr, nullptr, primed, T, H,
                               I, E, k, normalize, swiglu_fusion, alpha, beta, limit, out, topk_ids_out, scratch,
                               &have, stream);
 }

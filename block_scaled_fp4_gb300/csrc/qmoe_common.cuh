@@ -96,6 +96,7 @@ qmoe_status no_alloc_scratch(void **addr);
 constexpr int kFusedRouteMaxTokens = 64;
 
 struct RouteOut {
+  const float *mix;    // [T, E] router_weights (mixing weights gathered at the selection), or null
   int32_t *ids;        // [T*k]
   float *weights;      // [T*k]
   int32_t *offsets;    // [E+1]
@@ -114,6 +115,7 @@ struct LayerArgs {
   float alpha, beta, limit;
   int fusion;              // FC1 gate/linear columns: 1 interleaved (2m, 2m + 1), 2 concatenated (m, I + m)
   const float *logits;     // fp32 [T, E] router logits
+  const float *mix;        // fp32 [T, E] router_weights (mixing weights), or null
   int normalize, route_n;  // routing: renormalise over the k; keys per lane (1, 2, 4, 8)
   int32_t *ids_out;        // [T, k] selected experts, or null
   const uint16_t *x;       // bf16 [T, H]

@@ -14,12 +14,13 @@
 namespace qmoe {
 
 template <int N>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T, int E, int k,
+__global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits,
+                                                        const float *__restrict__ mix, int T, int E, int k,
                                                         int normalize, int32_t *__restrict__ ids,
                                                         float *__restrict__ weights) {
   const int warps = blockDim.x >> 5;
   const int t = blockIdx.x * warps + (int)(threadIdx.x >> 5);
-  if (t < T) route_one_token<N>(logits, t, E, k, normalize, ids, weights);
+  if (t < T) route_one_token<N>(logits, mix, t, E, k, normalize, ids, weights);
 }
 
 // Stable ranking of the R = T*k assignments by expert, done by one CTA.
@@ -106,12 +107,12 @@ __global__ void __launch_bounds__(256) route_maps_fused_kernel(const float *__re
   const int R = T * k;
   if (R <= 64) {
     int32_t *ids_s = smem_i32, *cnt = smem_i32 + 64, *off = cnt + E;
-    for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights, ids_s);
+    for (int t = w; t < T; t += W) route_one_token<N>(logits, o.mix, t, E, k, normalize, o.ids, o.weights, ids_s);
     __syncthreads();
     if (w == 0) build_maps_small(ids_s, R, E, o, cnt, off);
     return;
   }
-  for (int t = w; t < T; t += W) route_one_token<N>(logits, t, E, k, normalize, o.ids, o.weights);
+  for (int t = w; t < T; t += W) route_one_token<N>(logits, o.mix, t, E, k, normalize, o.ids, o.weights);
   __syncthreads();
   build_maps(o.ids, R, E, o.offsets, o.p2e, o.e2p, smem_i32, smem_i32 + W * E);
 }
@@ -142,8 +143,8 @@ static cudaError_t launch_route_n(const float *logits, int T, int E, int k, int 
     return cudaGetLastError();
   }
   const int warps = 8;
-  route_topk_kernel<N><<<(T + warps - 1) / warps, warps * 32, 0, stream>>>(logits, T, E, k, normalize, o.ids,
-                                                                            o.weights);
+  route_topk_kernel<N><<<(T + warps - 1) / warps, warps * 32, 0, stream>>>(logits, o.mix, T, E, k, normalize,
+                                                                            o.ids, o.weights);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int threads = 1024, W = threads / 32;

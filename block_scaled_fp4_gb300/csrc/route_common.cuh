@@ -89,10 +89,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One warp routes token t: ids/weights for its k experts.
+// One warp routes token t: ids/weights for its k experts.  With mix (the
+// operator's router_weights, [T, E], input 14 of "MoE and QMoE - CUDA
+// Operator Documentation" §2.3) the logits only select and the weights are
+// mix[t][id] gathered at the selected experts, renormalised over the k like
+// the softmax weights when normalize is set.
 template <int N>
-__device__ __forceinline__ void route_one_token(const float *__restrict__ logits, int t, int E, int k,
-                                                int normalize, int32_t *__restrict__ ids,
+__device__ __forceinline__ void route_one_token(const float *__restrict__ logits, const float *__restrict__ mix, int t,
+                                                int E, int k, int normalize, int32_t *__restrict__ ids,
                                                 float *__restrict__ weights, int32_t *ids_smem = nullptr) {
   const int lane = (int)lane_id();
   const float *row = logits + (size_t)t * E;
@@ -109,7 +113,7 @@ __device__ __forceinline__ void route_one_token(const float *__restrict__ logits
   warp_topk_keys<N>(key, k, top);
   const float mx = key_logit(top[0]);
   float s = 0.f;  // softmax denominator over all E (not needed when the k weights are renormalised)
-  if (!normalize) {
+  if (!normalize && !mix) {
 #pragma unroll
     for (int i = 0; i < N; ++i)
       if (lane + 32 * i < E) s += expf(v[i] - mx);
@@ -122,7 +126,7 @@ __device__ __forceinline__ void route_one_token(const float *__restrict__ logits
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     if (j < k) {
-      const float ej = expf(key_logit(top[j]) - mx);
+      const float ej = mix ? __ldg(mix + (size_t)t * E + key_expert(top[j])) : expf(key_logit(top[j]) - mx);
       sel_sum += ej;
       if (j == lane) { mine_e = ej; mine_id = key_expert(top[j]); }
     }
@@ -130,7 +134,7 @@ __device__ __forceinline__ void route_one_token(const float *__restrict__ logits
   if (lane < k) {
     ids[(size_t)t * k + lane] = mine_id;
     if (ids_smem) ids_smem[t * k + lane] = mine_id;
-    weights[(size_t)t * k + lane] = normalize ? mine_e / sel_sum : mine_e / s;
+    weights[(size_t)t * k + lane] = normalize ? mine_e / sel_sum : (mix ? mine_e : mine_e / s);
   }
 }
 

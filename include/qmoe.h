@@ -119,9 +119,15 @@ typedef enum {
  * (warp top-k with a stable tie-break, renormalised weights, stable ranking of
  * the T*k assignments by expert).
  *
- *   logits           fp32 [T, E] router logits.
+ *   logits           fp32 [T, E] router logits (router_probs): they select.
+ *   router_weights   fp32 [T, E] mixing weights, or NULL (operator doc §2.3,
+ *                    input 14: "DeepSeek-style routing", router_probs select
+ *                    and router_weights, gathered at the selected experts,
+ *                    mix).  NULL: the softmax of the logits mixes.  4-byte
+ *                    aligned.
  *   T, E, k          tokens (>= 1), experts (1..256), experts per token (1..min(8, E)).
- *   normalize        0: weight = softmax over all E at the selected expert;
+ *   normalize        0: weight = softmax over all E at the selected expert
+ *                    (with router_weights: router_weights[t][expert]);
  *                    != 0: those k weights divided by their sum.
  *   topk_ids         int32 [T, k] out: selected experts per token, ordered by
  *                    (logit descending, expert index ascending).
@@ -136,7 +142,7 @@ typedef enum {
  * Selection is exact (made on the fp32 logits; -0.0 and +0.0 compare equal).
  * NaN logits are outside the contract.
  */
-qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normalize,
+qmoe_status qmoe_route_topk(const float *logits, const float *router_weights, int T, int E, int k, int normalize,
                             int32_t *topk_ids, float *topk_weights,
                             int32_t *expert_offsets, int32_t *perm_to_expanded,
                             int32_t *expanded_to_perm,
@@ -155,6 +161,8 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  *
  *   x            bf16 [T, H] activations.
  *   logits       fp32 [T, E] router logits (routed as in qmoe_route_topk).
+ *   router_weights fp32 [T, E] mixing weights gathered at the selected
+ *                experts, or NULL (as in qmoe_route_topk).
  *   fc1_w        uint8 [E, H, I]  packed e2m1, K = H, N = 2I.
  *   fc1_s        uint8 [E, 2I, H/bs] block scales ([E, H/bs, 2I] with
  *                QMOE_SCALES_KMAJOR).
@@ -201,7 +209,7 @@ qmoe_status qmoe_route_topk(const float *logits, int T, int E, int k, int normal
  * un-permute.  Numerically the two paths agree within the tolerance of fp32
  * accumulation, not bit for bit.
  */
-qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits,
+qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const float *router_weights,
                                  const uint8_t *fc1_w, const uint8_t *fc1_s, const float *fc1_g,
                                  const uint8_t *fc2_w, const uint8_t *fc2_s, const float *fc2_g,
                                  const uint16_t *fc1_wd, const uint16_t *fc2_wd,

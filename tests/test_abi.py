@@ -68,12 +68,12 @@ def _in_child_without_gpu(body: str) -> None:
 
 def _fwd(L, **kw):
     P = ctypes.c_void_p
-    a = dict(x=P(256), logits=P(256), w1=P(256), s1=P(256), g1=None, w2=P(256), s2=P(256), g2=None,
+    a = dict(x=P(256), logits=P(256), rw=None, w1=P(256), s1=P(256), g1=None, w2=P(256), s2=P(256), g2=None,
              wd1=None, wd2=None, fmt=0, T=4, H=2048, I=512, E=256, k=8, normalize=1, fusion=1,
              alpha=1.0, beta=0.0, limit=math.inf, out=P(256), ids=None, ws=None)
     a.update(kw)
     nb = ctypes.c_size_t(a.pop("nbytes", 0))
-    rc = L.qmoe_fp4_moe_forward(a["x"], a["logits"], a["w1"], a["s1"], a["g1"], a["w2"], a["s2"],
+    rc = L.qmoe_fp4_moe_forward(a["x"], a["logits"], a["rw"], a["w1"], a["s1"], a["g1"], a["w2"], a["s2"],
                                 a["g2"], a["wd1"], a["wd2"], a["fmt"], a["T"], a["H"], a["I"], a["E"],
                                 a["k"], a["normalize"], a["fusion"], a["alpha"], a["beta"],
                                 a["limit"], a["out"], a["ids"], a["ws"], ctypes.byref(nb), None)
@@ -95,6 +95,8 @@ def check_forward_validation(L):
     assert _fwd(L, fusion=0) == (0, need)                         # read as interleaved
     assert _fwd(L, fmt=2)[0] == 3
     assert _fwd(L, alpha=float("nan"))[0] == 1
+    assert _fwd(L, rw=ctypes.c_void_p(258))[0] == 2               # router_weights not 4-byte aligned
+    assert _fwd(L, rw=ctypes.c_void_p(256)) == (0, need)          # router_weights: same workspace
     ws = ctypes.c_void_p(1 << 20)
     assert _fwd(L, ws=ws, nbytes=need - 1)[0] == 4                # workspace too small
     assert _fwd(L, ws=ws, nbytes=need, x=ctypes.c_void_p(258))[0] == 2   # misaligned
@@ -109,11 +111,13 @@ def test_forward_validation(qm):
 def check_route_and_dequant_validation(L):
     P = ctypes.c_void_p
     nb = ctypes.c_size_t(99)
-    assert L.qmoe_route_topk(P(256), 4, 256, 8, 1, None, None, None, None, None, None,
+    assert L.qmoe_route_topk(P(256), None, 4, 256, 8, 1, None, None, None, None, None, None,
                              ctypes.byref(nb), None) == 0 and nb.value == 0
-    assert L.qmoe_route_topk(P(256), 4, 256, 9, 1, None, None, None, None, None, None,
+    assert L.qmoe_route_topk(P(256), None, 4, 256, 9, 1, None, None, None, None, None, None,
                              ctypes.byref(nb), None) == 1
-    assert L.qmoe_route_topk(P(258), 4, 256, 8, 1, P(256), P(256), P(256), P(256), P(256), None,
+    assert L.qmoe_route_topk(P(258), None, 4, 256, 8, 1, P(256), P(256), P(256), P(256), P(256), None,
+                             ctypes.byref(nb), None) == 2
+    assert L.qmoe_route_topk(P(256), P(258), 4, 256, 8, 1, P(256), P(256), P(256), P(256), P(256), None,
                              ctypes.byref(nb), None) == 2
     assert L.qmoe_fp4_dequant(None, P(256), None, 1, 64, 64, 0, P(256), None) == 1
     assert L.qmoe_fp4_dequant(P(256), P(256), None, 1, 96, 64, 0, P(256), None) == 3
