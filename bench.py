@@ -602,10 +602,12 @@ def bench_dequant(device, peak: float, reps: int = 10, E: int = 128, K: int = 20
 
 def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
     """The prefill path on the NVFP4 prefill workload (2048 tokens, 128
-    experts, top-8, H=2048, I=1536): the whole forward call (routing, FP4 ->
-    bf16 dequantisation of both FCs, two grouped GEMMs, un-permute) and the
-    same call with the dequantised weights given (routing + GEMMs +
-    un-permute).  Event-timed on the launching stream after warm-up."""
+    experts, top-8, H=2048, I=1536): the whole forward call with k-major block
+    scales (routing, fused W4A16 GEMM for FC1 with SwiGLU, fused W4A16 GEMM for
+    FC2, un-permute), the same with scales as stored (two scale rewrites
+    more), and with bf16 dequantised weights given (the bf16 grouped GEMMs).
+    Per-stage times from events recorded between the call's kernels.
+    Event-timed on the launching stream after warm-up."""
     import numpy as np
     import torch
     import block_scaled_fp4_gb300 as q
@@ -631,17 +633,20 @@ def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
     lg = torch.from_numpy(syn.logits(rng, T, E, wl.logit_std)).to(device)
     w1, s1, g1 = codes((E, H, I)), e4m3((E, 2 * I, H // 16)), gscale()
     w2, s2, g2 = codes((E, I, H // 2)), e4m3((E, H, I // 16)), gscale()
+    s1k, s2k = q.scales_kmajor(s1, q.NVFP4), q.scales_kmajor(s2, q.NVFP4)
     w1d, w2d = q.dequant(w1, s1, g1, q.NVFP4), q.dequant(w2, s2, g2, q.NVFP4)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.Stream(device=device)
     # inputs and the workspace were written on the current stream: order them first
     stream.wait_stream(torch.cuda.current_stream())
-    ws_full = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4), dtype=torch.uint8, device=device)
+    KM = q.NVFP4 | q.SCALES_KMAJOR
+    ws_page = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4), dtype=torch.uint8, device=device)
+    ws_km = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, KM), dtype=torch.uint8, device=device)
     ws_gemm = torch.empty(q.forward_workspace_bytes(T, H, I, E, k, q.NVFP4, True), dtype=torch.uint8, device=device)
 
     def timed(fn):
         with torch.cuda.stream(stream):
-            for _ in range(2):
+            for _ in range(3):
                 fn()
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
             ev[0].record(stream)
@@ -652,26 +657,60 @@ def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
         us = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(reps))
         return us[len(us) // 2]
 
-    full = timed(lambda: q.moe_forward(x, lg, w1, s1, g1, w2, s2, g2, q.NVFP4, k, out=out, workspace=ws_full,
-                                       stream=stream))
-    gemm = timed(lambda: q.moe_forward(x, lg, w1, s1, g1, w2, s2, g2, q.NVFP4, k, w1_dequant=w1d,
-                                       w2_dequant=w2d, out=out, workspace=ws_gemm, stream=stream))
+    def stages(fn):
+        """median per-stage times (us) of `fn` with the six prefill stage events"""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            fn()
+            for e6 in evs:
+                for e in e6:
+                    e.record(stream)
+                q.set_stage_events(e6)
+                fn()
+            q.set_stage_events(None)
+        torch.cuda.synchronize()
+        names = ["route", "scale_rewrite", "fc1_gemm", "fc2_gemm", "unpermute"]
+        res = {}
+        for i, n in enumerate(names):
+            v = sorted(e6[i].elapsed_time(e6[i + 1]) * 1e3 for e6 in evs)
+            res[n] = round(v[len(v) // 2], 1)
+        return res
+
+    f_km = lambda: q.moe_forward(x, lg, w1, s1k, g1, w2, s2k, g2, KM, k, out=out, workspace=ws_km, stream=stream)
+    f_page = lambda: q.moe_forward(x, lg, w1, s1, g1, w2, s2, g2, q.NVFP4, k, out=out, workspace=ws_page,
+                                   stream=stream)
+    f_bf16 = lambda: q.moe_forward(x, lg, w1, s1, g1, w2, s2, g2, q.NVFP4, k, w1_dequant=w1d, w2_dequant=w2d,
+                                   out=out, workspace=ws_gemm, stream=stream)
+    km = timed(f_km)
+    page = timed(f_page)
+    gemm = timed(f_bf16)
+    st_km = stages(f_km)
+    st_bf16 = stages(f_bf16)
     R = T * k
-    flops = 2.0 * R * (H * 2 * I + I * H)
-    wbytes = E * (2 * I * H + H * I) * 2  # bf16 weights streamed by the GEMMs
+    flops1, flops2 = 2.0 * R * H * 2 * I, 2.0 * R * I * H
+    flops = flops1 + flops2
+    pbytes1 = E * (H * I + 2 * I * H // 16)   # FC1 packed codes + E4M3 scales
+    pbytes2 = E * (I * H // 2 + H * I // 16)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     tc_peak = float(peaks.get("bf16_tflops", 1900.0))
-    tflops = flops / (gemm * 1e-6) / 1e12
-    del w1d, w2d, ws_full, ws_gemm
+    fc1_tf = flops1 / (st_km["fc1_gemm"] * 1e-6) / 1e12
+    fc2_tf = flops2 / (st_km["fc2_gemm"] * 1e-6) / 1e12
+    gemm_tf = flops / ((st_km["fc1_gemm"] + st_km["fc2_gemm"]) * 1e-6) / 1e12
+    del w1d, w2d, ws_page, ws_km, ws_gemm
     return {"workload": f"nvfp4_prefill: T={T} E={E} k={k} H={H} I={I} NVFP4 SwiGLU",
-            "us_forward": round(full, 1), "us_forward_predequantised": round(gemm, 1),
-            "gemm_flops": int(flops), "tflops": round(tflops, 1), "tensor_peak_tflops": tc_peak,
-            "tensor_frac": round(tflops / tc_peak, 4),
-            "bf16_weight_bytes": int(wbytes), "weight_gbs": round(wbytes / (gemm * 1e-6) / 1e9, 1),
-            "hbm_frac": round(wbytes / (gemm * 1e-6) / 1e9 / hbm_peak, 4),
-            "kernels": "route, dequant x2 (full call only), grouped_gemm_tc_kernel x2 (tcgen05.mma bf16, "
-                       "TMEM accumulator), unpermute"}
+            "us_forward_kmajor": round(km, 1), "us_forward": round(page, 1),
+            "us_forward_predequantised": round(gemm, 1),
+            "stages_us_kmajor": st_km, "stages_us_predequantised": st_bf16,
+            "gemm_flops": int(flops), "tflops_fused_gemms": round(gemm_tf, 1),
+            "tflops_fc1": round(fc1_tf, 1), "tflops_fc2": round(fc2_tf, 1),
+            "tensor_peak_tflops": tc_peak, "tensor_frac_fc1": round(fc1_tf / tc_peak, 4),
+            "tensor_frac_fused_gemms": round(gemm_tf / tc_peak, 4),
+            "packed_weight_bytes": int(pbytes1 + pbytes2),
+            "packed_weight_gbs_fc1": round(pbytes1 / (st_km["fc1_gemm"] * 1e-6) / 1e9, 1),
+            "kernels": "route x2, fp4_grouped_gemm_kernel x2 (tcgen05.mma bf16 with the FP4 weights decoded in "
+                       "shared memory, TMEM accumulators), unpermute; scales as stored add transpose_bytes x2; "
+                       "the predequantised call runs grouped_gemm_tc_kernel x2"}
 
 
 # ---------------------------------------------------------------- CPU (oracle)

@@ -137,12 +137,15 @@ def route_topk(logits, k: int, normalize: int = 1, stream=None, router_weights=N
 
 
 def forward_workspace_bytes(T, H, I, E, k, fmt=NVFP4, with_dequantized=False) -> int:
-    """Workspace bytes ``moe_forward`` needs for these sizes."""
+    """Workspace bytes ``moe_forward`` needs for these sizes.
+    ``with_dequantized``: True when both FCs' bf16 dequantised weights are
+    given, or a pair (fc1 given, fc2 given)."""
+    w1d, w2d = with_dequantized if isinstance(with_dequantized, tuple) else (with_dequantized,) * 2
     nbytes = ctypes.c_size_t(0)
     dummy = ctypes.c_void_p(16)
     _check(load().qmoe_fp4_moe_forward(None, dummy, None, None, None, None, None, None, None,
-                                       dummy if with_dequantized else None,
-                                       dummy if with_dequantized else None, fmt, T, H, I, E, k, 1, 1,
+                                       dummy if w1d else None,
+                                       dummy if w2d else None, fmt, T, H, I, E, k, 1, 1,
                                        1.0, 0.0, math.inf, None, None, None, ctypes.byref(nbytes),
                                        None))
     return nbytes.value
@@ -167,7 +170,7 @@ def moe_forward(x, logits, w1, s1, g1, w2, s2, g2, fmt: int, k: int, normalize: 
     E, _, I = w1.shape
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
-    need = forward_workspace_bytes(T, H, I, E, k, fmt, w1_dequant is not None)
+    need = forward_workspace_bytes(T, H, I, E, k, fmt, (w1_dequant is not None, w2_dequant is not None))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     nbytes = ctypes.c_size_t(workspace.numel() * workspace.element_size())

@@ -41,7 +41,7 @@ int num_sms() {
 static cudaEvent_t *g_stage_events = nullptr;
 static int g_stage_nevents = 0;
 
-static inline void stage_event(int i, cudaStream_t s) {
+void stage_event(int i, cudaStream_t s) {
   if (g_stage_events && i < g_stage_nevents) cudaEventRecord(g_stage_events[i], s);
 }
 
@@ -191,12 +191,15 @@ struct PrefillLayout {
   int32_t *meta;  // the header: word 1 is the device error flag (the counters are never written here)
   int32_t *ids, *offsets, *p2e, *e2p;
   float *weights, *y;
-  uint16_t *w1d, *w2d, *act;
-  uint8_t *s1p, *s2p;
+  uint16_t *act;
+  uint8_t *s1k, *s2k;  // block scales rewritten k-major for the fused GEMMs (scales given as stored)
   size_t bytes;
 };
 
-static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k, int bs, bool need_w1, bool need_w2,
+// fused1 / fused2: the FC runs the fused W4A16 GEMM (no dequantised weights
+// given); with scales as stored ([E, N, K/bs]) its scales are rewritten
+// k-major into the workspace first.
+static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k, int bs, bool fused1, bool fused2,
                                     bool kmajor) {
   const size_t R = (size_t)T * k;
   Carve c(ws);
@@ -209,17 +212,16 @@ static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k,
   L.e2p = c.take<int32_t>(R);
   L.act = c.take<uint16_t>(R * I);
   L.y = c.take<float>(R * H);
-  if (need_w1) L.w1d = c.take<uint16_t>((size_t)E * 2 * I * H);
-  if (need_w2) L.w2d = c.take<uint16_t>((size_t)E * H * I);
-  if (need_w1 && kmajor) L.s1p = c.take<uint8_t>((size_t)E * 2 * I * (H / bs));
-  if (need_w2 && kmajor) L.s2p = c.take<uint8_t>((size_t)E * H * (I / bs));
+  if (fused1 && !kmajor) L.s1k = c.take<uint8_t>((size_t)E * 2 * I * (H / bs));
+  if (fused2 && !kmajor) L.s2k = c.take<uint8_t>((size_t)E * H * (I / bs));
   L.bytes = (c.off + 255) & ~(size_t)255;
   return L;
 }
 
-// T * k > QMOE_GEMV_MAX_ROWS: route, dequantise (unless given), grouped GEMMs,
-// weighted un-permute.  Arguments already checked by the caller: routing
-// sizes, format, H and I, swiglu_fusion, alpha / beta / limit.
+// T * k > QMOE_GEMV_MAX_ROWS: route, grouped GEMMs (fused W4A16, or bf16 over
+// dequantised weights the caller gives), weighted un-permute.  Arguments
+// already checked by the caller: routing sizes, format, H and I,
+// swiglu_fusion, alpha / beta / limit.
 static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const float *mix, const uint8_t *fc1_w,
                                    const uint8_t *fc1_s,
                                    const float *fc1_g, const uint8_t *fc2_w, const uint8_t *fc2_s, const float *fc2_g,
@@ -254,36 +256,29 @@ static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const
   ro.offsets = L.offsets;
   ro.p2e = L.p2e;
   ro.e2p = L.e2p;
+  stage_event(0, stream);
   cudaError_t err = launch_route(logits, T, E, k, normalize, ro, stream);
   if (err != cudaSuccess) return cuda_status(err, "route launch");
-  const uint16_t *w1d = fc1_wd, *w2d = fc2_wd;
-  if (need_w1) {
-    const uint8_t *s1 = fc1_s;
-    if (kmajor) {  // [E, H/bs, 2I] -> [E, 2I, H/bs]
-      err = launch_transpose_bytes(fc1_s, E, H / bs, 2 * I, L.s1p, stream);
-      if (err != cudaSuccess) return cuda_status(err, "scale transpose launch");
-      s1 = L.s1p;
-    }
-    err = launch_dequant(fc1_w, s1, fc1_g, E, 2 * I, H, fmt, L.w1d, stream);
-    if (err != cudaSuccess) return cuda_status(err, "dequant launch");
-    w1d = L.w1d;
+  stage_event(1, stream);
+  // fused FCs read k-major block scales: [E, N, K/bs] -> [E, K/bs, N] when given as stored
+  const uint8_t *s1k = fc1_s, *s2k = fc2_s;
+  if (need_w1 && !kmajor) {
+    err = launch_transpose_bytes(fc1_s, E, 2 * I, H / bs, L.s1k, stream);
+    if (err != cudaSuccess) return cuda_status(err, "scale transpose launch");
+    s1k = L.s1k;
   }
-  if (need_w2) {
-    const uint8_t *s2 = fc2_s;
-    if (kmajor) {  // [E, I/bs, H] -> [E, H, I/bs]
-      err = launch_transpose_bytes(fc2_s, E, I / bs, H, L.s2p, stream);
-      if (err != cudaSuccess) return cuda_status(err, "scale transpose launch");
-      s2 = L.s2p;
-    }
-    err = launch_dequant(fc2_w, s2, fc2_g, E, H, I, fmt, L.w2d, stream);
-    if (err != cudaSuccess) return cuda_status(err, "dequant launch");
-    w2d = L.w2d;
+  if (need_w2 && !kmajor) {
+    err = launch_transpose_bytes(fc2_s, E, H, I / bs, L.s2k, stream);
+    if (err != cudaSuccess) return cuda_status(err, "scale transpose launch");
+    s2k = L.s2k;
   }
+  stage_event(2, stream);
   PrefillArgs a{};
-  a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
+  a.fmt = fmt; a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
   a.alpha = alpha; a.beta = beta; a.limit = limit; a.fusion = fusion;
   a.x = x; a.offsets = L.offsets; a.p2e = L.p2e; a.e2p = L.e2p; a.weights = L.weights;
-  a.w1d = w1d; a.w2d = w2d; a.act = L.act; a.y = L.y; a.out = out;
+  a.w1 = fc1_w; a.s1k = s1k; a.g1 = fc1_g; a.w2 = fc2_w; a.s2k = s2k; a.g2 = fc2_g;
+  a.w1d = fc1_wd; a.w2d = fc2_wd; a.act = L.act; a.y = L.y; a.out = out;
   a.err_flag = L.meta + 1;
   return cuda_status(launch_prefill(a, stream), "prefill launch");
 }

@@ -318,7 +318,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   static std::atomic<int> smem_set[kMaxDevices];
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
-  if (!smem_set[dev].load(std::memory_order_acquire)) {
+  if ((a.w1d || a.w2d) && !smem_set[dev].load(std::memory_order_acquire)) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (err != cudaSuccess) return err;
     smem_set[dev].store(1, std::memory_order_release);
@@ -327,28 +327,55 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   const int R = a.T * a.k;
   const int na_max = a.E < R ? a.E : R;
   const unsigned mtiles = (unsigned)((R + kTcBM - 1) / kTcBM + na_max);  // >= the sum over experts of ceil(rows / kTcBM)
-  GroupedGemm g1{};
-  g1.A = a.x; g1.perm = a.p2e; g1.ktop = a.k; g1.lda = a.H;
-  g1.B = a.w1d; g1.offsets = a.offsets; g1.E = a.E; g1.N = 2 * a.I; g1.K = a.H;
-  g1.swiglu = 1; g1.concat = a.fusion == 2 ? 1 : 0;
-  g1.out_a = a.act; g1.alpha = a.alpha; g1.beta = a.beta; g1.limit = a.limit;
-  grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g1.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
-      g1, err_flag);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err;
+  if (a.w1d) {
+    GroupedGemm g1{};
+    g1.A = a.x; g1.perm = a.p2e; g1.ktop = a.k; g1.lda = a.H;
+    g1.B = a.w1d; g1.offsets = a.offsets; g1.E = a.E; g1.N = 2 * a.I; g1.K = a.H;
+    g1.swiglu = 1; g1.concat = a.fusion == 2 ? 1 : 0;
+    g1.out_a = a.act; g1.alpha = a.alpha; g1.beta = a.beta; g1.limit = a.limit;
+    grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g1.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
+        g1, err_flag);
+    err = cudaGetLastError();
+  } else {
+    Fp4GemmArgs f{};
+    f.mode = a.fusion == 2 ? 1 : 0;
+    f.fmt = a.fmt; f.R = R; f.E = a.E; f.H = a.H; f.I = a.I;
+    f.w = a.w1; f.s = a.s1k; f.gscale = a.g1;
+    f.A = a.x; f.perm = a.p2e; f.ktop = a.k; f.offsets = a.offsets;
+    f.out_a = a.act; f.alpha = a.alpha; f.beta = a.beta; f.limit = a.limit;
+    f.err_flag = err_flag;
+    err = launch_fp4_gemm(f, stream);
+  }
   if (err != cudaSuccess) return err;
-  GroupedGemm g2{};
-  g2.A = a.act; g2.perm = nullptr; g2.ktop = 1; g2.lda = a.I;
-  g2.B = a.w2d; g2.offsets = a.offsets; g2.E = a.E; g2.N = a.H; g2.K = a.I;
-  g2.swiglu = 0; g2.out_y = a.y;
-  grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g2.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
-      g2, err_flag);
-  err = cudaGetLastError();
+  stage_event(3, stream);
+  if (a.w2d) {
+    GroupedGemm g2{};
+    g2.A = a.act; g2.perm = nullptr; g2.ktop = 1; g2.lda = a.I;
+    g2.B = a.w2d; g2.offsets = a.offsets; g2.E = a.E; g2.N = a.H; g2.K = a.I;
+    g2.swiglu = 0; g2.out_y = a.y;
+    grouped_gemm_tc_kernel<<<dim3(mtiles, (unsigned)((g2.N + kTcBN - 1) / kTcBN)), kTcThreads, kTcSmem, stream>>>(
+        g2, err_flag);
+    err = cudaGetLastError();
+  } else {
+    Fp4GemmArgs f{};
+    f.mode = 2;
+    f.fmt = a.fmt; f.R = R; f.E = a.E; f.H = a.H; f.I = a.I;
+    f.w = a.w2; f.s = a.s2k; f.gscale = a.g2;
+    f.A = a.act; f.perm = nullptr; f.ktop = 1; f.offsets = a.offsets;
+    f.out_y = a.y;
+    f.err_flag = err_flag;
+    err = launch_fp4_gemm(f, stream);
+  }
   if (err != cudaSuccess) return err;
+  stage_event(4, stream);
   const long long work = (long long)a.T * (a.H / 2);
   long long grid = (work + 255) / 256;
   if (grid > (long long)num_sms() * 8) grid = (long long)num_sms() * 8;
   unpermute_kernel<<<(unsigned)grid, 256, 0, stream>>>(a.y, a.e2p, a.weights, a.T, a.H, a.k, a.out);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  stage_event(5, stream);
+  return err;
 }
 
 }  // namespace qmoe

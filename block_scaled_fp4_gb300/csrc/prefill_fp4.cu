@@ -1,0 +1,581 @@
+// Fused W4A16 grouped GEMM of the prefill path: the FP4 expert weights are
+// decoded inside the GEMM, so no bf16 copy of them is written or read
+// ("MoE and QMoE - CUDA Operator Documentation" §1 pipeline GEMM1 ->
+// activation -> GEMM2, §4.3 and §9b for the E2M1 codes, the E4M3 / E8M0
+// block scales and the fp32 global scale; the k-major block-scale layout
+// [E, K/bs, N] of §9b.2).
+//
+// Product per tile (swapped operands): D[n][p] = sum_k W[k][n] * X[p][k] with
+//  * M side (tcgen05 "A", 128 tensor-memory lanes) = 128 weight columns n,
+//    decoded from the packed codes into shared memory as bf16, K-major with
+//    the 128-byte swizzle.  The value written is the exact product
+//    e2m1 * block scale (at most 6 significant bits, so exact in bf16); the
+//    expert's global scale multiplies the fp32 accumulator in the epilogue;
+//  * N side ("B") = the expert's permuted token rows p, 16..256 of them (one
+//    row chunk of one expert), gathered bf16 activation rows;
+//  * fp32 accumulator in tensor memory, double-buffered (2 x 256 columns) so
+//    that one tile's epilogue overlaps the next tile's MMAs.
+// A row chunk is all of an expert's rows when they number <= 256, else an
+// even split in multiples of 16: the MMA's N follows the expert's row count,
+// so an expert with 130 rows costs 144 columns, not two 128-row tiles.
+//
+// Roles (persistent CTAs, one per SM, tiles taken round-robin):
+//  * warp 0: tensor-memory allocation; lane 0 issues tcgen05.mma
+//    (kind::f16, M = 128, N = tile rows, K = 16, four per 64-deep stage) and
+//    commits stage and accumulator barriers;
+//  * warp 1, lane 0: tensor copies of the packed codes (64 k rows x 64 bytes)
+//    and the k-major scale rows of a stage;
+//  * warps 2-3: cp.async gather of the activation rows (perm_to_expanded / k
+//    for the first GEMM), published with a lag of two stages;
+//  * warps 4-7: decode codes x scales -> bf16 into the stage's M-side tile;
+//  * warps 8-11: epilogue: tcgen05.ld of the accumulator, x global scale,
+//    SwiGLU of the (gate, linear) pair and bf16 store of the activation
+//    (first GEMM), or fp32 store of the FC2 row (second GEMM).
+// Every wait is bounded: on a timeout the CTA sets the device error flag,
+// stops, waits (bounded) for its copies and MMAs in flight and frees its
+// tensor memory.
+#include <atomic>
+
+#include "decode_common.cuh"
+#include "qmoe_common.cuh"
+
+namespace qmoe {
+namespace fg {
+
+constexpr int kBM = 128;     // weight columns per tile (MMA M, tensor-memory lanes)
+constexpr int kBK = 64;      // k rows per stage: one 128-byte swizzled row of bf16
+constexpr int kMaxN = 256;   // token rows per tile (MMA N)
+constexpr int kStages = 4;
+constexpr int kLag = 2;      // activation stages in flight before the loader publishes one
+constexpr int kThreads = 384;
+constexpr int kWarpMma = 0, kWarpTma = 1, kWarpLoad0 = 2, kLoadThreads = 64, kWarpDec0 = 4, kDecThreads = 128,
+              kWarpEpi0 = 8, kEpiThreads = 128;
+constexpr int kATile = kBM * kBK * 2;     // 16 KB
+constexpr int kBTile = kMaxN * kBK * 2;   // 32 KB
+constexpr int kCodeBytes = kBK * kBM / 2; // 4 KB: 64 k rows x 64 bytes
+constexpr int kScaleBytes = 512;          // <= 4 block rows x 128 columns
+constexpr int kPTile = kCodeBytes + kScaleBytes;
+constexpr int kSmem = kStages * (kATile + kBTile + kPTile) + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kWaitLimit = 1u << 22;
+static_assert(kLag < kStages, "the loader's lag must leave a stage to wait on");
+static_assert(kSmem <= 227 * 1024 - 4096, "stages fit in shared memory");
+
+// MODE: 0 first GEMM, gate / linear interleaved (columns 2m, 2m + 1);
+//       1 first GEMM, concatenated (columns m, I + m);
+//       2 second GEMM.
+struct Params {
+  CUtensorMap tm_codes;    // packed codes as bytes: [E*K rows][N/2]
+  CUtensorMap tm_scales;   // k-major block scales as bytes: [E*K/bs rows][N]
+  const uint16_t *A;       // bf16 activation rows
+  const int32_t *perm;     // non-null: permuted row p reads A row perm[p] / ktop
+  int ktop, lda;
+  const int32_t *offsets;  // [E + 1] first permuted row of each expert
+  const float *gscale;     // [E] global scales, or null
+  int E, K, N, I;          // expert weight: K x N; I: first GEMM's output width
+  int ncb;                 // column blocks: I / 64 (first GEMM), ceil(N / 128) (second)
+  uint16_t *out_a;         // first GEMM: [R, I] bf16
+  float *out_y;            // second GEMM: [R, N] fp32
+  float alpha, beta, limit;
+  int32_t *err_flag;
+};
+
+struct Bars {
+  uint64_t pk_full[kStages], pk_empty[kStages];  // packed stage landed / decoded
+  uint64_t a_full[kStages], b_full[kStages];     // M-side tile decoded / activation rows landed
+  uint64_t ab_empty[kStages];                    // the stage's MMAs are done
+  uint64_t acc_full[2], acc_empty[2];            // accumulator buffers
+  uint64_t drain;                                // final MMA commit
+};
+
+struct Tile {
+  int e, cb, r0, rows, nr;
+};
+
+// Chunk c of the expert-ordered chunk list, column block cb.
+__device__ __forceinline__ Tile tile_at(const Params &p, const int *cpre, const int *offs, int t) {
+  Tile T;
+  const int c = t / p.ncb;
+  T.cb = t - c * p.ncb;
+  int lo = 0, hi = p.E;  // cpre[lo] <= c < cpre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cpre[mid] <= c) lo = mid;
+    else hi = mid;
+  }
+  T.e = lo;
+  const int n = offs[lo + 1] - offs[lo], nch = cpre[lo + 1] - cpre[lo], j = c - cpre[lo];
+  const int cs = (((n + nch - 1) / nch) + 15) & ~15;
+  T.r0 = offs[lo] + j * cs;
+  T.rows = min(cs, n - j * cs);
+  T.nr = (T.rows + 15) & ~15;
+  return T;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_s,
+                                             int32_t *err_flag, int code) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_s) return false;
+  }
+  *abort_s = 1;
+  atomicCAS(err_flag, 0, code);
+  return false;
+}
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile:
+// start >> 4, leading byte offset 16 (unused with this swizzle), 1024 bytes
+// between 8-row groups, descriptor version 1, swizzle mode 128 B.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// byte offset of 16-byte chunk c of row r in a K-major 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ uint32_t bf16x2_of(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t h2) { return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))); }
+__device__ __forceinline__ float f16_hi(uint32_t h2) { return __half2float(__ushort_as_half((unsigned short)(h2 >> 16))); }
+
+// ---- roles ----------------------------------------------------------------------
+
+template <int MODE, int FMT>
+__device__ __forceinline__ void tma_role(const Params &p, const int *cpre, const int *offs, int ntiles,
+                                         unsigned char *P_ring, Bars &B, volatile int *abort_s) {
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  constexpr int NSR = kBK / BS;  // scale block rows per stage
+  const int KT = p.K / kBK;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    const Tile T = tile_at(p, cpre, offs, t);
+    for (int kt = 0; kt < KT; ++kt, ++it) {
+      const int s = (int)(it % kStages);
+      const uint32_t u = it / kStages;
+      if (!wait_bounded(&B.pk_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 410)) {
+        ok = false;
+        break;
+      }
+      unsigned char *P = P_ring + (size_t)s * kPTile;
+      mbar_expect_tx(&B.pk_full[s], (uint32_t)(kCodeBytes + NSR * 128));
+      const int yc = T.e * p.K + kt * kBK, ys = T.e * (p.K / BS) + kt * NSR;
+      if constexpr (MODE == 1) {
+        tensor_g2s_2d(P, &p.tm_codes, 32 * T.cb, yc, &B.pk_full[s]);
+        tensor_g2s_2d(P + kCodeBytes / 2, &p.tm_codes, (p.I + 64 * T.cb) / 2, yc, &B.pk_full[s]);
+        tensor_g2s_2d(P + kCodeBytes, &p.tm_scales, 64 * T.cb, ys, &B.pk_full[s]);
+        tensor_g2s_2d(P + kCodeBytes + NSR * 64, &p.tm_scales, p.I + 64 * T.cb, ys, &B.pk_full[s]);
+      } else {
+        tensor_g2s_2d(P, &p.tm_codes, 64 * T.cb, yc, &B.pk_full[s]);
+        tensor_g2s_2d(P + kCodeBytes, &p.tm_scales, 128 * T.cb, ys, &B.pk_full[s]);
+      }
+    }
+  }
+  // copies still in flight land before the CTA leaves (a no-op when every
+  // stage was consumed)
+  const uint32_t n = it < (uint32_t)kStages ? it : (uint32_t)kStages;
+  for (uint32_t d = 1; d <= n; ++d) {
+    const uint32_t j = it - d;
+    wait_bounded(&B.pk_full[j % kStages], (j / kStages) & 1u, abort_s, p.err_flag, 411);
+  }
+}
+
+__device__ __forceinline__ void loader_role(const Params &p, const int *cpre, const int *offs, int ntiles,
+                                            unsigned char *B_ring, Bars &B, volatile int *abort_s, int lt) {
+  const int cth = lt & 7, rth = lt >> 3;
+  const int KT = p.K / kBK;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    const Tile T = tile_at(p, cpre, offs, t);
+    int arow[kMaxN / 8];
+#pragma unroll
+    for (int q = 0; q < kMaxN / 8; ++q) {
+      const int r = rth + 8 * q;
+      arow[q] = -1;
+      if (r < T.rows) arow[q] = p.perm ? __ldg(p.perm + T.r0 + r) / p.ktop : T.r0 + r;
+    }
+    for (int kt = 0; kt < KT; ++kt, ++it) {
+      const int s = (int)(it % kStages);
+      const uint32_t u = it / kStages;
+      if (!wait_bounded(&B.ab_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 420)) {
+        ok = false;
+        break;
+      }
+      unsigned char *Bs = B_ring + (size_t)s * kBTile;
+      const uint16_t *src0 = p.A + kt * kBK + 8 * cth;
+#pragma unroll
+      for (int q = 0; q < kMaxN / 8; ++q)
+        if (arow[q] >= 0) cp_async16(Bs + sw128(rth + 8 * q, cth), src0 + (size_t)arow[q] * p.lda);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (it >= (uint32_t)kLag) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&B.b_full[(it - kLag) % kStages]);
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (ok) {
+    const uint32_t n = it < (uint32_t)kLag ? it : (uint32_t)kLag;
+    for (uint32_t d = n; d >= 1; --d) mbar_arrive(&B.b_full[(it - d) % kStages]);
+  }
+}
+
+// Decoder thread (w, kc): column word w (tile columns 8w..8w+7) of k rows
+// 8kc..8kc+7.  Tile column n = 8w + j goes to M-side row 16j + w: a store
+// phase of 8 lanes (w0..w0+7, one kc) then covers 8 distinct swizzle chunks.
+template <int MODE, int FMT>
+__device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsigned char *A_ring,
+                                             const unsigned char *P_ring, Bars &B, volatile int *abort_s, int dt) {
+  constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
+  constexpr int NSR = kBK / BS;
+  const int lane = dt & 31;
+  const int w = lane & 15, sw = lane >> 4, kc = 2 * (dt >> 5) + sw;
+  const int sr = (8 * kc) / BS;
+  // byte offsets of this thread's code word in row 0 and its 8 scales
+  int code_off, pitch, sc_off;
+  if constexpr (MODE == 1) {
+    code_off = (w >> 3) * (kCodeBytes / 2) + (w & 7) * 4;
+    pitch = 32;
+    sc_off = kCodeBytes + (w >> 3) * (NSR * 64) + sr * 64 + (w & 7) * 8;
+  } else {
+    code_off = w * 4;
+    pitch = 64;
+    sc_off = kCodeBytes + sr * 128 + w * 8;
+  }
+  for (int it = 0; it < my_steps; ++it) {
+    const int s = it % kStages;
+    const uint32_t u = (uint32_t)it / kStages;
+    if (!wait_bounded(&B.pk_full[s], u & 1u, abort_s, p.err_flag, 430)) return;
+    const unsigned char *P = P_ring + (size_t)s * kPTile;
+    // half-warps read the two rows of a pair in opposite order: their row
+    // parities differ, so the 32 loads hit 32 distinct banks
+    uint32_t c[8];
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      const int ra = 8 * kc + 2 * pr + sw, rb = 8 * kc + 2 * pr + (1 - sw);
+      const uint32_t a = *reinterpret_cast<const uint32_t *>(P + code_off + ra * pitch);
+      const uint32_t b = *reinterpret_cast<const uint32_t *>(P + code_off + rb * pitch);
+      c[2 * pr] = sw ? b : a;
+      c[2 * pr + 1] = sw ? a : b;
+    }
+    const uint2 sv = *reinterpret_cast<const uint2 *>(P + sc_off);
+    mbar_arrive(&B.pk_empty[s]);
+    if (!wait_bounded(&B.ab_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 431)) return;
+    unsigned char *As = A_ring + (size_t)s * kATile;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float lo[8], hi[8];
+      if constexpr (FMT == QMOE_NVFP4) {
+        const uint32_t sh = e4m3x2_to_f16x2(((jj < 2 ? sv.x : sv.y) >> (16 * (jj & 1))) & 0xFFFFu);
+        const uint16_t s_lo = (uint16_t)(sh & 0xFFFFu), s_hi = (uint16_t)(sh >> 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t h = e2m1x2_to_f16x2(c[i] >> (8 * jj));
+          lo[i] = fma_f16_f32((uint16_t)(h & 0xFFFFu), s_lo, -0.0f);
+          hi[i] = fma_f16_f32((uint16_t)(h >> 16), s_hi, -0.0f);
+        }
+      } else {
+        const uint32_t sb = (jj < 2 ? sv.x : sv.y) >> (16 * (jj & 1));
+        const float f_lo = e8m0_to_f32(sb & 0xFFu), f_hi = e8m0_to_f32((sb >> 8) & 0xFFu);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t h = e2m1x2_to_f16x2(c[i] >> (8 * jj));
+          lo[i] = f16_lo(h) * f_lo;
+          hi[i] = f16_hi(h) * f_hi;
+        }
+      }
+      const int ar0 = 16 * (2 * jj) + w, ar1 = ar0 + 16;
+      *reinterpret_cast<uint4 *>(As + sw128(ar0, kc)) =
+          make_uint4(bf16x2_of(lo[0], lo[1]), bf16x2_of(lo[2], lo[3]), bf16x2_of(lo[4], lo[5]), bf16x2_of(lo[6], lo[7]));
+      *reinterpret_cast<uint4 *>(As + sw128(ar1, kc)) =
+          make_uint4(bf16x2_of(hi[0], hi[1]), bf16x2_of(hi[2], hi[3]), bf16x2_of(hi[4], hi[5]), bf16x2_of(hi[6], hi[7]));
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive(&B.a_full[s]);
+  }
+}
+
+__device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const int *offs, int ntiles,
+                                         const unsigned char *A_ring, const unsigned char *B_ring, Bars &B,
+                                         uint32_t tmem, volatile int *abort_s) {
+  const int KT = p.K / kBK;
+  uint32_t it = 0, tl = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
+    const Tile T = tile_at(p, cpre, offs, t);
+    const uint32_t ab = tl & 1u, ua = tl >> 1;
+    if (!wait_bounded(&B.acc_empty[ab], (ua & 1u) ^ 1u, abort_s, p.err_flag, 440)) break;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t d = tmem + ab * (uint32_t)kMaxN;
+    // fp32 accumulator, bf16 A and B, both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(T.nr >> 3) << 17) |
+                           ((uint32_t)(kBM >> 4) << 24);
+    for (int kt = 0; kt < KT; ++kt, ++it) {
+      const int s = (int)(it % kStages);
+      const uint32_t u = it / kStages;
+      if (!wait_bounded(&B.a_full[s], u & 1u, abort_s, p.err_flag, 441) ||
+          !wait_bounded(&B.b_full[s], u & 1u, abort_s, p.err_flag, 442)) {
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t a_addr = smem_addr(A_ring + (size_t)s * kATile), b_addr = smem_addr(B_ring + (size_t)s * kBTile);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t da = desc_sw128(a_addr + kk * 32), db = desc_sw128(b_addr + kk * 32);
+        const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+            "l"(da), "l"(db), "r"(idesc), "r"(acc)
+            : "memory");
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_addr(&B.ab_empty[s]))
+                   : "memory");
+    }
+    if (!ok) break;
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(&B.acc_full[ab]))
+                 : "memory");
+  }
+  // every MMA issued above has completed before the tensor memory is freed
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(&B.drain))
+               : "memory");
+  wait_bounded(&B.drain, 0u, abort_s, p.err_flag, 443);
+}
+
+// Epilogue thread: tensor-memory lane 32q + l = M-side row 16j + w, i.e. tile
+// column n = 8w + j with w = l & 15, j = 2q + (l >> 4).
+template <int MODE>
+__device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, const int *offs, int ntiles, Bars &B,
+                                              uint32_t tmem, volatile int *abort_s, int warp) {
+  const int q = warp & 3, lane = (int)lane_id();
+  const int w = lane & 15, j = 2 * q + (lane >> 4), n = 8 * w + j;
+  uint32_t tl = 0;
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+    const Tile T = tile_at(p, cpre, offs, t);
+    const uint32_t ab = tl & 1u, ua = tl >> 1;
+    if (!wait_bounded(&B.acc_full[ab], ua & 1u, abort_s, p.err_flag, 450)) return;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const float g = p.gscale ? __ldg(p.gscale + T.e) : 1.0f;
+    const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + ab * (uint32_t)kMaxN;
+    for (int cc = 0; cc * 32 < T.nr; ++cc) {
+      uint32_t v[32];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+          "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+            "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+            "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          : "r"(tbase + (uint32_t)(cc * 32)));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const int rbase = cc * 32;
+      if constexpr (MODE == 2) {
+        const int h = 128 * T.cb + n;
+        if (h < p.N) {
+          float *dst = p.out_y + (size_t)(T.r0 + rbase) * p.N + h;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (rbase + i < T.rows) dst[(size_t)i * p.N] = __uint_as_float(v[i]) * g;
+        }
+      } else {
+        // (gate, linear) partners: lanes l and l ^ 16 (interleaved: j even /
+        // odd, same w) or l and l ^ 8 (concatenated: w < 8 / w >= 8, same j)
+        constexpr int kX = MODE == 0 ? 16 : 8;
+        const bool gate = MODE == 0 ? (lane < 16) : (w < 8);
+        const int m = 64 * T.cb + (MODE == 0 ? (n >> 1) : (8 * w + j));
+        uint16_t *dst = p.out_a + (size_t)(T.r0 + rbase) * p.I + m;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float mine = __uint_as_float(v[i]) * g;
+          const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, kX);
+          if (gate && rbase + i < T.rows)
+            dst[(size_t)i * p.I] = (uint16_t)f32_to_bf16_rne(swiglu(mine, other, p.alpha, p.beta, p.limit));
+        }
+      }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    mbar_arrive(&B.acc_empty[ab]);
+  }
+}
+
+template <int MODE, int FMT>
+__global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  __shared__ Bars B;
+  __shared__ uint32_t tmem_s;
+  __shared__ int cpre[kMaxExperts + 1], offs[kMaxExperts + 1];
+  __shared__ volatile int abort_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char *base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
+  unsigned char *A_ring = base;
+  unsigned char *B_ring = A_ring + kStages * kATile;
+  unsigned char *P_ring = B_ring + kStages * kBTile;
+
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_s)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else if (warp == kWarpTma && lane == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&B.pk_full[i], 1);
+      mbar_init(&B.pk_empty[i], kDecThreads);
+      mbar_init(&B.a_full[i], kDecThreads);
+      mbar_init(&B.b_full[i], kLoadThreads);
+      mbar_init(&B.ab_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.acc_full[i], 1);
+      mbar_init(&B.acc_empty[i], kEpiThreads);
+    }
+    mbar_init(&B.drain, 1);
+    mbar_fence_init();
+    abort_s = 0;
+  } else if (warp == kWarpLoad0) {  // chunks per expert and their prefix (E <= 256)
+    const int per = (p.E + 31) / 32;
+    int sum = 0;
+    for (int q = 0; q < per; ++q) {
+      const int e = lane * per + q;
+      if (e <= p.E) offs[e] = __ldg(p.offsets + e);
+      if (e < p.E) sum += (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e) + kMaxN - 1) / kMaxN;
+    }
+    if (lane == 31 && per * 32 == p.E) offs[p.E] = __ldg(p.offsets + p.E);
+    int incl = sum;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+      if (lane >= m) incl += v;
+    }
+    int run = incl - sum;
+    for (int q = 0; q < per; ++q) {
+      const int e = lane * per + q;
+      if (e < p.E) {
+        cpre[e] = run;
+        run += (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e) + kMaxN - 1) / kMaxN;
+      }
+    }
+    if (lane == 31) cpre[p.E] = incl;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_s;
+  const int ntiles = cpre[p.E] * p.ncb;
+
+  if (warp == kWarpMma) {
+    if (lane == 0) mma_role(p, cpre, offs, ntiles, A_ring, B_ring, B, tmem, &abort_s);
+    __syncwarp();
+  } else if (warp == kWarpTma) {
+    if (lane == 0) tma_role<MODE, FMT>(p, cpre, offs, ntiles, P_ring, B, &abort_s);
+    __syncwarp();
+  } else if (warp < kWarpDec0) {
+    loader_role(p, cpre, offs, ntiles, B_ring, B, &abort_s, tid - 32 * kWarpLoad0);
+  } else if (warp < kWarpEpi0) {
+    const int mine = (int)blockIdx.x < ntiles ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    decoder_role<MODE, FMT>(p, mine * (p.K / kBK), A_ring, P_ring, B, &abort_s, tid - 32 * kWarpDec0);
+  } else {
+    epilogue_role<MODE>(p, cpre, offs, ntiles, B, tmem, &abort_s, warp);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A 2-D byte array [rows][cols] (row pitch = cols) as a tensor map with a
+// box of box_cols x box_rows.
+static cudaError_t encode_bytes_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                                   uint32_t box_rows) {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (err != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr) {
+      set_error("cuTensorMapEncodeTiled is not available");
+      return err != cudaSuccess ? err : cudaErrorNotSupported;
+    }
+    f = reinterpret_cast<EncodeTiledFn>(ptr);
+    fn.store(f, std::memory_order_release);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+template <int MODE, int FMT>
+static cudaError_t launch_mode(const Params &p, int grid, cudaStream_t stream) {
+  static std::atomic<int> smem_set[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  auto kfn = fp4_grouped_gemm_kernel<MODE, FMT>;
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
+    cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (err != cudaSuccess) return err;
+    smem_set[dev].store(1, std::memory_order_release);
+  }
+  kfn<<<grid, kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fg
+
+cudaError_t launch_fp4_gemm(const Fp4GemmArgs &a, cudaStream_t stream) {
+  using namespace fg;
+  const int bs = block_size(a.fmt);
+  Params p{};
+  const bool first = a.mode != 2;
+  const int N = first ? 2 * a.I : a.H, K = first ? a.H : a.I;
+  const int R = a.R;
+  if (R <= 0) return cudaSuccess;
+  p.A = a.A; p.perm = a.perm; p.ktop = a.ktop; p.lda = K;
+  p.offsets = a.offsets; p.gscale = a.gscale;
+  p.E = a.E; p.K = K; p.N = N; p.I = a.I;
+  p.ncb = first ? a.I / 64 : (a.H + kBM - 1) / kBM;
+  p.out_a = a.out_a; p.out_y = a.out_y;
+  p.alpha = a.alpha; p.beta = a.beta; p.limit = a.limit;
+  p.err_flag = a.err_flag;
+  const uint32_t code_box = a.mode == 1 ? 32u : 64u, scale_box = a.mode == 1 ? 64u : 128u;
+  cudaError_t err = encode_bytes_2d(&p.tm_codes, a.w, (uint64_t)N / 2, (uint64_t)a.E * K, code_box, (uint32_t)kBK);
+  if (err != cudaSuccess) return err;
+  err = encode_bytes_2d(&p.tm_scales, a.s, (uint64_t)N, (uint64_t)a.E * (K / bs), scale_box, (uint32_t)(kBK / bs));
+  if (err != cudaSuccess) return err;
+  // tiles <= (sum over experts of ceil(rows / 256)) * column blocks
+  const long long chunks = (long long)R / kMaxN + (a.E < R ? a.E : R) + 1;
+  long long grid = chunks * p.ncb;
+  if (grid > num_sms()) grid = num_sms();
+  const bool nv = a.fmt == QMOE_NVFP4;
+  switch (a.mode) {
+    case 0: return nv ? launch_mode<0, QMOE_NVFP4>(p, (int)grid, stream) : launch_mode<0, QMOE_MXFP4>(p, (int)grid, stream);
+    case 1: return nv ? launch_mode<1, QMOE_NVFP4>(p, (int)grid, stream) : launch_mode<1, QMOE_MXFP4>(p, (int)grid, stream);
+    default: return nv ? launch_mode<2, QMOE_NVFP4>(p, (int)grid, stream) : launch_mode<2, QMOE_MXFP4>(p, (int)grid, stream);
+  }
+}
+
+}  // namespace qmoe

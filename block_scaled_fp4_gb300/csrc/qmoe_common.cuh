@@ -82,6 +82,9 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 // ---- host side -------------------------------------------------------------------
 
 void set_error(const char *fmt, ...);
+// Benchmark instrumentation: record stage event i on `s` when the caller set
+// events with qmoe_set_stage_events (a no-op otherwise).
+void stage_event(int i, cudaStream_t s);
 int num_sms();
 // Per-device host caches (kernel attributes, symbol addresses) hold this many devices.
 constexpr int kMaxDevices = 64;
@@ -195,17 +198,39 @@ cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const f
 // directions of the block-scale layout conversion).
 cudaError_t launch_transpose_bytes(const uint8_t *in, int E, int rows, int cols, uint8_t *out, cudaStream_t stream);
 
-// Prefill (T * k > 64): grouped GEMMs over dequantised bf16 weights.
+// Fused W4A16 grouped GEMM of one FC at prefill (prefill_fp4.cu): packed
+// codes [E, K, N/2], k-major block scales [E, K/bs, N], decoded inside the GEMM.
+struct Fp4GemmArgs {
+  int mode;                 // 0: FC1, gate / linear interleaved; 1: FC1 concatenated; 2: FC2
+  int fmt, R, E, H, I;
+  const uint8_t *w, *s;     // packed codes, k-major block scales
+  const float *gscale;      // [E] or null
+  const uint16_t *A;        // FC1: x [T, H]; FC2: act [R, I]
+  const int32_t *perm;      // FC1: perm_to_expanded (row p reads x row perm[p] / ktop); FC2: null
+  int ktop;
+  const int32_t *offsets;   // [E + 1]
+  uint16_t *out_a;          // FC1: act [R, I] bf16
+  float *out_y;             // FC2: y [R, H] fp32
+  float alpha, beta, limit;
+  int32_t *err_flag;
+};
+cudaError_t launch_fp4_gemm(const Fp4GemmArgs &a, cudaStream_t stream);
+
+// Prefill (T * k > 64): per FC, the fused W4A16 GEMM over the packed weights,
+// or the bf16 grouped GEMM over dequantised weights the caller passes.
 struct PrefillArgs {
-  int T, H, I, E, k;
+  int fmt, T, H, I, E, k;
   float alpha, beta, limit;
   int fusion;                // FC1 gate/linear columns: 1 interleaved, 2 concatenated
   const uint16_t *x;         // bf16 [T, H]
   const int32_t *offsets;    // [E + 1]
   const int32_t *p2e, *e2p;  // [T * k] permute maps
   const float *weights;      // [T * k] routing weights
-  const uint16_t *w1d;       // bf16 [E, 2I, H]
-  const uint16_t *w2d;       // bf16 [E, H, I]
+  const uint8_t *w1, *s1k;   // FC1 packed codes [E, H, I] bytes and k-major scales [E, H/bs, 2I]
+  const uint8_t *w2, *s2k;   // FC2 packed codes [E, I, H/2] and k-major scales [E, I/bs, H]
+  const float *g1, *g2;      // global scales [E] or null
+  const uint16_t *w1d;       // bf16 [E, 2I, H] given by the caller, or null (fused FC1)
+  const uint16_t *w2d;       // bf16 [E, H, I] given by the caller, or null (fused FC2)
   uint16_t *act;             // bf16 [T * k, I] FC1 activations, permuted order
   float *y;                  // fp32 [T * k, H] FC2 rows, permuted order
   uint16_t *out;             // bf16 [T, H]

@@ -108,9 +108,9 @@ typedef enum {
 #define QMOE_WORKSPACE_HEADER_BYTES 64
 
 /* Largest number of expanded rows (T * k) the decode GEMV path takes; more rows
- * take the prefill path (dequantise + tensor-core grouped GEMM).  The window
- * is the one PR #31159 sets for MTP verification ("kMaxProfiledExpandedRows
- * 8 -> 64"). */
+ * take the prefill path (tensor-core grouped GEMMs over the packed weights).
+ * The window is the one PR #31159 sets for MTP verification
+ * ("kMaxProfiledExpandedRows 8 -> 64"). */
 #define QMOE_GEMV_MAX_ROWS 64
 
 /*
@@ -173,9 +173,12 @@ qmoe_status qmoe_route_topk(const float *logits, const float *router_weights, in
  *   fc2_g        fp32 [E] global scales, or NULL.
  *   fc1_wd       bf16 [E, 2I, H] already-dequantised FC1 weights, or NULL;
  *   fc2_wd       bf16 [E, H, I] already-dequantised FC2 weights, or NULL.
- *                (Used only when T * k > QMOE_GEMV_MAX_ROWS; when NULL that
- *                path dequantises into the workspace, so its workspace holds
- *                E * 3 * H * I bf16 values more.)
+ *                (Used only when T * k > QMOE_GEMV_MAX_ROWS: an FC whose
+ *                fc*_wd is given runs a bf16 grouped GEMM over it; one
+ *                without runs the fused W4A16 GEMM over fc*_w / fc*_s, and
+ *                with block scales as stored ([E, N, K/bs]) its scales are
+ *                first rewritten k-major into the workspace, E * N * K / bs
+ *                bytes more.)
  *   fmt          QMOE_NVFP4 or QMOE_MXFP4, optionally | QMOE_SCALES_KMAJOR
  *                (both FCs' block scales in the k-major layout).  The result
  *                does not depend on the layout beyond the order of the fp32
@@ -201,13 +204,13 @@ qmoe_status qmoe_route_topk(const float *logits, const float *router_weights, in
  * The decode kernel is a cooperative launch of one CTA per SM:
  * it needs the whole GPU's residency and returns QMOE_ERR_CUDA if another
  * context keeps it from launching.  Larger T * k runs the prefill path
- * ("[CUDA] Coalesce QMoE MXFP4/NVFP4 weight dequantization", PR #31349;
- * operator doc §4.3, §9b.1): routing, FP4 -> bf16 dequantisation of both FCs
- * (skipped for the FCs whose fc*_wd is given), two grouped bf16 GEMMs on the
- * tensor cores with fp32 accumulation (the gather folded into the first, the
- * SwiGLU into its epilogue; the activation rounded to bf16), and the weighted
- * un-permute.  Numerically the two paths agree within the tolerance of fp32
- * accumulation, not bit for bit.
+ * (operator doc §1 pipeline, §4.3, §9b): routing, then per FC a grouped GEMM
+ * on the tensor cores with fp32 accumulation -- over the packed weights,
+ * decoded to bf16 (e2m1 * block scale, exact) inside the GEMM with the global
+ * scale applied to the accumulator, or over the caller's fc*_wd -- with the
+ * gather folded into the first GEMM and the SwiGLU into its epilogue (the
+ * activation rounded to bf16), and the weighted un-permute.  Numerically the
+ * paths agree within the tolerance of fp32 accumulation, not bit for bit.
  */
 qmoe_status qmoe_fp4_moe_forward(const uint16_t *x, const float *logits, const float *router_weights,
                                  const uint8_t *fc1_w, const uint8_t *fc1_s, const float *fc1_g,
@@ -337,7 +340,10 @@ const char *qmoe_last_error(void);
  * Returns the number of kernels one forward call launches for decode shapes
  * (one: the fused routing + FC1 + FC2 + un-permute kernel, after a memset of
  * the workspace header unless QMOE_WORKSPACE_PRIMED), i.e. how many events
- * after the first are used.
+ * after the first are used.  Prefill shapes record six points: events[0]
+ * before routing, [1] after routing, [2] after the block-scale rewrites (if
+ * any), [3] after the FC1 GEMM, [4] after the FC2 GEMM, [5] after the
+ * un-permute.
  */
 int qmoe_set_stage_events(cudaEvent_t *events, int n_events);
 

@@ -224,3 +224,21 @@ def test_no_alloc_rejects_sizes_beyond_its_scratch(qm):
         assert rc == 4, rc
         assert b"static scratch" in L.qmoe_last_error()
     """)
+
+
+def test_prefill_workspace_sizes(qm):
+    """Prefill shapes (T * k > 64): the fused GEMMs need no bf16 weight copy;
+    block scales as stored add their k-major rewrite (E * N * K / bs bytes per
+    FC) to the workspace, an FC given as bf16 weights does not."""
+    T, H, I, E, k = 2048, 2048, 1536, 128, 8
+    page = qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4)
+    km = qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4 | qm.SCALES_KMAJOR)
+    s1_bytes, s2_bytes = E * 2 * I * (H // 16), E * H * (I // 16)
+    assert page - km == s1_bytes + s2_bytes
+    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, True) == km
+    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, (True, False)) == km + s2_bytes
+    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, (False, True)) == km + s1_bytes
+    # routing maps, activations (bf16 [R, I]) and FC2 rows (fp32 [R, H]) at least
+    R = T * k
+    assert km >= qm.WORKSPACE_HEADER_BYTES + R * I * 2 + R * H * 4
+    assert km < qm.WORKSPACE_HEADER_BYTES + R * I * 2 + R * H * 4 + 64 * R + 8192

@@ -1,7 +1,10 @@
-"""The prefill path (more than 64 expanded rows: dequantise, two grouped bf16
-GEMMs on the tensor cores, weighted un-permute) against the oracle, row-L2
-relative error <= 1e-2: small shapes in full, the NVFP4 prefill workload on
-128 sampled tokens, the caller-dequantised-weights variant and k-major scales."""
+"""The prefill path (more than 64 expanded rows: two grouped GEMMs on the
+tensor cores -- the fused W4A16 GEMM over the packed weights, or the bf16 one
+over caller-dequantised weights -- and the weighted un-permute) against the
+oracle, row-L2 relative error <= 1e-2: small shapes in full, the NVFP4
+prefill workload on 128 sampled tokens, the caller-dequantised-weights
+variant (both FCs or one), k-major scales, experts whose rows split into
+several chunks and experts with no rows."""
 import numpy as np
 import pytest
 import torch
@@ -13,11 +16,13 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(qgpu, wl, L, kmajor=False, dequantised=False):
+    """dequantised: True (both FCs), "fc1" or "fc2" (that FC alone) given as bf16."""
     d = to_dev(L)
     s1, s2, fmt = d["s1"], d["s2"], wl.fmt
     kw = {}
-    if dequantised:
+    if dequantised in (True, "fc1"):
         kw["w1_dequant"] = qgpu.dequant(d["w1"], d["s1"], d["g1"], wl.fmt)
+    if dequantised in (True, "fc2"):
         kw["w2_dequant"] = qgpu.dequant(d["w2"], d["s2"], d["g2"], wl.fmt)
     if kmajor:
         s1, s2, fmt = qgpu.scales_kmajor(s1, wl.fmt), qgpu.scales_kmajor(s2, wl.fmt), wl.fmt | qgpu.SCALES_KMAJOR
@@ -39,6 +44,9 @@ SMALL = [
     syn.small("pf_gptoss", T=70, E=12, k=3, H=192, I=256, fmt=1, alpha=1.702, beta=1.0, limit=7.0),
     syn.small("pf_nonorm", T=33, E=32, k=4, H=128, I=320, normalize=0),
     syn.small("pf_rows", T=300, E=4, k=2, H=256, I=192),                    # > 128 rows per expert: several row tiles
+    syn.small("pf_chunks", T=700, E=4, k=2, H=128, I=128),                  # > 256 rows per expert: split into chunks
+    syn.small("pf_sparse", T=9, E=64, k=8, H=128, I=64),                    # 72 rows over 64 experts: most empty
+    syn.small("pf_mx_chunks", T=520, E=2, k=1, H=192, I=192, fmt=1),        # MXFP4, 260 rows each, H % 128 = 64
 ]
 
 
@@ -51,11 +59,12 @@ def test_prefill_small(qgpu, oracle, wl):
     assert err <= OUTPUT_RTOL, (wl.name, err, elem)
 
 
-@pytest.mark.parametrize("wl", SMALL[:2], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", SMALL[:2] + SMALL[5:6], ids=lambda w: w.name)
 def test_prefill_kmajor_and_dequantised(qgpu, oracle, wl):
     L = syn.layer(wl, 22)
     ref = _ref(oracle, wl, L)
-    for kw in (dict(kmajor=True), dict(dequantised=True)):
+    for kw in (dict(kmajor=True), dict(dequantised=True), dict(dequantised="fc1"),
+               dict(dequantised="fc2", kmajor=True)):
         got, _ = _run(qgpu, wl, L, **kw)
         err, elem = row_rel_l2(got, ref)
         assert err <= OUTPUT_RTOL, (wl.name, kw, err, elem)
