@@ -775,7 +775,8 @@ def run_reference(args):
 
 def profile_case(workload: str, n_layers: int) -> None:
     """A small case for ncu captures: n_layers distinct layers of one decode
-    workload (k-major scales, primed workspace), each run twice, eagerly."""
+    workload (k-major scales, primed workspace), or of the prefill workload
+    (k-major scales), each run twice, eagerly."""
     import torch
     import block_scaled_fp4_gb300 as q
     device = torch.device("cuda", torch.cuda.current_device())
@@ -785,7 +786,7 @@ def profile_case(workload: str, n_layers: int) -> None:
     for L in layers:
         L["s1"] = q.scales_kmajor(L["s1"], wl.fmt)
         L["s2"] = q.scales_kmajor(L["s2"], wl.fmt)
-    fmt = wl.fmt | q.SCALES_KMAJOR | q.WORKSPACE_PRIMED
+    fmt = wl.fmt | q.SCALES_KMAJOR | (q.WORKSPACE_PRIMED if workload in DECODE_KERNEL else 0)
     ws = torch.zeros(q.forward_workspace_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, fmt), dtype=torch.uint8,
                      device=device)
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in layers]
@@ -816,9 +817,9 @@ def main(argv=None):
                     help="skip the other decode workloads, the page-layout line and the routing line")
     ap.add_argument("--scales", default="kmajor", choices=["kmajor", "page"],
                     help="block-scale layout the layer reads (default: k-major, prepared once at load)")
-    ap.add_argument("--profile-case", default=None, choices=sorted(DECODE_KERNEL),
-                    help="profiler helper: run --layers layers of one decode workload twice, eagerly, and exit "
-                         "(no timing, no JSON line)")
+    ap.add_argument("--profile-case", default=None, choices=sorted(DECODE_KERNEL) + ["nvfp4_prefill"],
+                    help="profiler helper: run --layers layers of one decode workload (or the prefill workload) "
+                         "twice, eagerly, and exit (no timing, no JSON line)")
     args = ap.parse_args(argv)
     if args.profile_case:
         profile_case(args.profile_case, args.layers)

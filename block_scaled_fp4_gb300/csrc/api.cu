@@ -191,7 +191,7 @@ struct PrefillLayout {
   int32_t *meta;  // the header: word 1 is the device error flag (the counters are never written here)
   int32_t *ids, *offsets, *p2e, *e2p;
   float *weights, *y;
-  uint16_t *act;
+  uint16_t *xp, *act;
   uint8_t *s1k, *s2k;  // block scales rewritten k-major for the fused GEMMs (scales given as stored)
   size_t bytes;
 };
@@ -212,6 +212,7 @@ static PrefillLayout prefill_layout(void *ws, int T, int H, int I, int E, int k,
   L.e2p = c.take<int32_t>(R);
   L.act = c.take<uint16_t>(R * I);
   L.y = c.take<float>(R * H);
+  if (fused1) L.xp = c.take<uint16_t>(R * H);
   if (fused1 && !kmajor) L.s1k = c.take<uint8_t>((size_t)E * 2 * I * (H / bs));
   if (fused2 && !kmajor) L.s2k = c.take<uint8_t>((size_t)E * H * (I / bs));
   L.bytes = (c.off + 255) & ~(size_t)255;
@@ -278,7 +279,7 @@ static qmoe_status prefill_forward(const uint16_t *x, const float *logits, const
   a.alpha = alpha; a.beta = beta; a.limit = limit; a.fusion = fusion;
   a.x = x; a.offsets = L.offsets; a.p2e = L.p2e; a.e2p = L.e2p; a.weights = L.weights;
   a.w1 = fc1_w; a.s1k = s1k; a.g1 = fc1_g; a.w2 = fc2_w; a.s2k = s2k; a.g2 = fc2_g;
-  a.w1d = fc1_wd; a.w2d = fc2_wd; a.act = L.act; a.y = L.y; a.out = out;
+  a.w1d = fc1_wd; a.w2d = fc2_wd; a.xp = L.xp; a.act = L.act; a.y = L.y; a.out = out;
   a.err_flag = L.meta + 1;
   return cuda_status(launch_prefill(a, stream), "prefill launch");
 }

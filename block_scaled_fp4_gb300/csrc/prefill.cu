@@ -292,6 +292,21 @@ __global__ void __launch_bounds__(kTcThreads) grouped_gemm_tc_kernel(const __gri
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128u) : "memory");
 }
 
+// xp[p] = x[perm_to_expanded[p] / k]: the token rows in expert order, 16
+// bytes per thread and step, each row's copies coalesced.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x,
+                                                          const int32_t *__restrict__ p2e, int R, int H, int k,
+                                                          uint16_t *__restrict__ xp) {
+  const int vpr = H / 8;  // 16-byte vectors per row
+  const long long n = (long long)R * vpr;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int pr = (int)(idx / vpr), v = (int)(idx - (long long)pr * vpr);
+    const int t = __ldg(p2e + pr) / k;
+    reinterpret_cast<uint4 *>(xp + (size_t)pr * H)[v] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H) + v);
+  }
+}
+
 // out[t][h] = bf16(sum_j w[t][j] * y[expanded_to_perm[t * k + j]][h]), j in order.
 __global__ void __launch_bounds__(256) unpermute_kernel(const float *__restrict__ y, const int32_t *__restrict__ e2p,
                                                         const float *__restrict__ w, int T, int H, int k,
@@ -338,11 +353,17 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
         g1, err_flag);
     err = cudaGetLastError();
   } else {
+    const long long vecs = (long long)R * (a.H / 8);
+    long long ggrid = (vecs + 255) / 256;
+    if (ggrid > (long long)num_sms() * 8) ggrid = (long long)num_sms() * 8;
+    gather_rows_kernel<<<(unsigned)ggrid, 256, 0, stream>>>(a.x, a.p2e, R, a.H, a.k, a.xp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     Fp4GemmArgs f{};
     f.mode = a.fusion == 2 ? 1 : 0;
     f.fmt = a.fmt; f.R = R; f.E = a.E; f.H = a.H; f.I = a.I;
     f.w = a.w1; f.s = a.s1k; f.gscale = a.g1;
-    f.A = a.x; f.perm = a.p2e; f.ktop = a.k; f.offsets = a.offsets;
+    f.A = a.xp; f.offsets = a.offsets;
     f.out_a = a.act; f.alpha = a.alpha; f.beta = a.beta; f.limit = a.limit;
     f.err_flag = err_flag;
     err = launch_fp4_gemm(f, stream);
@@ -362,7 +383,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     f.mode = 2;
     f.fmt = a.fmt; f.R = R; f.E = a.E; f.H = a.H; f.I = a.I;
     f.w = a.w2; f.s = a.s2k; f.gscale = a.g2;
-    f.A = a.act; f.perm = nullptr; f.ktop = 1; f.offsets = a.offsets;
+    f.A = a.act; f.offsets = a.offsets;
     f.out_y = a.y;
     f.err_flag = err_flag;
     err = launch_fp4_gemm(f, stream);

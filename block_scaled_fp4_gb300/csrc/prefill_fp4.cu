@@ -44,22 +44,26 @@ namespace fg {
 
 constexpr int kBM = 128;     // weight columns per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 64;      // k rows per stage: one 128-byte swizzled row of bf16
-constexpr int kMaxN = 256;   // token rows per tile (MMA N)
-constexpr int kStages = 4;
-constexpr int kLag = 2;      // activation stages in flight before the loader publishes one
-constexpr int kThreads = 384;
-constexpr int kWarpMma = 0, kWarpTma = 1, kWarpLoad0 = 2, kLoadThreads = 64, kWarpDec0 = 4, kDecThreads = 128,
-              kWarpEpi0 = 8, kEpiThreads = 128;
+constexpr int kMaxN = 192;   // token rows per tile (MMA N)
+constexpr int kAccCols = 256;  // tensor-memory columns between the two accumulator buffers
+// Ring depths: the packed-weight ring covers HBM latency, the activation ring
+// L2 latency, the decoded ring only the MMA's own latency.
+constexpr int kPStages = 8, kBStages = 5, kAStages = 3;
+constexpr int kBoxRows = 16;  // activation rows per tensor copy
+constexpr int kWarpMma = 0, kWarpTma = 1, kWarpRows = 2, kWarpDec0 = 3, kDecThreads = 256, kWarpEpi0 = 11,
+              kEpiThreads = 128;
+constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 480
 constexpr int kATile = kBM * kBK * 2;     // 16 KB
-constexpr int kBTile = kMaxN * kBK * 2;   // 32 KB
+constexpr int kBTile = kMaxN * kBK * 2;   // 24 KB
 constexpr int kCodeBytes = kBK * kBM / 2; // 4 KB: 64 k rows x 64 bytes
 constexpr int kScaleBytes = 512;          // <= 4 block rows x 128 columns
 constexpr int kPTile = kCodeBytes + kScaleBytes;
-constexpr int kSmem = kStages * (kATile + kBTile + kPTile) + 1024;
+constexpr int kSmem = kAStages * kATile + kBStages * kBTile + kPStages * kPTile + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
-static_assert(kLag < kStages, "the loader's lag must leave a stage to wait on");
+static_assert(kMaxN <= kAccCols && 2 * kAccCols <= (int)kTmemCols, "two accumulator buffers");
 static_assert(kSmem <= 227 * 1024 - 4096, "stages fit in shared memory");
+static_assert(kEpiThreads == 128, "four epilogue warps: warp w reads tensor-memory lanes 32 (w % 4) ..");
 
 // MODE: 0 first GEMM, gate / linear interleaved (columns 2m, 2m + 1);
 //       1 first GEMM, concatenated (columns m, I + m);
@@ -67,9 +71,7 @@ static_assert(kSmem <= 227 * 1024 - 4096, "stages fit in shared memory");
 struct Params {
   CUtensorMap tm_codes;    // packed codes as bytes: [E*K rows][N/2]
   CUtensorMap tm_scales;   // k-major block scales as bytes: [E*K/bs rows][N]
-  const uint16_t *A;       // bf16 activation rows
-  const int32_t *perm;     // non-null: permuted row p reads A row perm[p] / ktop
-  int ktop, lda;
+  CUtensorMap tm_rows;     // bf16 activation rows in expert order [R][K], 128-byte swizzle, 64 x 16 boxes
   const int32_t *offsets;  // [E + 1] first permuted row of each expert
   const float *gscale;     // [E] global scales, or null
   int E, K, N, I;          // expert weight: K x N; I: first GEMM's output width
@@ -81,11 +83,12 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t pk_full[kStages], pk_empty[kStages];  // packed stage landed / decoded
-  uint64_t a_full[kStages], b_full[kStages];     // M-side tile decoded / activation rows landed
-  uint64_t ab_empty[kStages];                    // the stage's MMAs are done
-  uint64_t acc_full[2], acc_empty[2];            // accumulator buffers
-  uint64_t drain;                                // final MMA commit
+  uint64_t pk_full[kPStages], pk_empty[kPStages];  // packed stage landed / read by the decoders
+  uint64_t a_full[kAStages], a_empty[kAStages];    // decoded tile written / its MMAs done
+  uint64_t b_full[kBStages], b_empty[kBStages];    // activation rows landed / their MMAs done
+
+  uint64_t acc_full[2], acc_empty[2];              // accumulator buffers
+  uint64_t drain;                                  // final MMA commit
 };
 
 struct Tile {
@@ -141,6 +144,15 @@ __device__ __forceinline__ uint32_t bf16x2_of(float lo, float hi) {
 __device__ __forceinline__ float f16_lo(uint32_t h2) { return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))); }
 __device__ __forceinline__ float f16_hi(uint32_t h2) { return __half2float(__ushort_as_half((unsigned short)(h2 >> 16))); }
 
+// SwiGLU of one (gate, linear) pair with the fast exponential and reciprocal
+// ("MoE and QMoE - CUDA Operator Documentation" §8: G = min(gate, limit),
+// L = clamp(linear, -limit, limit), G * sigmoid(alpha * G) * (L + beta)).
+__device__ __forceinline__ float swiglu_fast(float gate, float lin, float alpha, float beta, float limit) {
+  const float G = fminf(gate, limit);
+  const float L = fmaxf(fminf(lin, limit), -limit);
+  return __fdividef(G, 1.0f + __expf(-alpha * G)) * (L + beta);
+}
+
 // ---- roles ----------------------------------------------------------------------
 
 template <int MODE, int FMT>
@@ -154,8 +166,8 @@ __device__ __forceinline__ void tma_role(const Params &p, const int *cpre, const
   for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
     const Tile T = tile_at(p, cpre, offs, t);
     for (int kt = 0; kt < KT; ++kt, ++it) {
-      const int s = (int)(it % kStages);
-      const uint32_t u = it / kStages;
+      const int s = (int)(it % kPStages);
+      const uint32_t u = it / kPStages;
       if (!wait_bounded(&B.pk_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 410)) {
         ok = false;
         break;
@@ -176,81 +188,71 @@ __device__ __forceinline__ void tma_role(const Params &p, const int *cpre, const
   }
   // copies still in flight land before the CTA leaves (a no-op when every
   // stage was consumed)
-  const uint32_t n = it < (uint32_t)kStages ? it : (uint32_t)kStages;
+  const uint32_t n = it < (uint32_t)kPStages ? it : (uint32_t)kPStages;
   for (uint32_t d = 1; d <= n; ++d) {
     const uint32_t j = it - d;
-    wait_bounded(&B.pk_full[j % kStages], (j / kStages) & 1u, abort_s, p.err_flag, 411);
+    wait_bounded(&B.pk_full[j % kPStages], (j / kPStages) & 1u, abort_s, p.err_flag, 411);
   }
 }
 
-__device__ __forceinline__ void loader_role(const Params &p, const int *cpre, const int *offs, int ntiles,
-                                            unsigned char *B_ring, Bars &B, volatile int *abort_s, int lt) {
-  const int cth = lt & 7, rth = lt >> 3;
+// Activation rows of a stage: nr rows x 64 k as tensor copies of 16 rows,
+// written by the copy engine in the 128-byte-swizzled K-major layout the MMA
+// descriptor reads (rows past the chunk's end are the next expert's or the
+// copy's zero fill; their accumulator columns are never stored).
+__device__ __forceinline__ void rows_role(const Params &p, const int *cpre, const int *offs, int ntiles,
+                                          unsigned char *B_ring, Bars &B, volatile int *abort_s) {
   const int KT = p.K / kBK;
   uint32_t it = 0;
   bool ok = true;
   for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
     const Tile T = tile_at(p, cpre, offs, t);
-    int arow[kMaxN / 8];
-#pragma unroll
-    for (int q = 0; q < kMaxN / 8; ++q) {
-      const int r = rth + 8 * q;
-      arow[q] = -1;
-      if (r < T.rows) arow[q] = p.perm ? __ldg(p.perm + T.r0 + r) / p.ktop : T.r0 + r;
-    }
+    const int nbox = T.nr / kBoxRows;
     for (int kt = 0; kt < KT; ++kt, ++it) {
-      const int s = (int)(it % kStages);
-      const uint32_t u = it / kStages;
-      if (!wait_bounded(&B.ab_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 420)) {
+      const int s = (int)(it % kBStages);
+      const uint32_t u = it / kBStages;
+      if (!wait_bounded(&B.b_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 420)) {
         ok = false;
         break;
       }
       unsigned char *Bs = B_ring + (size_t)s * kBTile;
-      const uint16_t *src0 = p.A + kt * kBK + 8 * cth;
-#pragma unroll
-      for (int q = 0; q < kMaxN / 8; ++q)
-        if (arow[q] >= 0) cp_async16(Bs + sw128(rth + 8 * q, cth), src0 + (size_t)arow[q] * p.lda);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      if (it >= (uint32_t)kLag) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&B.b_full[(it - kLag) % kStages]);
-      }
+      mbar_expect_tx(&B.b_full[s], (uint32_t)(nbox * kBoxRows * kBK * 2));
+      for (int b = 0; b < nbox; ++b)
+        tensor_g2s_2d(Bs + b * (kBoxRows * kBK * 2), &p.tm_rows, kt * kBK, T.r0 + b * kBoxRows, &B.b_full[s]);
     }
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  if (ok) {
-    const uint32_t n = it < (uint32_t)kLag ? it : (uint32_t)kLag;
-    for (uint32_t d = n; d >= 1; --d) mbar_arrive(&B.b_full[(it - d) % kStages]);
+  const uint32_t n = it < (uint32_t)kBStages ? it : (uint32_t)kBStages;
+  for (uint32_t d = 1; d <= n; ++d) {
+    const uint32_t j = it - d;
+    wait_bounded(&B.b_full[j % kBStages], (j / kBStages) & 1u, abort_s, p.err_flag, 421);
   }
 }
 
-// Decoder thread (w, kc): column word w (tile columns 8w..8w+7) of k rows
-// 8kc..8kc+7.  Tile column n = 8w + j goes to M-side row 16j + w: a store
-// phase of 8 lanes (w0..w0+7, one kc) then covers 8 distinct swizzle chunks.
+// Decoder thread (w, kc, jh): column pairs 2jh, 2jh + 1 of column word w
+// (tile columns 8w + 4jh .. 8w + 4jh + 3) over k rows 8kc..8kc+7.  Tile
+// column n = 8w + j goes to M-side row 16j + w: a store phase of 8 lanes
+// (w0..w0+7, one kc) then covers 8 distinct swizzle chunks.
 template <int MODE, int FMT>
 __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsigned char *A_ring,
                                              const unsigned char *P_ring, Bars &B, volatile int *abort_s, int dt) {
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   constexpr int NSR = kBK / BS;
-  const int lane = dt & 31;
-  const int w = lane & 15, sw = lane >> 4, kc = 2 * (dt >> 5) + sw;
+  const int lane = dt & 31, dw = dt >> 5;
+  const int w = lane & 15, sw = lane >> 4, kc = 2 * (dw & 3) + sw, jh = dw >> 2;
   const int sr = (8 * kc) / BS;
-  // byte offsets of this thread's code word in row 0 and its 8 scales
+  // byte offsets of this thread's code word in row 0 and of its 4 scales
   int code_off, pitch, sc_off;
   if constexpr (MODE == 1) {
     code_off = (w >> 3) * (kCodeBytes / 2) + (w & 7) * 4;
     pitch = 32;
-    sc_off = kCodeBytes + (w >> 3) * (NSR * 64) + sr * 64 + (w & 7) * 8;
+    sc_off = kCodeBytes + (w >> 3) * (NSR * 64) + sr * 64 + (w & 7) * 8 + 4 * jh;
   } else {
     code_off = w * 4;
     pitch = 64;
-    sc_off = kCodeBytes + sr * 128 + w * 8;
+    sc_off = kCodeBytes + sr * 128 + w * 8 + 4 * jh;
   }
   for (int it = 0; it < my_steps; ++it) {
-    const int s = it % kStages;
-    const uint32_t u = (uint32_t)it / kStages;
+    const int s = it % kPStages;
+    const uint32_t u = (uint32_t)it / kPStages;
     if (!wait_bounded(&B.pk_full[s], u & 1u, abort_s, p.err_flag, 430)) return;
     const unsigned char *P = P_ring + (size_t)s * kPTile;
     // half-warps read the two rows of a pair in opposite order: their row
@@ -264,15 +266,18 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
       c[2 * pr] = sw ? b : a;
       c[2 * pr + 1] = sw ? a : b;
     }
-    const uint2 sv = *reinterpret_cast<const uint2 *>(P + sc_off);
+    const uint32_t sv = *reinterpret_cast<const uint32_t *>(P + sc_off);
     mbar_arrive(&B.pk_empty[s]);
-    if (!wait_bounded(&B.ab_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 431)) return;
-    unsigned char *As = A_ring + (size_t)s * kATile;
+    const int sa = it % kAStages;
+    const uint32_t ua = (uint32_t)it / kAStages;
+    if (!wait_bounded(&B.a_empty[sa], (ua & 1u) ^ 1u, abort_s, p.err_flag, 431)) return;
+    unsigned char *As = A_ring + (size_t)sa * kATile;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int q = 0; q < 2; ++q) {
+      const int jj = 2 * jh + q;  // column pair of the word
       float lo[8], hi[8];
       if constexpr (FMT == QMOE_NVFP4) {
-        const uint32_t sh = e4m3x2_to_f16x2(((jj < 2 ? sv.x : sv.y) >> (16 * (jj & 1))) & 0xFFFFu);
+        const uint32_t sh = e4m3x2_to_f16x2((sv >> (16 * q)) & 0xFFFFu);
         const uint16_t s_lo = (uint16_t)(sh & 0xFFFFu), s_hi = (uint16_t)(sh >> 16);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -281,7 +286,7 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
           hi[i] = fma_f16_f32((uint16_t)(h >> 16), s_hi, -0.0f);
         }
       } else {
-        const uint32_t sb = (jj < 2 ? sv.x : sv.y) >> (16 * (jj & 1));
+        const uint32_t sb = sv >> (16 * q);
         const float f_lo = e8m0_to_f32(sb & 0xFFu), f_hi = e8m0_to_f32((sb >> 8) & 0xFFu);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -297,8 +302,13 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
           make_uint4(bf16x2_of(hi[0], hi[1]), bf16x2_of(hi[2], hi[3]), bf16x2_of(hi[4], hi[5]), bf16x2_of(hi[6], hi[7]));
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive(&B.a_full[s]);
+    mbar_arrive(&B.a_full[sa]);
   }
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const int *offs, int ntiles,
@@ -312,20 +322,19 @@ __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const
     const uint32_t ab = tl & 1u, ua = tl >> 1;
     if (!wait_bounded(&B.acc_empty[ab], (ua & 1u) ^ 1u, abort_s, p.err_flag, 440)) break;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t d = tmem + ab * (uint32_t)kMaxN;
+    const uint32_t d = tmem + ab * (uint32_t)kAccCols;
     // fp32 accumulator, bf16 A and B, both K-major, N >> 3 at bit 17, M >> 4 at bit 24
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(T.nr >> 3) << 17) |
                            ((uint32_t)(kBM >> 4) << 24);
     for (int kt = 0; kt < KT; ++kt, ++it) {
-      const int s = (int)(it % kStages);
-      const uint32_t u = it / kStages;
-      if (!wait_bounded(&B.a_full[s], u & 1u, abort_s, p.err_flag, 441) ||
-          !wait_bounded(&B.b_full[s], u & 1u, abort_s, p.err_flag, 442)) {
+      const int sa = (int)(it % kAStages), sb = (int)(it % kBStages);
+      if (!wait_bounded(&B.a_full[sa], (it / kAStages) & 1u, abort_s, p.err_flag, 441) ||
+          !wait_bounded(&B.b_full[sb], (it / kBStages) & 1u, abort_s, p.err_flag, 442)) {
         ok = false;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a_addr = smem_addr(A_ring + (size_t)s * kATile), b_addr = smem_addr(B_ring + (size_t)s * kBTile);
+      const uint32_t a_addr = smem_addr(A_ring + (size_t)sa * kATile), b_addr = smem_addr(B_ring + (size_t)sb * kBTile);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         const uint64_t da = desc_sw128(a_addr + kk * 32), db = desc_sw128(b_addr + kk * 32);
@@ -336,19 +345,14 @@ __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const
             "l"(da), "l"(db), "r"(idesc), "r"(acc)
             : "memory");
       }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_addr(&B.ab_empty[s]))
-                   : "memory");
+      mma_commit(&B.a_empty[sa]);
+      mma_commit(&B.b_empty[sb]);
     }
     if (!ok) break;
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_addr(&B.acc_full[ab]))
-                 : "memory");
+    mma_commit(&B.acc_full[ab]);
   }
   // every MMA issued above has completed before the tensor memory is freed
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_addr(&B.drain))
-               : "memory");
+  mma_commit(&B.drain);
   wait_bounded(&B.drain, 0u, abort_s, p.err_flag, 443);
 }
 
@@ -359,6 +363,13 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, 
                                               uint32_t tmem, volatile int *abort_s, int warp) {
   const int q = warp & 3, lane = (int)lane_id();
   const int w = lane & 15, j = 2 * q + (lane >> 4), n = 8 * w + j;
+  // first GEMM: (gate, linear) partners are lanes l and l ^ 16 (interleaved:
+  // j even / odd, same w) or l and l ^ 8 (concatenated: w < 8 / >= 8, same
+  // j).  Of rows 2a and 2a + 1 the gate lane finishes row 2a, the linear
+  // lane row 2a + 1, each with the value the other sends it.
+  constexpr int kX = MODE == 0 ? 16 : 8;
+  const bool gate = MODE == 0 ? (lane < 16) : (w < 8);
+  const int m_in = MODE == 0 ? 4 * w + q : 8 * (w & 7) + j;  // output column of the pair within the tile
   uint32_t tl = 0;
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
     const Tile T = tile_at(p, cpre, offs, t);
@@ -366,7 +377,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, 
     if (!wait_bounded(&B.acc_full[ab], ua & 1u, abort_s, p.err_flag, 450)) return;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const float g = p.gscale ? __ldg(p.gscale + T.e) : 1.0f;
-    const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + ab * (uint32_t)kMaxN;
+    const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + ab * (uint32_t)kAccCols;
     for (int cc = 0; cc * 32 < T.nr; ++cc) {
       uint32_t v[32];
       asm volatile(
@@ -388,18 +399,16 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, 
             if (rbase + i < T.rows) dst[(size_t)i * p.N] = __uint_as_float(v[i]) * g;
         }
       } else {
-        // (gate, linear) partners: lanes l and l ^ 16 (interleaved: j even /
-        // odd, same w) or l and l ^ 8 (concatenated: w < 8 / w >= 8, same j)
-        constexpr int kX = MODE == 0 ? 16 : 8;
-        const bool gate = MODE == 0 ? (lane < 16) : (w < 8);
-        const int m = 64 * T.cb + (MODE == 0 ? (n >> 1) : (8 * w + j));
-        uint16_t *dst = p.out_a + (size_t)(T.r0 + rbase) * p.I + m;
+        const int r_odd = gate ? 0 : 1;  // which row of each pair this lane finishes
+        uint16_t *dst = p.out_a + (size_t)(T.r0 + rbase + r_odd) * p.I + 64 * T.cb + m_in;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float mine = __uint_as_float(v[i]) * g;
-          const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, kX);
-          if (gate && rbase + i < T.rows)
-            dst[(size_t)i * p.I] = (uint16_t)f32_to_bf16_rne(swiglu(mine, other, p.alpha, p.beta, p.limit));
+        for (int a = 0; a < 16; ++a) {
+          const float v0 = __uint_as_float(v[2 * a]) * g, v1 = __uint_as_float(v[2 * a + 1]) * g;
+          // gate lane sends its row-(2a+1) gate, linear lane its row-2a linear
+          const float got = __shfl_xor_sync(0xFFFFFFFFu, gate ? v1 : v0, kX);
+          const float gv = gate ? v0 : got, lv = gate ? got : v1;
+          if (rbase + 2 * a + r_odd < T.rows)
+            dst[(size_t)(2 * a) * p.I] = (uint16_t)f32_to_bf16_rne(swiglu_fast(gv, lv, p.alpha, p.beta, p.limit));
         }
       }
     }
@@ -418,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char *base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
   unsigned char *A_ring = base;
-  unsigned char *B_ring = A_ring + kStages * kATile;
-  unsigned char *P_ring = B_ring + kStages * kBTile;
+  unsigned char *B_ring = A_ring + kAStages * kATile;
+  unsigned char *P_ring = B_ring + kBStages * kBTile;
 
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_s)),
@@ -427,12 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   } else if (warp == kWarpTma && lane == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kPStages; ++i) {
       mbar_init(&B.pk_full[i], 1);
       mbar_init(&B.pk_empty[i], kDecThreads);
+    }
+    for (int i = 0; i < kAStages; ++i) {
       mbar_init(&B.a_full[i], kDecThreads);
-      mbar_init(&B.b_full[i], kLoadThreads);
-      mbar_init(&B.ab_empty[i], 1);
+      mbar_init(&B.a_empty[i], 1);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(&B.b_full[i], 1);
+      mbar_init(&B.b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.acc_full[i], 1);
@@ -441,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
     mbar_init(&B.drain, 1);
     mbar_fence_init();
     abort_s = 0;
-  } else if (warp == kWarpLoad0) {  // chunks per expert and their prefix (E <= 256)
+  } else if (warp == kWarpRows) {  // chunks per expert and their prefix (E <= 256)
     const int per = (p.E + 31) / 32;
     int sum = 0;
     for (int q = 0; q < per; ++q) {
@@ -478,8 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
   } else if (warp == kWarpTma) {
     if (lane == 0) tma_role<MODE, FMT>(p, cpre, offs, ntiles, P_ring, B, &abort_s);
     __syncwarp();
-  } else if (warp < kWarpDec0) {
-    loader_role(p, cpre, offs, ntiles, B_ring, B, &abort_s, tid - 32 * kWarpLoad0);
+  } else if (warp == kWarpRows) {
+    if (lane == 0) rows_role(p, cpre, offs, ntiles, B_ring, B, &abort_s);
+    __syncwarp();
   } else if (warp < kWarpEpi0) {
     const int mine = (int)blockIdx.x < ntiles ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     decoder_role<MODE, FMT>(p, mine * (p.K / kBK), A_ring, P_ring, B, &abort_s, tid - 32 * kWarpDec0);
@@ -500,8 +515,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 // A 2-D byte array [rows][cols] (row pitch = cols) as a tensor map with a
 // box of box_cols x box_rows.
-static cudaError_t encode_bytes_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                                   uint32_t box_rows) {
+static cudaError_t encode_fn(EncodeTiledFn *out) {
   static std::atomic<EncodeTiledFn> fn{nullptr};
   EncodeTiledFn f = fn.load(std::memory_order_acquire);
   if (!f) {
@@ -515,12 +529,41 @@ static cudaError_t encode_bytes_2d(CUtensorMap *m, const void *base, uint64_t co
     f = reinterpret_cast<EncodeTiledFn>(ptr);
     fn.store(f, std::memory_order_release);
   }
+  *out = f;
+  return cudaSuccess;
+}
+
+static cudaError_t encode_bytes_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                                   uint32_t box_rows) {
+  EncodeTiledFn f = nullptr;
+  cudaError_t err = encode_fn(&f);
+  if (err != cudaSuccess) return err;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+// bf16 rows [rows][cols] as a tensor map with 64 x kBoxRows boxes in the
+// 128-byte swizzle (16-byte chunk c of box row r at chunk c ^ (r & 7)).
+static cudaError_t encode_rows_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn f = nullptr;
+  cudaError_t err = encode_fn(&f);
+  if (err != cudaSuccess) return err;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -554,7 +597,6 @@ cudaError_t launch_fp4_gemm(const Fp4GemmArgs &a, cudaStream_t stream) {
   const int N = first ? 2 * a.I : a.H, K = first ? a.H : a.I;
   const int R = a.R;
   if (R <= 0) return cudaSuccess;
-  p.A = a.A; p.perm = a.perm; p.ktop = a.ktop; p.lda = K;
   p.offsets = a.offsets; p.gscale = a.gscale;
   p.E = a.E; p.K = K; p.N = N; p.I = a.I;
   p.ncb = first ? a.I / 64 : (a.H + kBM - 1) / kBM;
@@ -565,6 +607,8 @@ cudaError_t launch_fp4_gemm(const Fp4GemmArgs &a, cudaStream_t stream) {
   cudaError_t err = encode_bytes_2d(&p.tm_codes, a.w, (uint64_t)N / 2, (uint64_t)a.E * K, code_box, (uint32_t)kBK);
   if (err != cudaSuccess) return err;
   err = encode_bytes_2d(&p.tm_scales, a.s, (uint64_t)N, (uint64_t)a.E * (K / bs), scale_box, (uint32_t)(kBK / bs));
+  if (err != cudaSuccess) return err;
+  err = encode_rows_sw128(&p.tm_rows, a.A, (uint64_t)K, (uint64_t)R);
   if (err != cudaSuccess) return err;
   // tiles <= (sum over experts of ceil(rows / 256)) * column blocks
   const long long chunks = (long long)R / kMaxN + (a.E < R ? a.E : R) + 1;

@@ -205,9 +205,7 @@ struct Fp4GemmArgs {
   int fmt, R, E, H, I;
   const uint8_t *w, *s;     // packed codes, k-major block scales
   const float *gscale;      // [E] or null
-  const uint16_t *A;        // FC1: x [T, H]; FC2: act [R, I]
-  const int32_t *perm;      // FC1: perm_to_expanded (row p reads x row perm[p] / ktop); FC2: null
-  int ktop;
+  const uint16_t *A;        // bf16 activation rows in expert order: FC1 x gathered [R, H]; FC2 act [R, I]
   const int32_t *offsets;   // [E + 1]
   uint16_t *out_a;          // FC1: act [R, I] bf16
   float *out_y;             // FC2: y [R, H] fp32
@@ -231,6 +229,7 @@ struct PrefillArgs {
   const float *g1, *g2;      // global scales [E] or null
   const uint16_t *w1d;       // bf16 [E, 2I, H] given by the caller, or null (fused FC1)
   const uint16_t *w2d;       // bf16 [E, H, I] given by the caller, or null (fused FC2)
+  uint16_t *xp;              // bf16 [T * k, H] x gathered in expert order (fused FC1), or null
   uint16_t *act;             // bf16 [T * k, I] FC1 activations, permuted order
   float *y;                  // fp32 [T * k, H] FC2 rows, permuted order
   uint16_t *out;             // bf16 [T, H]

@@ -235,10 +235,12 @@ def test_prefill_workspace_sizes(qm):
     km = qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4 | qm.SCALES_KMAJOR)
     s1_bytes, s2_bytes = E * 2 * I * (H // 16), E * H * (I // 16)
     assert page - km == s1_bytes + s2_bytes
-    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, True) == km
-    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, (True, False)) == km + s2_bytes
-    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, (False, True)) == km + s1_bytes
-    # routing maps, activations (bf16 [R, I]) and FC2 rows (fp32 [R, H]) at least
+    # the fused FC1 reads x gathered in expert order (bf16 [R, H])
     R = T * k
-    assert km >= qm.WORKSPACE_HEADER_BYTES + R * I * 2 + R * H * 4
-    assert km < qm.WORKSPACE_HEADER_BYTES + R * I * 2 + R * H * 4 + 64 * R + 8192
+    xp_bytes = R * H * 2
+    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, True) == km - xp_bytes
+    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, (True, False)) == km - xp_bytes + s2_bytes
+    assert qm.forward_workspace_bytes(T, H, I, E, k, qm.NVFP4, (False, True)) == km + s1_bytes
+    # routing maps, gathered x, activations (bf16 [R, I]) and FC2 rows (fp32 [R, H]) at least
+    assert km >= qm.WORKSPACE_HEADER_BYTES + xp_bytes + R * I * 2 + R * H * 4
+    assert km < qm.WORKSPACE_HEADER_BYTES + xp_bytes + R * I * 2 + R * H * 4 + 64 * R + 8192
