@@ -50,9 +50,19 @@ constexpr int kAccCols = 256;  // tensor-memory columns between the two accumula
 // L2 latency, the decoded ring only the MMA's own latency.
 constexpr int kPStages = 8, kBStages = 5, kAStages = 3;
 constexpr int kBoxRows = 16;  // activation rows per tensor copy
-constexpr int kWarpMma = 0, kWarpTma = 1, kWarpRows = 2, kWarpDec0 = 3, kDecThreads = 256, kWarpEpi0 = 11,
-              kEpiThreads = 128;
-constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 480
+// CTAs of a cluster share one row chunk (consecutive column blocks): each
+// copies a quarter of the activation boxes, multicast to all of them.
+constexpr int kCluster = 4;
+constexpr int kPLag = kPStages - 2;  // packed stages in flight before the copying warp publishes one
+// Warp roles.  Warp w issues from scheduler w % 4, whose instruction cache
+// it shares: the MMA warp's scheduler also runs only the two copy loops and
+// one epilogue warp, the decoders' large unrolled loop runs on the other three.
+//   scheduler 0: warp 0 MMA, 4 activation rows, 8 packed codes, 12 epilogue
+//   schedulers 1-3: warps 1-3, 5-7, 9-10 decode, 11 idle, 13-15 epilogue
+constexpr int kWarpMma = 0, kWarpRows = 4, kWarpCodes = 8, kWarpEpi0 = 12, kDecThreads = 256, kEpiThreads = 128;
+constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 512
+// decoder index of warp w (w % 4 != 0, w < kWarpEpi0): 0..8 in warp order
+__host__ __device__ constexpr int dec_index(int w) { return (w / 4) * 3 + (w % 4) - 1; }
 constexpr int kATile = kBM * kBK * 2;     // 16 KB
 constexpr int kBTile = kMaxN * kBK * 2;   // 24 KB
 constexpr int kCodeBytes = kBK * kBM / 2; // 4 KB: 64 k rows x 64 bytes
@@ -63,19 +73,22 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
 static_assert(kMaxN <= kAccCols && 2 * kAccCols <= (int)kTmemCols, "two accumulator buffers");
 static_assert(kSmem <= 227 * 1024 - 4096, "stages fit in shared memory");
-static_assert(kEpiThreads == 128, "four epilogue warps: warp w reads tensor-memory lanes 32 (w % 4) ..");
+static_assert(kEpiThreads == 128 && kWarpEpi0 % 4 == 0,
+              "four epilogue warps: warp w reads tensor-memory lanes 32 (w % 4) ..");
+static_assert(dec_index(kWarpEpi0 - 1) + 1 >= kDecThreads / 32, "enough decoder warps");
 
 // MODE: 0 first GEMM, gate / linear interleaved (columns 2m, 2m + 1);
 //       1 first GEMM, concatenated (columns m, I + m);
 //       2 second GEMM.
 struct Params {
-  CUtensorMap tm_codes;    // packed codes as bytes: [E*K rows][N/2]
-  CUtensorMap tm_scales;   // k-major block scales as bytes: [E*K/bs rows][N]
   CUtensorMap tm_rows;     // bf16 activation rows in expert order [R][K], 128-byte swizzle, 64 x 16 boxes
+  const uint8_t *codes;    // packed codes [E*K rows][N/2]
+  const uint8_t *scales;   // k-major block scales [E*K/bs rows][N]
   const int32_t *offsets;  // [E + 1] first permuted row of each expert
   const float *gscale;     // [E] global scales, or null
   int E, K, N, I;          // expert weight: K x N; I: first GEMM's output width
   int ncb;                 // column blocks: I / 64 (first GEMM), ceil(N / 128) (second)
+  int ncbg;                // column-block groups: ceil(ncb / kCluster)
   uint16_t *out_a;         // first GEMM: [R, I] bf16
   float *out_y;            // second GEMM: [R, N] fp32
   float alpha, beta, limit;
@@ -95,11 +108,14 @@ struct Tile {
   int e, cb, r0, rows, nr;
 };
 
-// Chunk c of the expert-ordered chunk list, column block cb.
-__device__ __forceinline__ Tile tile_at(const Params &p, const int *cpre, const int *offs, int t) {
+// Cluster tile st = (chunk c of the expert-ordered chunk list, column-block
+// group g); this CTA's column block is g * kCluster + its rank (>= ncb for
+// the padding CTAs of a last, partial group: they copy and compute, but
+// store nothing).
+__device__ __forceinline__ Tile tile_at(const Params &p, const int *cpre, const int *offs, int st, int rank) {
   Tile T;
-  const int c = t / p.ncb;
-  T.cb = t - c * p.ncb;
+  const int c = st / p.ncbg;
+  T.cb = (st - c * p.ncbg) * kCluster + rank;
   int lo = 0, hi = p.E;  // cpre[lo] <= c < cpre[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -113,6 +129,38 @@ __device__ __forceinline__ Tile tile_at(const Params &p, const int *cpre, const 
   T.rows = min(cs, n - j * cs);
   T.nr = (T.rows + 15) & ~15;
   return T;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2-D tensor copy multicast to the CTAs of `mask`: each receives the box at
+// the same shared-memory offset and a complete_tx on its mbarrier at `bar`'s
+// offset.
+__device__ __forceinline__ void tensor_g2s_2d_mc(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                                 uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
+// Non-blocking test of a phase: issued early, its result is read only later,
+// so that the check's latency overlaps other work.
+__device__ __forceinline__ uint32_t mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done;
 }
 
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_s,
@@ -155,16 +203,23 @@ __device__ __forceinline__ float swiglu_fast(float gate, float lin, float alpha,
 
 // ---- roles ----------------------------------------------------------------------
 
+// Packed codes (64 k rows x 64 bytes) and k-major scale rows of a stage,
+// copied by the 32 lanes of one warp with cp.async (the load/store path, so
+// that the copy engine serves the activation rows alone); a stage is
+// published kPLag stages later, once the lane's copies have landed.
 template <int MODE, int FMT>
-__device__ __forceinline__ void tma_role(const Params &p, const int *cpre, const int *offs, int ntiles,
-                                         unsigned char *P_ring, Bars &B, volatile int *abort_s) {
+__device__ __forceinline__ void codes_role(const Params &p, const int *cpre, const int *offs, int nst, int rank,
+                                           unsigned char *P_ring, Bars &B, volatile int *abort_s, int lane) {
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   constexpr int NSR = kBK / BS;  // scale block rows per stage
   const int KT = p.K / kBK;
+  const int rowb = p.N / 2;
+  const int nclu = (int)gridDim.x / kCluster;
   uint32_t it = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-    const Tile T = tile_at(p, cpre, offs, t);
+  for (int st = (int)blockIdx.x / kCluster; st < nst && ok; st += nclu) {
+    const Tile T = tile_at(p, cpre, offs, st, rank);
+    const bool live = T.cb < p.ncb;
     for (int kt = 0; kt < KT; ++kt, ++it) {
       const int s = (int)(it % kPStages);
       const uint32_t u = it / kPStages;
@@ -173,57 +228,87 @@ __device__ __forceinline__ void tma_role(const Params &p, const int *cpre, const
         break;
       }
       unsigned char *P = P_ring + (size_t)s * kPTile;
-      mbar_expect_tx(&B.pk_full[s], (uint32_t)(kCodeBytes + NSR * 128));
-      const int yc = T.e * p.K + kt * kBK, ys = T.e * (p.K / BS) + kt * NSR;
-      if constexpr (MODE == 1) {
-        tensor_g2s_2d(P, &p.tm_codes, 32 * T.cb, yc, &B.pk_full[s]);
-        tensor_g2s_2d(P + kCodeBytes / 2, &p.tm_codes, (p.I + 64 * T.cb) / 2, yc, &B.pk_full[s]);
-        tensor_g2s_2d(P + kCodeBytes, &p.tm_scales, 64 * T.cb, ys, &B.pk_full[s]);
-        tensor_g2s_2d(P + kCodeBytes + NSR * 64, &p.tm_scales, p.I + 64 * T.cb, ys, &B.pk_full[s]);
-      } else {
-        tensor_g2s_2d(P, &p.tm_codes, 64 * T.cb, yc, &B.pk_full[s]);
-        tensor_g2s_2d(P + kCodeBytes, &p.tm_scales, 128 * T.cb, ys, &B.pk_full[s]);
+      const size_t row0 = (size_t)T.e * p.K + kt * kBK;
+      if (live) {
+        // codes: 256 chunks of 16 bytes, 8 per lane
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int ch = lane + 32 * c8, r = ch >> 2, cc = ch & 3;
+          if constexpr (MODE == 1) {
+            const int piece = cc >> 1, c2 = cc & 1;
+            const int xb = piece ? (p.I + 64 * T.cb) / 2 : 32 * T.cb;
+            cp_async16(P + piece * (kCodeBytes / 2) + r * 32 + c2 * 16, p.codes + (row0 + r) * rowb + xb + c2 * 16);
+          } else {
+            const int xb = 64 * T.cb + cc * 16;
+            if (xb < rowb) cp_async16(P + r * 64 + cc * 16, p.codes + (row0 + r) * rowb + xb);
+          }
+        }
+        // scales: NSR rows x 128 bytes
+        if (lane < NSR * 8) {
+          const int r = lane >> 3, cc = lane & 7;
+          const size_t srow = (size_t)T.e * (p.K / BS) + kt * NSR + r;
+          if constexpr (MODE == 1) {
+            const int piece = cc >> 2, c4 = cc & 3;
+            const int xb = piece ? p.I + 64 * T.cb : 64 * T.cb;
+            cp_async16(P + kCodeBytes + piece * NSR * 64 + r * 64 + c4 * 16, p.scales + srow * p.N + xb + c4 * 16);
+          } else {
+            const int xb = 128 * T.cb + cc * 16;
+            if (xb < p.N) cp_async16(P + kCodeBytes + r * 128 + cc * 16, p.scales + srow * p.N + xb);
+          }
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (it >= (uint32_t)kPLag) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kPLag) : "memory");
+        mbar_arrive(&B.pk_full[(it - kPLag) % kPStages]);
       }
     }
   }
-  // copies still in flight land before the CTA leaves (a no-op when every
-  // stage was consumed)
-  const uint32_t n = it < (uint32_t)kPStages ? it : (uint32_t)kPStages;
-  for (uint32_t d = 1; d <= n; ++d) {
-    const uint32_t j = it - d;
-    wait_bounded(&B.pk_full[j % kPStages], (j / kPStages) & 1u, abort_s, p.err_flag, 411);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (ok) {
+    const uint32_t n = it < (uint32_t)kPLag ? it : (uint32_t)kPLag;
+    for (uint32_t d = n; d >= 1; --d) mbar_arrive(&B.pk_full[(it - d) % kPStages]);
   }
 }
 
 // Activation rows of a stage: nr rows x 64 k as tensor copies of 16 rows,
 // written by the copy engine in the 128-byte-swizzled K-major layout the MMA
 // descriptor reads (rows past the chunk's end are the next expert's or the
-// copy's zero fill; their accumulator columns are never stored).
-__device__ __forceinline__ void rows_role(const Params &p, const int *cpre, const int *offs, int ntiles,
+// copy's zero fill; their accumulator columns are never stored).  Every CTA
+// of the cluster needs the same rows: CTA `rank` copies boxes rank,
+// rank + kCluster, ... multicast to all, and expects the whole stage.
+__device__ __forceinline__ void rows_role(const Params &p, const int *cpre, const int *offs, int nst, int rank,
                                           unsigned char *B_ring, Bars &B, volatile int *abort_s) {
   const int KT = p.K / kBK;
+  const int nclu = (int)gridDim.x / kCluster;
+  const uint16_t all = (uint16_t)((1u << kCluster) - 1u);
   uint32_t it = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-    const Tile T = tile_at(p, cpre, offs, t);
+  for (int st = (int)blockIdx.x / kCluster; st < nst && ok; st += nclu) {
+    const Tile T = tile_at(p, cpre, offs, st, rank);
     const int nbox = T.nr / kBoxRows;
     for (int kt = 0; kt < KT; ++kt, ++it) {
       const int s = (int)(it % kBStages);
       const uint32_t u = it / kBStages;
+      // the stage is free in every CTA of the cluster (b_empty counts their MMA commits)
       if (!wait_bounded(&B.b_empty[s], (u & 1u) ^ 1u, abort_s, p.err_flag, 420)) {
         ok = false;
         break;
       }
       unsigned char *Bs = B_ring + (size_t)s * kBTile;
       mbar_expect_tx(&B.b_full[s], (uint32_t)(nbox * kBoxRows * kBK * 2));
-      for (int b = 0; b < nbox; ++b)
-        tensor_g2s_2d(Bs + b * (kBoxRows * kBK * 2), &p.tm_rows, kt * kBK, T.r0 + b * kBoxRows, &B.b_full[s]);
+      for (int b = rank; b < nbox; b += kCluster)
+        tensor_g2s_2d_mc(Bs + b * (kBoxRows * kBK * 2), &p.tm_rows, kt * kBK, T.r0 + b * kBoxRows, &B.b_full[s],
+                         all);
     }
   }
+  // before the CTA may leave: the copies into it have landed, and every CTA's
+  // MMA commits for the last stages (remote arrivals on b_empty) are in
   const uint32_t n = it < (uint32_t)kBStages ? it : (uint32_t)kBStages;
   for (uint32_t d = 1; d <= n; ++d) {
     const uint32_t j = it - d;
     wait_bounded(&B.b_full[j % kBStages], (j / kBStages) & 1u, abort_s, p.err_flag, 421);
+    wait_bounded(&B.b_empty[j % kBStages], (j / kBStages) & 1u, abort_s, p.err_flag, 422);
   }
 }
 
@@ -311,14 +396,17 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const int *offs, int ntiles,
+__device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const int *offs, int nst, int rank,
                                          const unsigned char *A_ring, const unsigned char *B_ring, Bars &B,
                                          uint32_t tmem, volatile int *abort_s) {
   const int KT = p.K / kBK;
   uint32_t it = 0, tl = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
-    const Tile T = tile_at(p, cpre, offs, t);
+  const int nclu = (int)gridDim.x / kCluster;
+  const uint16_t all = (uint16_t)((1u << kCluster) - 1u);
+  bool ready = false;  // the next stage's barriers were found complete
+  for (int st = (int)blockIdx.x / kCluster; st < nst && ok; st += nclu, ++tl) {
+    const Tile T = tile_at(p, cpre, offs, st, rank);
     const uint32_t ab = tl & 1u, ua = tl >> 1;
     if (!wait_bounded(&B.acc_empty[ab], (ua & 1u) ^ 1u, abort_s, p.err_flag, 440)) break;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -328,12 +416,17 @@ __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const
                            ((uint32_t)(kBM >> 4) << 24);
     for (int kt = 0; kt < KT; ++kt, ++it) {
       const int sa = (int)(it % kAStages), sb = (int)(it % kBStages);
-      if (!wait_bounded(&B.a_full[sa], (it / kAStages) & 1u, abort_s, p.err_flag, 441) ||
-          !wait_bounded(&B.b_full[sb], (it / kBStages) & 1u, abort_s, p.err_flag, 442)) {
+      // the test of this stage's barriers was issued during the previous
+      // stage's MMAs; wait only if it found them incomplete
+      if (!ready && (!wait_bounded(&B.a_full[sa], (it / kAStages) & 1u, abort_s, p.err_flag, 441) ||
+                     !wait_bounded(&B.b_full[sb], (it / kBStages) & 1u, abort_s, p.err_flag, 442))) {
         ok = false;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t nx = it + 1;
+      const uint32_t ta = mbar_test(&B.a_full[nx % kAStages], (nx / kAStages) & 1u);
+      const uint32_t tb = mbar_test(&B.b_full[nx % kBStages], (nx / kBStages) & 1u);
       const uint32_t a_addr = smem_addr(A_ring + (size_t)sa * kATile), b_addr = smem_addr(B_ring + (size_t)sb * kBTile);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -346,7 +439,13 @@ __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const
             : "memory");
       }
       mma_commit(&B.a_empty[sa]);
-      mma_commit(&B.b_empty[sb]);
+      // the activation stage is free for the copies once every CTA's MMAs are done with it
+      asm volatile(
+          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+              smem_addr(&B.b_empty[sb])),
+          "h"(all)
+          : "memory");
+      ready = (ta & tb) != 0u;
     }
     if (!ok) break;
     mma_commit(&B.acc_full[ab]);
@@ -359,8 +458,8 @@ __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const
 // Epilogue thread: tensor-memory lane 32q + l = M-side row 16j + w, i.e. tile
 // column n = 8w + j with w = l & 15, j = 2q + (l >> 4).
 template <int MODE>
-__device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, const int *offs, int ntiles, Bars &B,
-                                              uint32_t tmem, volatile int *abort_s, int warp) {
+__device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, const int *offs, int nst, int rank,
+                                              Bars &B, uint32_t tmem, volatile int *abort_s, int warp) {
   const int q = warp & 3, lane = (int)lane_id();
   const int w = lane & 15, j = 2 * q + (lane >> 4), n = 8 * w + j;
   // first GEMM: (gate, linear) partners are lanes l and l ^ 16 (interleaved:
@@ -371,14 +470,16 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const int *cpre, 
   const bool gate = MODE == 0 ? (lane < 16) : (w < 8);
   const int m_in = MODE == 0 ? 4 * w + q : 8 * (w & 7) + j;  // output column of the pair within the tile
   uint32_t tl = 0;
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
-    const Tile T = tile_at(p, cpre, offs, t);
+  const int nclu = (int)gridDim.x / kCluster;
+  for (int st = (int)blockIdx.x / kCluster; st < nst; st += nclu, ++tl) {
+    const Tile T = tile_at(p, cpre, offs, st, rank);
     const uint32_t ab = tl & 1u, ua = tl >> 1;
     if (!wait_bounded(&B.acc_full[ab], ua & 1u, abort_s, p.err_flag, 450)) return;
+    const bool live = T.cb < p.ncb;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const float g = p.gscale ? __ldg(p.gscale + T.e) : 1.0f;
     const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + ab * (uint32_t)kAccCols;
-    for (int cc = 0; cc * 32 < T.nr; ++cc) {
+    for (int cc = 0; live && cc * 32 < T.nr; ++cc) {
       uint32_t v[32];
       asm volatile(
           "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -435,9 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  } else if (warp == kWarpTma && lane == 0) {
+  } else if (warp == kWarpCodes && lane == 0) {
     for (int i = 0; i < kPStages; ++i) {
-      mbar_init(&B.pk_full[i], 1);
+      mbar_init(&B.pk_full[i], 32);
       mbar_init(&B.pk_empty[i], kDecThreads);
     }
     for (int i = 0; i < kAStages; ++i) {
@@ -446,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
     }
     for (int i = 0; i < kBStages; ++i) {
       mbar_init(&B.b_full[i], 1);
-      mbar_init(&B.b_empty[i], 1);
+      mbar_init(&B.b_empty[i], kCluster);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.acc_full[i], 1);
@@ -482,27 +583,35 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  // every CTA's barriers are initialised before a peer's multicast signals them
+  cluster_sync();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_s;
-  const int ntiles = cpre[p.E] * p.ncb;
+  const int rank = (int)cluster_rank();
+  const int nst = cpre[p.E] * p.ncbg;
 
   if (warp == kWarpMma) {
-    if (lane == 0) mma_role(p, cpre, offs, ntiles, A_ring, B_ring, B, tmem, &abort_s);
+    if (lane == 0) mma_role(p, cpre, offs, nst, rank, A_ring, B_ring, B, tmem, &abort_s);
     __syncwarp();
-  } else if (warp == kWarpTma) {
-    if (lane == 0) tma_role<MODE, FMT>(p, cpre, offs, ntiles, P_ring, B, &abort_s);
-    __syncwarp();
+  } else if (warp == kWarpCodes) {
+    codes_role<MODE, FMT>(p, cpre, offs, nst, rank, P_ring, B, &abort_s, lane);
   } else if (warp == kWarpRows) {
-    if (lane == 0) rows_role(p, cpre, offs, ntiles, B_ring, B, &abort_s);
+    if (lane == 0) rows_role(p, cpre, offs, nst, rank, B_ring, B, &abort_s);
     __syncwarp();
   } else if (warp < kWarpEpi0) {
-    const int mine = (int)blockIdx.x < ntiles ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    decoder_role<MODE, FMT>(p, mine * (p.K / kBK), A_ring, P_ring, B, &abort_s, tid - 32 * kWarpDec0);
+    const int di = dec_index(warp);
+    if (di < kDecThreads / 32) {
+      const int ci = (int)blockIdx.x / kCluster, nclu = (int)gridDim.x / kCluster;
+      const int mine = ci < nst ? (nst - ci + nclu - 1) / nclu : 0;
+      decoder_role<MODE, FMT>(p, mine * (p.K / kBK), A_ring, P_ring, B, &abort_s, 32 * di + lane);
+    }
   } else {
-    epilogue_role<MODE>(p, cpre, offs, ntiles, B, tmem, &abort_s, warp);
+    epilogue_role<MODE>(p, cpre, offs, nst, rank, B, tmem, &abort_s, warp);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  // no CTA leaves while a peer may still multicast into it or signal its barriers
+  cluster_sync();
   if (warp == kWarpMma) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -533,25 +642,6 @@ static cudaError_t encode_fn(EncodeTiledFn *out) {
   return cudaSuccess;
 }
 
-static cudaError_t encode_bytes_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                                   uint32_t box_rows) {
-  EncodeTiledFn f = nullptr;
-  cudaError_t err = encode_fn(&f);
-  if (err != cudaSuccess) return err;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return cudaErrorInvalidValue;
-  }
-  return cudaSuccess;
-}
-
 // bf16 rows [rows][cols] as a tensor map with 64 x kBoxRows boxes in the
 // 128-byte swizzle (16-byte chunk c of box row r at chunk c ^ (r & 7)).
 static cudaError_t encode_rows_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
@@ -572,53 +662,70 @@ static cudaError_t encode_rows_sw128(CUtensorMap *m, const void *base, uint64_t 
   return cudaSuccess;
 }
 
+// Launch as clusters of kCluster CTAs, one CTA per SM, as many clusters as
+// fit on the device at once (at most one per cluster tile).
 template <int MODE, int FMT>
-static cudaError_t launch_mode(const Params &p, int grid, cudaStream_t stream) {
-  static std::atomic<int> smem_set[kMaxDevices];
+static cudaError_t launch_mode(const Params &p, long long max_clusters, cudaStream_t stream) {
+  static std::atomic<int> fit[kMaxDevices];  // clusters resident at once, per device (0: not yet known)
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   auto kfn = fp4_grouped_gemm_kernel<MODE, FMT>;
-  if (!smem_set[dev].load(std::memory_order_acquire)) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = fit[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
-    smem_set[dev].store(1, std::memory_order_release);
+    cfg.gridDim = dim3(kCluster * (unsigned)(num_sms() / kCluster), 1, 1);
+    err = cudaOccupancyMaxActiveClusters(&n, kfn, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n < 1) {
+      set_error("the fused prefill GEMM's %d-CTA clusters do not fit on this device", kCluster);
+      return cudaErrorInvalidConfiguration;
+    }
+    fit[dev].store(n, std::memory_order_release);
   }
-  kfn<<<grid, kThreads, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  const long long clusters = max_clusters < n ? max_clusters : n;
+  cfg.gridDim = dim3((unsigned)(clusters * kCluster), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kfn, p);
 }
 
 }  // namespace fg
 
 cudaError_t launch_fp4_gemm(const Fp4GemmArgs &a, cudaStream_t stream) {
   using namespace fg;
-  const int bs = block_size(a.fmt);
   Params p{};
   const bool first = a.mode != 2;
   const int N = first ? 2 * a.I : a.H, K = first ? a.H : a.I;
   const int R = a.R;
   if (R <= 0) return cudaSuccess;
+  p.codes = a.w; p.scales = a.s;
   p.offsets = a.offsets; p.gscale = a.gscale;
   p.E = a.E; p.K = K; p.N = N; p.I = a.I;
   p.ncb = first ? a.I / 64 : (a.H + kBM - 1) / kBM;
+  p.ncbg = (p.ncb + kCluster - 1) / kCluster;
   p.out_a = a.out_a; p.out_y = a.out_y;
   p.alpha = a.alpha; p.beta = a.beta; p.limit = a.limit;
   p.err_flag = a.err_flag;
-  const uint32_t code_box = a.mode == 1 ? 32u : 64u, scale_box = a.mode == 1 ? 64u : 128u;
-  cudaError_t err = encode_bytes_2d(&p.tm_codes, a.w, (uint64_t)N / 2, (uint64_t)a.E * K, code_box, (uint32_t)kBK);
+  cudaError_t err = encode_rows_sw128(&p.tm_rows, a.A, (uint64_t)K, (uint64_t)R);
   if (err != cudaSuccess) return err;
-  err = encode_bytes_2d(&p.tm_scales, a.s, (uint64_t)N, (uint64_t)a.E * (K / bs), scale_box, (uint32_t)(kBK / bs));
-  if (err != cudaSuccess) return err;
-  err = encode_rows_sw128(&p.tm_rows, a.A, (uint64_t)K, (uint64_t)R);
-  if (err != cudaSuccess) return err;
-  // tiles <= (sum over experts of ceil(rows / 256)) * column blocks
+  // cluster tiles <= (sum over experts of ceil(rows / kMaxN)) * column-block groups
   const long long chunks = (long long)R / kMaxN + (a.E < R ? a.E : R) + 1;
-  long long grid = chunks * p.ncb;
-  if (grid > num_sms()) grid = num_sms();
+  const long long max_clusters = chunks * p.ncbg;
   const bool nv = a.fmt == QMOE_NVFP4;
   switch (a.mode) {
-    case 0: return nv ? launch_mode<0, QMOE_NVFP4>(p, (int)grid, stream) : launch_mode<0, QMOE_MXFP4>(p, (int)grid, stream);
-    case 1: return nv ? launch_mode<1, QMOE_NVFP4>(p, (int)grid, stream) : launch_mode<1, QMOE_MXFP4>(p, (int)grid, stream);
-    default: return nv ? launch_mode<2, QMOE_NVFP4>(p, (int)grid, stream) : launch_mode<2, QMOE_MXFP4>(p, (int)grid, stream);
+    case 0: return nv ? launch_mode<0, QMOE_NVFP4>(p, max_clusters, stream) : launch_mode<0, QMOE_MXFP4>(p, max_clusters, stream);
+    case 1: return nv ? launch_mode<1, QMOE_NVFP4>(p, max_clusters, stream) : launch_mode<1, QMOE_MXFP4>(p, max_clusters, stream);
+    default: return nv ? launch_mode<2, QMOE_NVFP4>(p, max_clusters, stream) : launch_mode<2, QMOE_MXFP4>(p, max_clusters, stream);
   }
 }
 
