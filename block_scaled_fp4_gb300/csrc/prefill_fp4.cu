@@ -11,29 +11,32 @@
 //    the 128-byte swizzle.  The value written is the exact product
 //    e2m1 * block scale (at most 6 significant bits, so exact in bf16); the
 //    expert's global scale multiplies the fp32 accumulator in the epilogue;
-//  * N side ("B") = the expert's permuted token rows p, 16..256 of them (one
-//    row chunk of one expert), gathered bf16 activation rows;
+//  * N side ("B") = the expert's token rows p in expert order, 16..192 of
+//    them (one row chunk of one expert);
 //  * fp32 accumulator in tensor memory, double-buffered (2 x 256 columns) so
 //    that one tile's epilogue overlaps the next tile's MMAs.
-// A row chunk is all of an expert's rows when they number <= 256, else an
+// A row chunk is all of an expert's rows when they number <= 192, else an
 // even split in multiples of 16: the MMA's N follows the expert's row count,
 // so an expert with 130 rows costs 144 columns, not two 128-row tiles.
 //
-// Roles (persistent CTAs, one per SM, tiles taken round-robin):
-//  * warp 0: tensor-memory allocation; lane 0 issues tcgen05.mma
-//    (kind::f16, M = 128, N = tile rows, K = 16, four per 64-deep stage) and
-//    commits stage and accumulator barriers;
-//  * warp 1, lane 0: tensor copies of the packed codes (64 k rows x 64 bytes)
-//    and the k-major scale rows of a stage;
-//  * warps 2-3: cp.async gather of the activation rows (perm_to_expanded / k
-//    for the first GEMM), published with a lag of two stages;
-//  * warps 4-7: decode codes x scales -> bf16 into the stage's M-side tile;
-//  * warps 8-11: epilogue: tcgen05.ld of the accumulator, x global scale,
-//    SwiGLU of the (gate, linear) pair and bf16 store of the activation
-//    (first GEMM), or fp32 store of the FC2 row (second GEMM).
+// Clusters of four CTAs (one per SM) take cluster tiles round-robin: a
+// cluster tile is one row chunk and four consecutive column blocks, one per
+// CTA, so the four CTAs need the same activation rows.  Roles in a CTA:
+//  * MMA (one thread): tcgen05.mma kind::f16, M = 128, N = chunk rows,
+//    K = 16, four per 64-deep stage; commits release the decoded stage
+//    locally and the activation stage in all four CTAs (multicast commit);
+//    the next stage's barriers are tested while this stage's MMAs issue;
+//  * activation rows (one thread): 16-row tensor copies in the 128-byte
+//    swizzle, each CTA copying a quarter of a stage's boxes multicast to the
+//    cluster, every CTA expecting the whole stage;
+//  * packed codes and k-major scale rows (one warp, cp.async);
+//  * decoders (eight warps): codes x scales -> bf16 M-side tile;
+//  * epilogue (four warps, one per tensor-memory lane quadrant):
+//    tcgen05.ld, x global scale, SwiGLU of the (gate, linear) pair and bf16
+//    store of the activation (first GEMM), or fp32 store of the FC2 row.
 // Every wait is bounded: on a timeout the CTA sets the device error flag,
-// stops, waits (bounded) for its copies and MMAs in flight and frees its
-// tensor memory.
+// stops, waits (bounded) for its copies and MMAs in flight, meets its
+// cluster and frees its tensor memory.
 #include <atomic>
 
 #include "decode_common.cuh"
@@ -43,12 +46,16 @@ namespace qmoe {
 namespace fg {
 
 constexpr int kBM = 128;     // weight columns per tile (MMA M, tensor-memory lanes)
-constexpr int kBK = 64;      // k rows per stage: one 128-byte swizzled row of bf16
-constexpr int kMaxN = 192;   // token rows per tile (MMA N)
+constexpr int kAtomK = 64;   // k of one 128-byte swizzled row of bf16 (a swizzle atom's depth)
+constexpr int kBK = 128;     // k rows per stage: two atoms side by side, eight MMAs
+constexpr int kHalves = kBK / kAtomK;
+constexpr int kMaxN = 160;   // token rows per tile (MMA N)
 constexpr int kAccCols = 256;  // tensor-memory columns between the two accumulator buffers
 // Ring depths: the packed-weight ring covers HBM latency, the activation ring
-// L2 latency, the decoded ring only the MMA's own latency.
-constexpr int kPStages = 8, kBStages = 5, kAStages = 3;
+// L2 latency, the decoded ring only the MMA's own latency.  A stage is 128
+// deep so that the MMA thread's barrier tests and commits (each costs it
+// about as much as an MMA issue) come once per eight MMAs.
+constexpr int kPStages = 4, kBStages = 3, kAStages = 2;
 constexpr int kBoxRows = 16;  // activation rows per tensor copy
 // CTAs of a cluster share one row chunk (consecutive column blocks): each
 // copies a quarter of the activation boxes, multicast to all of them.
@@ -63,16 +70,19 @@ constexpr int kWarpMma = 0, kWarpRows = 4, kWarpCodes = 8, kWarpEpi0 = 12, kDecT
 constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 512
 // decoder index of warp w (w % 4 != 0, w < kWarpEpi0): 0..8 in warp order
 __host__ __device__ constexpr int dec_index(int w) { return (w / 4) * 3 + (w % 4) - 1; }
-constexpr int kATile = kBM * kBK * 2;     // 16 KB
-constexpr int kBTile = kMaxN * kBK * 2;   // 24 KB
-constexpr int kCodeBytes = kBK * kBM / 2; // 4 KB: 64 k rows x 64 bytes
-constexpr int kScaleBytes = 512;          // <= 4 block rows x 128 columns
+constexpr int kAHalf = kBM * kAtomK * 2;   // 16 KB: one atom-deep M-side tile
+constexpr int kBHalf = kMaxN * kAtomK * 2; // 20 KB: one atom-deep N-side tile
+constexpr int kATile = kHalves * kAHalf;
+constexpr int kBTile = kHalves * kBHalf;
+constexpr int kCodeBytes = kBK * kBM / 2;  // 8 KB: 128 k rows x 64 bytes
+constexpr int kScaleBytes = (kBK / kNvfp4Block) * kBM;  // <= 8 block rows x 128 columns
 constexpr int kPTile = kCodeBytes + kScaleBytes;
 constexpr int kSmem = kAStages * kATile + kBStages * kBTile + kPStages * kPTile + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
 static_assert(kMaxN <= kAccCols && 2 * kAccCols <= (int)kTmemCols, "two accumulator buffers");
 static_assert(kSmem <= 227 * 1024 - 4096, "stages fit in shared memory");
+static_assert(kAHalf % 1024 == 0 && kBHalf % 1024 == 0, "atom tiles start on 1 KB swizzle boundaries");
 static_assert(kEpiThreads == 128 && kWarpEpi0 % 4 == 0,
               "four epilogue warps: warp w reads tensor-memory lanes 32 (w % 4) ..");
 static_assert(dec_index(kWarpEpi0 - 1) + 1 >= kDecThreads / 32, "enough decoder warps");
@@ -212,7 +222,7 @@ __device__ __forceinline__ void codes_role(const Params &p, const int *cpre, con
                                            unsigned char *P_ring, Bars &B, volatile int *abort_s, int lane) {
   constexpr int BS = FMT == QMOE_NVFP4 ? kNvfp4Block : kMxfp4Block;
   constexpr int NSR = kBK / BS;  // scale block rows per stage
-  const int KT = p.K / kBK;
+  const int KT = (p.K + kBK - 1) / kBK;
   const int rowb = p.N / 2;
   const int nclu = (int)gridDim.x / kCluster;
   uint32_t it = 0;
@@ -229,11 +239,13 @@ __device__ __forceinline__ void codes_role(const Params &p, const int *cpre, con
       }
       unsigned char *P = P_ring + (size_t)s * kPTile;
       const size_t row0 = (size_t)T.e * p.K + kt * kBK;
+      const int krows = min(kBK, p.K - kt * kBK);  // 128, or 64 for a trailing half stage
       if (live) {
-        // codes: 256 chunks of 16 bytes, 8 per lane
+        // codes: krows x 64 bytes in chunks of 16 bytes, 16 per lane
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int c8 = 0; c8 < kBK * 4 / 32; ++c8) {
           const int ch = lane + 32 * c8, r = ch >> 2, cc = ch & 3;
+          if (r >= krows) continue;
           if constexpr (MODE == 1) {
             const int piece = cc >> 1, c2 = cc & 1;
             const int xb = piece ? (p.I + 64 * T.cb) / 2 : 32 * T.cb;
@@ -243,9 +255,10 @@ __device__ __forceinline__ void codes_role(const Params &p, const int *cpre, con
             if (xb < rowb) cp_async16(P + r * 64 + cc * 16, p.codes + (row0 + r) * rowb + xb);
           }
         }
-        // scales: NSR rows x 128 bytes
-        if (lane < NSR * 8) {
-          const int r = lane >> 3, cc = lane & 7;
+        // scales: NSR rows x 128 bytes (those of the stage's krows)
+        for (int c = lane; c < NSR * 8; c += 32) {
+          const int r = c >> 3, cc = c & 7;
+          if (r * BS >= krows) continue;
           const size_t srow = (size_t)T.e * (p.K / BS) + kt * NSR + r;
           if constexpr (MODE == 1) {
             const int piece = cc >> 2, c4 = cc & 3;
@@ -279,7 +292,7 @@ __device__ __forceinline__ void codes_role(const Params &p, const int *cpre, con
 // rank + kCluster, ... multicast to all, and expects the whole stage.
 __device__ __forceinline__ void rows_role(const Params &p, const int *cpre, const int *offs, int nst, int rank,
                                           unsigned char *B_ring, Bars &B, volatile int *abort_s) {
-  const int KT = p.K / kBK;
+  const int KT = (p.K + kBK - 1) / kBK;
   const int nclu = (int)gridDim.x / kCluster;
   const uint16_t all = (uint16_t)((1u << kCluster) - 1u);
   uint32_t it = 0;
@@ -296,10 +309,13 @@ __device__ __forceinline__ void rows_role(const Params &p, const int *cpre, cons
         break;
       }
       unsigned char *Bs = B_ring + (size_t)s * kBTile;
-      mbar_expect_tx(&B.b_full[s], (uint32_t)(nbox * kBoxRows * kBK * 2));
-      for (int b = rank; b < nbox; b += kCluster)
-        tensor_g2s_2d_mc(Bs + b * (kBoxRows * kBK * 2), &p.tm_rows, kt * kBK, T.r0 + b * kBoxRows, &B.b_full[s],
-                         all);
+      // one atom-deep half after the other (a trailing stage may hold one half)
+      const int nh = min(kHalves, (p.K - kt * kBK) / kAtomK);
+      mbar_expect_tx(&B.b_full[s], (uint32_t)(nh * nbox * kBoxRows * kAtomK * 2));
+      for (int h = 0; h < nh; ++h)
+        for (int b = rank; b < nbox; b += kCluster)
+          tensor_g2s_2d_mc(Bs + h * kBHalf + b * (kBoxRows * kAtomK * 2), &p.tm_rows, kt * kBK + h * kAtomK,
+                           T.r0 + b * kBoxRows, &B.b_full[s], all);
     }
   }
   // before the CTA may leave: the copies into it have landed, and every CTA's
@@ -313,7 +329,8 @@ __device__ __forceinline__ void rows_role(const Params &p, const int *cpre, cons
 }
 
 // Decoder thread (w, kc, jh): column pairs 2jh, 2jh + 1 of column word w
-// (tile columns 8w + 4jh .. 8w + 4jh + 3) over k rows 8kc..8kc+7.  Tile
+// (tile columns 8w + 4jh .. 8w + 4jh + 3) over k rows 8kc..8kc+7 of each
+// 64-deep half of the stage (its two swizzle-atom tiles).  Tile
 // column n = 8w + j goes to M-side row 16j + w: a store phase of 8 lanes
 // (w0..w0+7, one kc) then covers 8 distinct swizzle chunks.
 template <int MODE, int FMT>
@@ -324,15 +341,19 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
   const int lane = dt & 31, dw = dt >> 5;
   const int w = lane & 15, sw = lane >> 4, kc = 2 * (dw & 3) + sw, jh = dw >> 2;
   const int sr = (8 * kc) / BS;
-  // byte offsets of this thread's code word in row 0 and of its 4 scales
-  int code_off, pitch, sc_off;
+  // byte offsets of this thread's code word in row 0 and of its 4 scales in
+  // the first half; the second half is kAtomK code rows and kAtomK / BS
+  // scale rows further on
+  int code_off, pitch, sc_off, sc_pitch;
   if constexpr (MODE == 1) {
     code_off = (w >> 3) * (kCodeBytes / 2) + (w & 7) * 4;
     pitch = 32;
+    sc_pitch = 64;
     sc_off = kCodeBytes + (w >> 3) * (NSR * 64) + sr * 64 + (w & 7) * 8 + 4 * jh;
   } else {
     code_off = w * 4;
     pitch = 64;
+    sc_pitch = 128;
     sc_off = kCodeBytes + sr * 128 + w * 8 + 4 * jh;
   }
   for (int it = 0; it < my_steps; ++it) {
@@ -342,21 +363,27 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
     const unsigned char *P = P_ring + (size_t)s * kPTile;
     // half-warps read the two rows of a pair in opposite order: their row
     // parities differ, so the 32 loads hit 32 distinct banks
-    uint32_t c[8];
+    uint32_t c[kHalves][8], svh[kHalves];
 #pragma unroll
-    for (int pr = 0; pr < 4; ++pr) {
-      const int ra = 8 * kc + 2 * pr + sw, rb = 8 * kc + 2 * pr + (1 - sw);
-      const uint32_t a = *reinterpret_cast<const uint32_t *>(P + code_off + ra * pitch);
-      const uint32_t b = *reinterpret_cast<const uint32_t *>(P + code_off + rb * pitch);
-      c[2 * pr] = sw ? b : a;
-      c[2 * pr + 1] = sw ? a : b;
+    for (int h = 0; h < kHalves; ++h) {
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        const int ra = h * kAtomK + 8 * kc + 2 * pr + sw, rb = h * kAtomK + 8 * kc + 2 * pr + (1 - sw);
+        const uint32_t a = *reinterpret_cast<const uint32_t *>(P + code_off + ra * pitch);
+        const uint32_t b = *reinterpret_cast<const uint32_t *>(P + code_off + rb * pitch);
+        c[h][2 * pr] = sw ? b : a;
+        c[h][2 * pr + 1] = sw ? a : b;
+      }
+      svh[h] = *reinterpret_cast<const uint32_t *>(P + sc_off + h * (kAtomK / BS) * sc_pitch);
     }
-    const uint32_t sv = *reinterpret_cast<const uint32_t *>(P + sc_off);
     mbar_arrive(&B.pk_empty[s]);
     const int sa = it % kAStages;
     const uint32_t ua = (uint32_t)it / kAStages;
     if (!wait_bounded(&B.a_empty[sa], (ua & 1u) ^ 1u, abort_s, p.err_flag, 431)) return;
-    unsigned char *As = A_ring + (size_t)sa * kATile;
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+    unsigned char *As = A_ring + (size_t)sa * kATile + h * kAHalf;
+    const uint32_t sv = svh[h];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int jj = 2 * jh + q;  // column pair of the word
@@ -366,18 +393,18 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
         const uint16_t s_lo = (uint16_t)(sh & 0xFFFFu), s_hi = (uint16_t)(sh >> 16);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint32_t h = e2m1x2_to_f16x2(c[i] >> (8 * jj));
-          lo[i] = fma_f16_f32((uint16_t)(h & 0xFFFFu), s_lo, -0.0f);
-          hi[i] = fma_f16_f32((uint16_t)(h >> 16), s_hi, -0.0f);
+          const uint32_t v = e2m1x2_to_f16x2(c[h][i] >> (8 * jj));
+          lo[i] = fma_f16_f32((uint16_t)(v & 0xFFFFu), s_lo, -0.0f);
+          hi[i] = fma_f16_f32((uint16_t)(v >> 16), s_hi, -0.0f);
         }
       } else {
         const uint32_t sb = sv >> (16 * q);
         const float f_lo = e8m0_to_f32(sb & 0xFFu), f_hi = e8m0_to_f32((sb >> 8) & 0xFFu);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint32_t h = e2m1x2_to_f16x2(c[i] >> (8 * jj));
-          lo[i] = f16_lo(h) * f_lo;
-          hi[i] = f16_hi(h) * f_hi;
+          const uint32_t v = e2m1x2_to_f16x2(c[h][i] >> (8 * jj));
+          lo[i] = f16_lo(v) * f_lo;
+          hi[i] = f16_hi(v) * f_hi;
         }
       }
       const int ar0 = 16 * (2 * jj) + w, ar1 = ar0 + 16;
@@ -385,6 +412,7 @@ __device__ __forceinline__ void decoder_role(const Params &p, int my_steps, unsi
           make_uint4(bf16x2_of(lo[0], lo[1]), bf16x2_of(lo[2], lo[3]), bf16x2_of(lo[4], lo[5]), bf16x2_of(lo[6], lo[7]));
       *reinterpret_cast<uint4 *>(As + sw128(ar1, kc)) =
           make_uint4(bf16x2_of(hi[0], hi[1]), bf16x2_of(hi[2], hi[3]), bf16x2_of(hi[4], hi[5]), bf16x2_of(hi[6], hi[7]));
+    }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(&B.a_full[sa]);
@@ -399,7 +427,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const int *offs, int nst, int rank,
                                          const unsigned char *A_ring, const unsigned char *B_ring, Bars &B,
                                          uint32_t tmem, volatile int *abort_s) {
-  const int KT = p.K / kBK;
+  const int KT = (p.K + kBK - 1) / kBK;
   uint32_t it = 0, tl = 0;
   bool ok = true;
   const int nclu = (int)gridDim.x / kCluster;
@@ -428,9 +456,13 @@ __device__ __forceinline__ void mma_role(const Params &p, const int *cpre, const
       const uint32_t ta = mbar_test(&B.a_full[nx % kAStages], (nx / kAStages) & 1u);
       const uint32_t tb = mbar_test(&B.b_full[nx % kBStages], (nx / kBStages) & 1u);
       const uint32_t a_addr = smem_addr(A_ring + (size_t)sa * kATile), b_addr = smem_addr(B_ring + (size_t)sb * kBTile);
+      const int nkk = min(kBK, p.K - kt * kBK) / 16;  // 8, or 4 in a trailing half stage
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t da = desc_sw128(a_addr + kk * 32), db = desc_sw128(b_addr + kk * 32);
+        if (kk >= nkk) break;
+        // 16-deep slice kk: atom tile kk / 4, 32 bytes per slice within it
+        const int h = kk / (kAtomK / 16), ks = kk % (kAtomK / 16);
+        const uint64_t da = desc_sw128(a_addr + h * kAHalf + ks * 32), db = desc_sw128(b_addr + h * kBHalf + ks * 32);
         const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
         asm volatile(
             "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -603,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_grouped_gemm_kernel(const __g
     if (di < kDecThreads / 32) {
       const int ci = (int)blockIdx.x / kCluster, nclu = (int)gridDim.x / kCluster;
       const int mine = ci < nst ? (nst - ci + nclu - 1) / nclu : 0;
-      decoder_role<MODE, FMT>(p, mine * (p.K / kBK), A_ring, P_ring, B, &abort_s, 32 * di + lane);
+      decoder_role<MODE, FMT>(p, mine * ((p.K + kBK - 1) / kBK), A_ring, P_ring, B, &abort_s, 32 * di + lane);
     }
   } else {
     epilogue_role<MODE>(p, cpre, offs, nst, rank, B, tmem, &abort_s, warp);
@@ -650,7 +682,7 @@ static cudaError_t encode_rows_sw128(CUtensorMap *m, const void *base, uint64_t 
   if (err != cudaSuccess) return err;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+  const cuuint32_t box[2] = {(cuuint32_t)kAtomK, (cuuint32_t)kBoxRows};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
