@@ -37,17 +37,28 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
   const int seg = (R + W - 1) / W;
   const int lo = w * seg, hi = min(R, lo + seg);
   int32_t *mycnt = cnt + w * E;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const int eid = i < hi ? ids[i] : -1;
-    const bool valid = i < hi && eid >= 0 && eid < E;
-    const int e = valid ? eid : -1 - lane;  // invalid lanes never match anyone
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    const unsigned lt = (1u << lane) - 1u;
-    if (valid) e2p[i] = mycnt[e] + __popc(peers & lt);  // rank within this warp's segment
-    __syncwarp();
-    if (valid && (peers & lt) == 0u) mycnt[e] += __popc(peers);
-    __syncwarp();
+  // kNB rounds of 32 ids are loaded together (independent loads, one
+  // latency), then ranked round by round
+  constexpr int kNB = 8;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32 * kNB) {
+    int eid[kNB];
+#pragma unroll
+    for (int j = 0; j < kNB; ++j) {
+      const int i = base + 32 * j + lane;
+      eid[j] = i < hi ? ids[i] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kNB; ++j) {
+      const int i = base + 32 * j + lane;
+      const bool valid = i < hi && eid[j] >= 0 && eid[j] < E;
+      const int e = valid ? eid[j] : -1 - lane;  // invalid lanes never match anyone
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      if (valid) e2p[i] = mycnt[e] + __popc(peers & lt);  // rank within this warp's segment
+      __syncwarp();
+      if (valid && (peers & lt) == 0u) mycnt[e] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
   // per expert: exclusive prefix over warps
@@ -88,12 +99,23 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
     if (lane == 31) offsets[E] = run;
   }
   __syncthreads();
-  for (int i = lo + lane; i < hi; i += 32) {
-    const int e = ids[i];
-    if (e < 0 || e >= E) continue;
-    const int p = tot[e] + mycnt[e] + e2p[i];
-    e2p[i] = p;
-    p2e[p] = i;
+  for (int base = lo; base < hi; base += 32 * kNB) {
+    int ev[kNB], rv[kNB];
+#pragma unroll
+    for (int j = 0; j < kNB; ++j) {
+      const int i = base + 32 * j + lane;
+      ev[j] = i < hi ? ids[i] : -1;
+      rv[j] = i < hi ? e2p[i] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kNB; ++j) {
+      const int i = base + 32 * j + lane;
+      const int e = ev[j];
+      if (i >= hi || e < 0 || e >= E) continue;
+      const int pr = tot[e] + mycnt[e] + rv[j];
+      e2p[i] = pr;
+      p2e[pr] = i;
+    }
   }
 }
 
