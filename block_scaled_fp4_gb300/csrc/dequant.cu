@@ -18,6 +18,8 @@
 //    and a normal-range product the fp32 product is exact and its low 16 bits
 //    are zero, so the bf16 is just the top half; otherwise the product is
 //    formed exactly in fp64 and rounded to bf16 through round-to-odd fp32.
+#include <atomic>
+
 #include "qmoe_common.cuh"
 
 namespace qmoe {
@@ -134,16 +136,21 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t *__re
 
 cudaError_t launch_dequant(const uint8_t *packed, const uint8_t *scales, const float *g, int E, int N, int K,
                            int fmt, uint16_t *out, cudaStream_t stream) {
-  static int blocks_per_sm[2] = {0, 0};
+  // resident CTAs per SM, per device and format (0: not yet known)
+  static std::atomic<int> blocks_per_sm[kMaxDevices][2];
   const long long ntiles = (long long)E * (N / kDqTileN) * (K / kDqTileK);
   if (ntiles == 0) return cudaSuccess;
-  int &bps = blocks_per_sm[fmt == QMOE_NVFP4 ? 0 : 1];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::atomic<int> &cache = blocks_per_sm[dev][fmt == QMOE_NVFP4 ? 0 : 1];
+  int bps = cache.load(std::memory_order_relaxed);
   if (bps == 0) {
     cudaError_t err = fmt == QMOE_NVFP4
                           ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, dequant_kernel<QMOE_NVFP4>, kDqThreads, 0)
                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, dequant_kernel<QMOE_MXFP4>, kDqThreads, 0);
     if (err != cudaSuccess) return err;
     if (bps < 1) bps = 1;
+    cache.store(bps, std::memory_order_relaxed);
   }
   long long grid = (long long)num_sms() * bps;
   if (grid > ntiles) grid = ntiles;
