@@ -709,7 +709,7 @@ def bench_prefill(device, hbm_peak: float, reps: int = 5) -> dict:
             "packed_weight_bytes": int(pbytes1 + pbytes2),
             "packed_weight_gbs_fc1": round(pbytes1 / (st_km["fc1_gemm"] * 1e-6) / 1e9, 1),
             "kernels": "route_topk + maps, gather_rows, fp4_grouped_gemm_kernel x2 (tcgen05.mma bf16 with the FP4 "
-                       "weights decoded in shared memory, TMEM accumulators, clusters of 4 sharing activation rows "
+                       "weights decoded in shared memory, TMEM accumulators, clusters of 2 sharing activation rows "
                        "by multicast tensor copies), unpermute; scales as stored add transpose_bytes x2; the "
                        "predequantised call runs grouped_gemm_tc_kernel x2 instead of the fused GEMMs"}
 

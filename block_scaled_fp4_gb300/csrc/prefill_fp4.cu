@@ -19,15 +19,15 @@
 // even split in multiples of 16: the MMA's N follows the expert's row count,
 // so an expert with 130 rows costs 144 columns, not two 128-row tiles.
 //
-// Clusters of four CTAs (one per SM) take cluster tiles round-robin: a
-// cluster tile is one row chunk and four consecutive column blocks, one per
-// CTA, so the four CTAs need the same activation rows.  Roles in a CTA:
+// Clusters of two CTAs (one per SM) take cluster tiles round-robin: a
+// cluster tile is one row chunk and two consecutive column blocks, one per
+// CTA, so the two CTAs need the same activation rows.  Roles in a CTA:
 //  * MMA (one thread): tcgen05.mma kind::f16, M = 128, N = chunk rows,
-//    K = 16, four per 64-deep stage; commits release the decoded stage
-//    locally and the activation stage in all four CTAs (multicast commit);
+//    K = 16, eight per 128-deep stage; commits release the decoded stage
+//    locally and the activation stage in both CTAs (multicast commit);
 //    the next stage's barriers are tested while this stage's MMAs issue;
 //  * activation rows (one thread): 16-row tensor copies in the 128-byte
-//    swizzle, each CTA copying a quarter of a stage's boxes multicast to the
+//    swizzle, each CTA copying half of a stage's boxes multicast to the
 //    cluster, every CTA expecting the whole stage;
 //  * packed codes and k-major scale rows (one warp, cp.async);
 //  * decoders (eight warps): codes x scales -> bf16 M-side tile;
@@ -58,8 +58,9 @@ constexpr int kAccCols = 256;  // tensor-memory columns between the two accumula
 constexpr int kPStages = 4, kBStages = 3, kAStages = 2;
 constexpr int kBoxRows = 16;  // activation rows per tensor copy
 // CTAs of a cluster share one row chunk (consecutive column blocks): each
-// copies a quarter of the activation boxes, multicast to all of them.
-constexpr int kCluster = 4;
+// copies its share of the activation boxes, multicast to all of them.  Pairs
+// measured faster than fours, of which only 36 fit on the device (144 SMs).
+constexpr int kCluster = 2;
 constexpr int kPLag = kPStages - 2;  // packed stages in flight before the copying warp publishes one
 // Warp roles.  Warp w issues from scheduler w % 4, whose instruction cache
 // it shares: the MMA warp's scheduler also runs only the two copy loops and
