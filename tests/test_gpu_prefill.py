@@ -47,6 +47,7 @@ SMALL = [
     syn.small("pf_chunks", T=700, E=4, k=2, H=128, I=128),                  # > 256 rows per expert: split into chunks
     syn.small("pf_sparse", T=9, E=64, k=8, H=128, I=64),                    # 72 rows over 64 experts: most empty
     syn.small("pf_mx_chunks", T=520, E=2, k=1, H=192, I=192, fmt=1),        # MXFP4, 260 rows each, H % 128 = 64
+    syn.small("pf_min_dims", T=40, E=4, k=2, H=64, I=64),                    # one 64-deep stage, half a column tile
 ]
 
 
