@@ -29,6 +29,20 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
 // same expert), per-warp per-expert counts go to shared memory, then each
 // expert's count is prefixed over warps (segment order = expanded order, so
 // the rank is stable), then over experts.
+// Lanes of the warp whose key equals this lane's: one ballot for validity and
+// one per key bit (keys < 2^nbits), ANDed.  An invalid lane matches only
+// itself.  Same result as __match_any_sync over the valid keys, without the
+// match instruction's long, throughput-bound latency.
+__device__ __forceinline__ unsigned match_key(int key, bool valid, int nbits) {
+  unsigned m = __ballot_sync(0xFFFFFFFFu, valid);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (key >> b) & 1;
+    const unsigned bb = __ballot_sync(0xFFFFFFFFu, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return valid ? m : (1u << lane_id());
+}
+
 __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, int32_t *p2e, int32_t *e2p,
                            int32_t *cnt /* smem [W][E] */, int32_t *tot /* smem [E+1] */) {
   const int W = blockDim.x >> 5, w = (int)(threadIdx.x >> 5), lane = (int)lane_id();
@@ -41,6 +55,8 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
   // latency), then ranked round by round
   constexpr int kNB = 8;
   const unsigned lt = (1u << lane) - 1u;
+  int nbits = 0;  // bits of the largest expert index
+  while ((1 << nbits) < E) ++nbits;
   for (int base = lo; base < hi; base += 32 * kNB) {
     int eid[kNB];
 #pragma unroll
@@ -52,8 +68,8 @@ __device__ void build_maps(const int32_t *ids, int R, int E, int32_t *offsets, i
     for (int j = 0; j < kNB; ++j) {
       const int i = base + 32 * j + lane;
       const bool valid = i < hi && eid[j] >= 0 && eid[j] < E;
-      const int e = valid ? eid[j] : -1 - lane;  // invalid lanes never match anyone
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      const int e = valid ? eid[j] : 0;
+      const unsigned peers = match_key(e, valid, nbits);  // invalid lanes match only themselves
       if (valid) e2p[i] = mycnt[e] + __popc(peers & lt);  // rank within this warp's segment
       __syncwarp();
       if (valid && (peers & lt) == 0u) mycnt[e] += __popc(peers);
