@@ -11,11 +11,11 @@
 //    the 128-byte swizzle.  The value written is the exact product
 //    e2m1 * block scale (at most 6 significant bits, so exact in bf16); the
 //    expert's global scale multiplies the fp32 accumulator in the epilogue;
-//  * N side ("B") = the expert's token rows p in expert order, 16..192 of
+//  * N side ("B") = the expert's token rows p in expert order, 16..160 of
 //    them (one row chunk of one expert);
 //  * fp32 accumulator in tensor memory, double-buffered (2 x 256 columns) so
 //    that one tile's epilogue overlaps the next tile's MMAs.
-// A row chunk is all of an expert's rows when they number <= 192, else an
+// A row chunk is all of an expert's rows when they number <= 160, else an
 // even split in multiples of 16: the MMA's N follows the expert's row count,
 // so an expert with 130 rows costs 144 columns, not two 128-row tiles.
 //
