@@ -1,19 +1,21 @@
-// Prefill path of the FP4 MoE layer (more than 64 expanded rows): the expert
-// weights are dequantised to bf16 ("[CUDA] Coalesce QMoE MXFP4/NVFP4 weight
-// dequantization", PR #31349; "MoE and QMoE - CUDA Operator Documentation"
-// §4.3, §9b.1), then two grouped GEMMs run on the tensor cores and a last
-// kernel forms the weighted sum over each token's experts (§1 pipeline:
-// GEMM1 -> activation -> GEMM2 -> un-permute -> weighted sum).
+// Prefill path of the FP4 MoE layer (more than 64 expanded rows), after the
+// routing ("MoE and QMoE - CUDA Operator Documentation" §1 pipeline: GEMM1 ->
+// activation -> GEMM2 -> un-permute -> weighted sum):
+//  * gather_rows_kernel puts the token rows in expert order for FC1;
+//  * per FC, the fused W4A16 grouped GEMM of prefill_fp4.cu over the packed
+//    weights, or -- when the caller gives bf16 weights dequantised by
+//    qmoe_fp4_dequant ("[CUDA] Coalesce QMoE MXFP4/NVFP4 weight
+//    dequantization", PR #31349; §4.3, §9b.1) -- grouped_gemm_tc_kernel below;
+//  * unpermute_kernel forms the weighted sum over each token's experts.
 //
-// Grouped GEMM: bf16 operands, fp32 accumulation on the 5th-generation tensor
-// cores (tcgen05.mma, accumulator in tensor memory); the rows of every expert
-// are contiguous in expert order (the permute maps) and a CTA computes a
-// 128-row x 128-column tile of one expert, the tiles of all experts numbered
-// expert by expert.  GEMM1's left operand is gathered on the fly (permuted
-// row p reads token perm_to_expanded[p] / k of x: no expanded copy of the
-// activations) and its epilogue applies SwiGLU to the adjacent (gate,
-// linear) columns of a row, writing a = bf16(SwiGLU) [R, I]; GEMM2 writes
-// y (fp32) [R, H].
+// grouped_gemm_tc_kernel: bf16 operands, fp32 accumulation on the
+// 5th-generation tensor cores (tcgen05.mma, accumulator in tensor memory);
+// the rows of every expert are contiguous in expert order (the permute maps)
+// and a CTA computes a 128-row x 128-column tile of one expert, the tiles of
+// all experts numbered expert by expert.  GEMM1's left operand is gathered
+// on the fly (permuted row p reads token perm_to_expanded[p] / k of x) and
+// its epilogue applies SwiGLU to the (gate, linear) columns of a row,
+// writing a = bf16(SwiGLU) [R, I]; GEMM2 writes y (fp32) [R, H].
 #include <atomic>
 
 #include "qmoe_common.cuh"
