@@ -178,7 +178,8 @@ qmoe_status qmoe_route_topk(const float *logits, const float *router_weights, in
  *                without runs the fused W4A16 GEMM over fc*_w / fc*_s, and
  *                with block scales as stored ([E, N, K/bs]) its scales are
  *                first rewritten k-major into the workspace, E * N * K / bs
- *                bytes more.)
+ *                bytes more.  The fused FC1 also keeps x in expert order in
+ *                the workspace, T * k * H bf16 values.)
  *   fmt          QMOE_NVFP4 or QMOE_MXFP4, optionally | QMOE_SCALES_KMAJOR
  *                (both FCs' block scales in the k-major layout).  The result
  *                does not depend on the layout beyond the order of the fp32
